@@ -1,0 +1,38 @@
+"""Small seeded batches shared by the oracle pins and the GPU parity tests.
+
+They are scaled-down versions of the five workloads: the oracle finishes each in well under a
+second, yet they span several key blocks, several 512-token partitions, ragged prefill chunks
+(query lengths that are not multiples of any tile), block tails, GQA groups of 1, 2, 4, 7 and 8
+and both block sizes.
+"""
+from paged_kv_cache_290_gb300.workloads import SeqSpec, build_batch
+
+
+def small_decode(d=128, bs=16, hq=32, hkv=8, seed=9100, lens=(1, 15, 16, 17, 300, 511, 512, 513,
+                                                                 1029, 1600)):
+    return build_batch(f"small_decode_d{d}_bs{bs}_g{hq // hkv}", [SeqSpec(L, 1) for L in lens],
+                       num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                       seed_base=seed)
+
+
+def small_mixed(d=128, bs=16, hq=32, hkv=8, seed=9200):
+    seqs = [
+        SeqSpec(70, 40),      # chunk over a 30-token context, ragged
+        SeqSpec(1, 1),        # first token of a sequence
+        SeqSpec(533, 1),      # decode over two partitions
+        SeqSpec(150, 17),     # short ragged chunk
+        SeqSpec(64, 64),      # whole prompt, no context (plain causal)
+        SeqSpec(5, 0),        # idle sequence in the batch: no rows
+        SeqSpec(700, 129),    # chunk whose keys cross a partition boundary
+        SeqSpec(48, 1),
+    ]
+    return build_batch(f"small_mixed_d{d}_bs{bs}_g{hq // hkv}", seqs, num_q_heads=hq,
+                       num_kv_heads=hkv, head_dim=d, block_size=bs, seed_base=seed,
+                       num_pad_slots=3)
+
+
+def small_prefix(seed=9300, n=6, prefix=64, d=128, bs=16):
+    lens = [prefix + 1 + 37 * i for i in range(n)]
+    return build_batch("small_prefix", [SeqSpec(L, 1) for L in lens], num_q_heads=28,
+                       num_kv_heads=4, head_dim=d, block_size=bs, seed_base=seed,
+                       shared_prefix_len=prefix)
