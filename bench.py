@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-attention hot path on one GB300 (or N independent replicas).
+
+One step = one serving step of the path: ``pa_reshape_and_cache`` writes this step's new K/V
+tokens into the paged pool, then ``pa_attention`` runs the block-table-indirected attention
+(decode partitions, chunked-prefill tiles when the batch has them, and the log-sum-exp merge).
+The default workload is the 32 x 8k Llama-3-70B-shaped decode step (one layer): 32 sequences
+of 8192 keys, 64 query / 8 KV heads, head_dim 128, block size 16, blocks randomly placed.
+
+Prints ONE JSON line.  ``value`` is the effective KV bandwidth: algorithmic bytes of the step
+(K/V of every attended token of every sequence, Q, output, used block-table entries and the
+batch descriptor, plus the new tokens read and written by the scatter) / device time of the
+step.  L2 is flushed (a 512 MiB write) before every timed step, outside the timed events.
+
+``--impl reference`` times the fp64 CPU oracle on this machine's host cores instead (a bounded
+sample of the same workload per step); there is no GPU reference implementation.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-attention KV GB/s and % of HBM roofline; decode tok/s per layer"
+DEFAULT_WORKLOAD = "llama70b_32x8k_decode"
+FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------------------------ bookkeeping
+
+def algorithmic_bytes(b) -> dict:
+    """Bytes the step must move at minimum.  K/V are counted per attended token of every
+    sequence ("logical"); "unique" counts each physical (block, offset) slot once, which is what
+    the roofline of an aliased-prefix batch is measured against."""
+    hkv, d, bs = b.num_kv_heads, b.head_dim, b.block_size
+    row_kv = hkv * d * 2 * 2  # K and V of one token, all kv heads, fp16
+    lens = np.array([s.seq_len for s in b.seqs], dtype=np.int64)
+    qlens = np.array([s.query_len for s in b.seqs], dtype=np.int64)
+    active = qlens > 0
+    kv_logical = int(lens[active].sum()) * row_kv
+    slots = []
+    bt = b.block_tables.numpy().astype(np.int64)
+    for s in np.nonzero(active)[0]:
+        pos = np.arange(lens[s])
+        slots.append(bt[s, pos // bs] * bs + pos % bs)
+    kv_unique = (np.unique(np.concatenate(slots)).size if slots else 0) * row_kv
+    t = b.num_tokens
+    q_bytes = t * b.num_q_heads * d * 2
+    out_bytes = q_bytes
+    table = int(((lens[active] + bs - 1) // bs).sum()) * 4
+    desc = b.num_seqs * 4 + (b.num_seqs + 1) * 4
+    t_new = int(b.k_new.shape[0])
+    cache = 2 * t_new * hkv * d * 2 * 2 + t_new * 8
+    attn = q_bytes + out_bytes + table + desc
+    return {
+        "kv_logical": kv_logical, "kv_unique": kv_unique,
+        "attention_logical": kv_logical + attn, "attention_unique": kv_unique + attn,
+        "reshape_and_cache": cache,
+        "step_logical": kv_logical + attn + cache,
+        "decode_rows": int((qlens == 1).sum()),
+        "flops": int(sum(4 * b.num_q_heads * d * (s.seq_len * s.query_len -
+                                                   s.query_len * (s.query_len - 1) // 2)
+                         for s in b.seqs)),
+    }
+
+
+def launches_per_step(b) -> int:
+    parts = max(1, math.ceil(b.max_seq_len / 512))
+    n = 1 if b.k_new.shape[0] > 0 else 0        # reshape_and_cache
+    n += 1                                        # decode partitions
+    n += 1 if b.max_query_len > 1 else 0          # chunked-prefill tiles
+    n += 1 if parts > 1 else 0                    # log-sum-exp merge
+    return n
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    """Max of a per-rank scalar over all ranks (identity when world == 1)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    return 6800.0, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str, interval_ms: int = 20):
+        self.uuid = uuid
+        self.interval_ms = interval_ms
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.interval_ms)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.6)  # let nvidia-smi start sampling before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            u = f[0]
+            if self.uuid and self.uuid not in u and u not in self.uuid:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ our arm
+
+def run_ours(args, world, rank, local):
+    import paged_kv_cache_290_gb300 as pa
+    from paged_kv_cache_290_gb300 import build as pa_build
+    from paged_kv_cache_290_gb300 import workloads as W
+
+    if rank == 0 or not os.path.exists(pa_build.LIB):
+        pa_build.build()
+    barrier(world)
+    pa.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    b = W.WORKLOADS[args.workload](keep_contiguous=False, keep_pre=False)
+    nbytes = algorithmic_bytes(b)
+    stream = torch.cuda.current_stream()
+
+    # device-resident inputs (the pool already holds every token; the scatter rewrites the new
+    # tokens' slots with the same values, exactly as a serving step would write them)
+    q = b.q.to(dev)
+    k_new, v_new, slots = b.k_new.to(dev), b.v_new.to(dev), b.slot_mapping.to(dev)
+    kc, vc = b.k_cache.to(dev), b.v_cache.to(dev)
+    bt, sl, qsl = b.block_tables.to(dev), b.seq_lens.to(dev), b.query_start_loc.to(dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(1, pa.workspace_size(b.num_tokens, b.num_q_heads, b.head_dim,
+                                              b.max_seq_len)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(q_, k_, v_, s_, bt_, sl_, qsl_, out_):
+        pa.reshape_and_cache(k_, v_, kc, vc, s_)
+        pa.attention(q_, kc, vc, bt_, sl_, qsl_, b.scale, out_, b.max_query_len, b.max_seq_len,
+                     workspace=ws)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 255)
+        step(q, k_new, v_new, slots, bt, sl, qsl, out)
+    torch.cuda.synchronize()
+    st, bits = pa.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error after warm-up: status {st} bits {bits}")
+
+    # -------- device-resident timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", ""))
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 255)
+        s0, s1, k0, k1 = ev[i]
+        pa.set_timing_events(k0, k1)
+        s0.record(stream)
+        step(q, k_new, v_new, slots, bt, sl, qsl, out)
+        s1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    pa.set_timing_events(None, None)
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(c) for a, c, _, _ in ev]
+    kern_ms = [k0.elapsed_time(k1) for _, _, k0, k1 in ev]
+    st, bits = pa.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error in timed region: status {st} bits {bits}")
+    ms = statistics.mean(step_ms)
+    ms_max = reduce_max(ms, world)
+    kern_mean = statistics.mean(kern_ms)
+
+    # -------- end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq_ = b.q.pin_memory()
+        hk, hv, hs = b.k_new.pin_memory(), b.v_new.pin_memory(), b.slot_mapping.pin_memory()
+        hbt, hsl, hqsl = (b.block_tables.pin_memory(), b.seq_lens.pin_memory(),
+                          b.query_start_loc.pin_memory())
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq, dk, dv, ds = (torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new),
+                          torch.empty_like(slots))
+        dbt, dsl, dqsl = torch.empty_like(bt), torch.empty_like(sl), torch.empty_like(qsl)
+        h2d = sum(x.numel() * x.element_size() for x in (hq_, hk, hv, hs, hbt, hsl, hqsl))
+        d2h = hout.numel() * hout.element_size()
+        n_e2e = max(3, min(args.steps, 100))
+        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_e2e)]
+        for i in range(n_e2e + 2):
+            flush.fill_(i & 255)
+            if i >= 2:
+                eev[i - 2][0].record(stream)
+            for d_, h_ in ((dq, hq_), (dk, hk), (dv, hv), (ds, hs), (dbt, hbt), (dsl, hsl),
+                           (dqsl, hqsl)):
+                d_.copy_(h_, non_blocking=True)
+            step(dq, dk, dv, ds, dbt, dsl, dqsl, out)
+            hout.copy_(out, non_blocking=True)
+            if i >= 2:
+                eev[i - 2][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(statistics.mean(a.elapsed_time(c) for a, c in eev), world)
+        assert torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16))
+        e2e = {"value": world * nbytes["step_logical"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": n_e2e}
+
+    peak, peak_src = load_peaks()
+    achieved = nbytes["attention_unique"] / (kern_mean * 1e-3) / 1e9
+    value = world * nbytes["step_logical"] / (ms_max * 1e-3) / 1e9
+    tok_s = world * nbytes["decode_rows"] / (ms_max * 1e-3)
+    result = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs": b.num_seqs,
+                   "max_seq_len": b.max_seq_len, "max_query_len": b.max_query_len,
+                   "num_tokens": b.num_tokens, "num_q_heads": b.num_q_heads,
+                   "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
+                   "block_size": b.block_size, "num_blocks": b.num_blocks,
+                   "partition_tokens": 512, "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every timed step (512 MiB write, outside the events)"},
+        "decode_tok_s_per_layer": tok_s,
+        "hbm_roofline_frac_step": (nbytes["step_logical"] / (ms * 1e-3) / 1e9) / peak,
+        "bytes": nbytes,
+        "roofline": {"kernel": "decode_partition_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_src, "traffic": None,
+                     "ms_per_launch": kern_mean,
+                     "bytes_per_launch": nbytes["attention_unique"]},
+        "gpu_launches": launches_per_step(b) * args.steps,
+        "wall_ms_per_step": wall * 1e3 / args.steps,
+        "clocks": clk,
+        "impl": "ours",
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(b, nbytes, budget_s=args.cpu_seconds)
+    traffic = load_traffic(args.workload)
+    if traffic is not None:
+        result["roofline"]["traffic"] = traffic
+    return result
+
+
+def load_traffic(workload):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    data = json.load(open(path))
+    entry = data.get(workload)
+    return entry.get("dram_bytes_per_launch") if entry else None
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+def _sub_batch(b, seqs):
+    """The same pool restricted to some sequences (for bounded oracle samples)."""
+    idx = torch.tensor(seqs, dtype=torch.int64)
+    qlens = torch.tensor([b.seqs[i].query_len for i in seqs], dtype=torch.int64)
+    qsl = torch.zeros(len(seqs) + 1, dtype=torch.int32)
+    qsl[1:] = torch.cumsum(qlens, 0).to(torch.int32)
+    rows = torch.cat([torch.arange(int(b.query_start_loc[i]), int(b.query_start_loc[i + 1]))
+                      for i in seqs])
+    return (b.q[rows], b.block_tables[idx], b.seq_lens[idx], qsl, rows)
+
+
+def _oracle_sample_seconds(b, seqs):
+    import oracle
+    q, bt, sl, qsl, rows = _sub_batch(b, seqs)
+    t0 = time.perf_counter()
+    oracle.attention(q, b.k_cache, b.v_cache, bt, sl, qsl, b.scale)
+    return time.perf_counter() - t0
+
+
+def _sample_bytes(b, seqs):
+    hkv, d, bs = b.num_kv_heads, b.head_dim, b.block_size
+    tot = 0
+    for i in seqs:
+        s = b.seqs[i]
+        tot += s.seq_len * hkv * d * 4 + 2 * s.query_len * b.num_q_heads * d * 2
+        tot += ((s.seq_len + bs - 1) // bs) * 4 + 8
+    return tot
+
+
+def cpu_baseline(b, nbytes, budget_s=12.0):
+    """The fp64 oracle, as it stands, on this host's cores: a bounded, seeded sample of the
+    workload's sequences, timed 3 times (median); value in the benchmark's unit (GB/s)."""
+    import oracle
+    oracle.build()
+    threads = oracle.get_threads()
+    g = torch.Generator().manual_seed(7)
+    order = torch.randperm(b.num_seqs, generator=g).tolist()
+    order = [i for i in order if b.seqs[i].query_len > 0]
+    probe = order[:1]
+    t1 = _oracle_sample_seconds(b, probe)
+    per = t1 / max(1, len(probe))
+    n = max(1, min(len(order), int((budget_s / 3) / max(per, 1e-6))))
+    seqs = order[:n]
+    times = [_oracle_sample_seconds(b, seqs) for _ in range(3)]
+    t = statistics.median(times)
+    sb = _sample_bytes(b, seqs)
+    return {"value": sb / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"attention of {len(seqs)} of {b.num_seqs} sequences (all their query rows "
+                      f"and heads; the scatter-write's copy is left out), fp64 C oracle with "
+                      f"OpenMP, median of 3 runs of {t:.2f} s",
+            "seconds": t}
+
+
+def run_reference(args, world, rank):
+    """The oracle timed as the reference arm: each step = the oracle on one bounded sample."""
+    if rank != 0:
+        return None
+    import oracle
+    from paged_kv_cache_290_gb300 import workloads as W
+    oracle.build()
+    b = W.WORKLOADS[args.workload](keep_contiguous=False, keep_pre=False)
+    threads = oracle.get_threads()
+    g = torch.Generator().manual_seed(11)
+    order = [i for i in torch.randperm(b.num_seqs, generator=g).tolist()
+             if b.seqs[i].query_len > 0]
+    # one sequence per step, cycling through the batch; keeps the default run within minutes
+    for i in range(args.warmup):
+        _oracle_sample_seconds(b, [order[i % len(order)]])
+    times, bytes_ = [], []
+    for i in range(args.steps):
+        seqs = [order[i % len(order)]]
+        times.append(_oracle_sample_seconds(b, seqs))
+        bytes_.append(_sample_bytes(b, seqs))
+    total_t = sum(times)
+    value = sum(bytes_) / total_t / 1e9
+    return {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_t * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs": b.num_seqs,
+                   "max_seq_len": b.max_seq_len, "num_q_heads": b.num_q_heads,
+                   "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
+                   "block_size": b.block_size, "parallelism": "host cores"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "attention of one sequence of the workload per step (all "
+                                   "its rows and heads), cycling through the batch"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        res = run_ours(args, world, rank, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

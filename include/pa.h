@@ -1,0 +1,166 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged-attention library.
+ *
+ * The library computes attention for decode and chunked-prefill queries over a KV cache stored
+ * in fixed-size physical blocks reached through a per-sequence block table, with grouped-query
+ * heads and prefix blocks that may be aliased across sequences:
+ *   - "Local_LLM_03_vLLM_Architecture", paged-KV slide: fixed-size blocks (16 tokens by
+ *     default), a per-sequence block table from logical positions to physical blocks, and an
+ *     attention kernel that gathers K/V from the scattered blocks; block-size slide: the block
+ *     size is a knob; KV-sizing slide: GQA-8; chunked-prefill slide: prefills cut into chunks
+ *     and interleaved with decodes.
+ *   - "vLLM: LLM Inference That Doesn't Waste Your GPU", sections "KV cache, in one picture"
+ *     (every processed token's K/V is stored once and reused), "Continuous batching" (prefill and
+ *     decode mixed in one step) and "PagedAttention: virtual memory for KV".
+ *   - "Scaling inference with vLLM": requests with the same start share physical pages.
+ *
+ * Conventions (the pages fix none of them):
+ *   - Every pointer in a pa_tensor is a DEVICE pointer of the current CUDA device.  The library
+ *     owns no buffer and allocates no device memory; the caller owns everything, including
+ *     the attention workspace.
+ *   - Strides are in elements.  The innermost dimension must be contiguous (stride 1).
+ *   - fp16 is IEEE binary16.  Accumulation is fp32; outputs are rounded to nearest-even.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream), like a
+ *     kernel launch.  Nothing synchronises except pa_get_device_error.
+ *   - Host-checkable errors are returned synchronously and nothing is launched.  Device-data
+ *     errors (a slot or block id outside the pool, query_len > seq_len, a sequence longer than
+ *     the hint) make the affected work item skip its memory accesses, set a bit in a device
+ *     error word and leave its output rows unwritten; pa_get_device_error reports them.
+ *   - Every wait inside a kernel gives up after two seconds and reports PA_ERR_TIMEOUT.
+ *   - Thread-safety: functions may be called from several host threads; pa_last_error is
+ *     per thread.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_VERSION 1
+#define PA_PARTITION_TOKENS 512 /* keys per split-context partition */
+#define PA_MAX_DIMS 5
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* bad pointer, dtype, rank, shape, stride or alignment */
+  PA_ERR_UNSUPPORTED = 2, /* well-formed but not built: head_dim, block_size, group size */
+  PA_ERR_CUDA = 3,        /* CUDA runtime error; pa_last_error() has the message */
+  PA_ERR_TIMEOUT = 4,     /* device: a bounded wait gave up (reported by pa_get_device_error) */
+  PA_ERR_OUT_OF_RANGE = 5,/* device: slot or block id outside the pool; access skipped */
+  PA_ERR_WORKSPACE = 6,   /* workspace missing, misaligned or smaller than required */
+  PA_ERR_DESCRIPTOR = 7   /* device: query_len > seq_len, short block table, or hint exceeded */
+} pa_status;
+
+typedef enum pa_dtype { PA_F16 = 0, PA_I32 = 1, PA_I64 = 2 } pa_dtype;
+
+typedef struct pa_tensor {
+  void* data;                 /* device pointer, 16-byte aligned for fp16 tensors */
+  int32_t dtype;              /* pa_dtype */
+  int32_t ndim;
+  int64_t shape[PA_MAX_DIMS];
+  int64_t stride[PA_MAX_DIMS];/* in elements */
+} pa_tensor;
+
+/* Host-side facts about the batch the scheduler already knows.  Upper bounds are fine; a
+ * sequence that exceeds them is skipped on the device and reported as PA_ERR_DESCRIPTOR. */
+typedef struct pa_batch_hint {
+  int32_t max_query_len; /* max over sequences of query_start_loc[s+1] - query_start_loc[s] */
+  int32_t max_seq_len;   /* max over sequences of seq_lens[s] */
+} pa_batch_hint;
+
+/*
+ * pa_reshape_and_cache -- write this step's new K/V tokens into their cache slots.
+ * ("vLLM: LLM Inference That Doesn't Waste Your GPU", "KV cache, in one picture": the K/V of every
+ * processed token is stored once; "Local_LLM_03_vLLM_Architecture", paged-KV slide: the store is a
+ * set of fixed-size blocks.)
+ *
+ *   k, v          fp16 [T_new, Hkv, d]; token stride free (multiple of 8), head stride d.
+ *   k_cache,
+ *   v_cache       fp16 [NB, Hkv, bs, d], contiguous ("HND" per block: one (block, kv head) is a
+ *                 contiguous bs x d tile).  Written in place.
+ *   slot_mapping  int64 [T_new]; token t goes to block slot/bs, offset slot%bs.  slot < 0 means
+ *                 "padding, skip".  A slot >= NB*bs is skipped and reported on the device.
+ * For every t with slot >= 0 and every kv head h: k_cache[slot/bs][h][slot%bs][:] = k[t][h][:]
+ * (bit-exact copy), same for v.  Two tokens with the same slot race (the last writer is
+ * unspecified), as the pages give no order between them.
+ * Supported: d in {64, 128}, bs in {16, 32}.
+ */
+int pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_tensor* k_cache,
+                         const pa_tensor* v_cache, const pa_tensor* slot_mapping, void* stream);
+
+/*
+ * pa_attention_workspace_size -- bytes of scratch pa_attention needs for a batch.
+ * Split-context partials: for T query rows, Hq heads and P = ceil(max_seq_len / 512)
+ * partitions, fp32 o[T][Hq][P][d] plus fp32 m[T][Hq][P] and l[T][Hq][P].  0 when P <= 1.
+ */
+size_t pa_attention_workspace_size(int64_t num_tokens, int64_t num_q_heads, int64_t head_dim,
+                                   int32_t max_seq_len);
+
+/*
+ * pa_attention -- paged attention for one mixed continuous-batching step.
+ * ("Local_LLM_03_vLLM_Architecture", paged-KV slide: the kernel gathers K/V from scattered
+ * physical blocks through the block table; chunked-prefill slide; "vLLM: LLM Inference That
+ * Doesn't Waste Your GPU", "Continuous batching": prefill and decode in the same step.)
+ *
+ *   q                fp16 [T, Hq, d]; token stride free (multiple of 8), head stride d.
+ *   k_cache, v_cache fp16 [NB, Hkv, bs, d] contiguous, already holding this step's tokens
+ *                    (call pa_reshape_and_cache first, on the same stream).
+ *   block_tables     int32 [N, MB]; row stride free.  Entry j of row s = physical block of
+ *                    logical positions j*bs .. j*bs+bs-1 of sequence s.  Entries past
+ *                    ceil(seq_lens[s]/bs) are never read.  Aliasing (the same block id in
+ *                    several rows) is allowed and is how shared prefixes are expressed.
+ *   seq_lens         int32 [N]; keys of sequence s after this step's tokens were written.
+ *   query_start_loc  int32 [N+1]; query_start_loc[0] = 0, non-decreasing, [N] = T.  Sequence s
+ *                    owns rows query_start_loc[s] .. query_start_loc[s+1]-1.  One row is a
+ *                    decode step, several a prefill chunk; any mix and order in one call.
+ *   scale            multiplies q.k before the softmax (typically 1/sqrt(d)).
+ *   out              fp16 [T, Hq, d] contiguous.
+ *   hint             required; see pa_batch_hint.
+ *   workspace        device scratch of at least pa_attention_workspace_size(T, Hq, d,
+ *                    hint->max_seq_len) bytes, 256-byte aligned (NULL allowed when that is 0).
+ *                    Owned by the caller; must not be shared by calls in flight at once.
+ * Row i of sequence s sits at absolute position seq_lens[s] - q_len + i and attends to keys
+ * 0 .. seq_lens[s] - q_len + i (bottom-right causal; q_len = 1 attends to all keys).  Query
+ * head h reads kv head h / (Hq / Hkv).  out = softmax(scale * q K^T) V per row and head.
+ * Rows with q_len = 1 and more than 512 keys are computed in 512-key partitions merged with
+ * the log-sum-exp rule.
+ * Supported: d in {64, 128}, bs in {16, 32}, Hq / Hkv in 1..16.
+ */
+int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                 const pa_tensor* block_tables, const pa_tensor* seq_lens,
+                 const pa_tensor* query_start_loc, float scale, const pa_tensor* out,
+                 const pa_batch_hint* hint, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+const char* pa_last_error(void);
+
+/*
+ * pa_get_device_error -- synchronise `stream`, then read and clear the device error word of
+ * the current device.  Returns PA_OK, PA_ERR_TIMEOUT, PA_ERR_OUT_OF_RANGE or PA_ERR_DESCRIPTOR
+ * (most severe first); *bits (may be NULL) receives the raw word: 1 timeout, 2 slot out of
+ * range, 4 block id out of range, 8 descriptor, 16 hint exceeded.
+ */
+int pa_get_device_error(void* stream, uint32_t* bits);
+
+/*
+ * pa_set_timing_events -- measurement hook.  When both are non-NULL (cudaEvent_t handles),
+ * every later pa_attention call on this host thread records `start` on its stream just before
+ * launching the decode-partition kernel and `stop` just after it, so a caller can time that
+ * kernel with CUDA events inside a longer step.  No work is skipped or reordered.  Pass NULL,
+ * NULL to turn it off.  Returns PA_OK.
+ */
+int pa_set_timing_events(void* start, void* stop);
+
+/* PA_VERSION of the built library. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,207 @@
+"""Thin ctypes binding over the C ABI in ``include/pa.h`` (argument marshalling only).
+
+Every computation runs in the sm_103a kernels of ``libpa_gb300.so``; this module turns torch
+tensors into ``pa_tensor`` descriptors, passes the current CUDA stream and raises on a non-OK
+status.  There is no fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpa_gb300.so")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_CUDA = 3
+PA_ERR_TIMEOUT = 4
+PA_ERR_OUT_OF_RANGE = 5
+PA_ERR_WORKSPACE = 6
+PA_ERR_DESCRIPTOR = 7
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
+                4: "PA_ERR_TIMEOUT", 5: "PA_ERR_OUT_OF_RANGE", 6: "PA_ERR_WORKSPACE",
+                7: "PA_ERR_DESCRIPTOR"}
+PA_F16, PA_I32, PA_I64 = 0, 1, 2
+PARTITION_TOKENS = 512
+EXPORTED = ("pa_reshape_and_cache", "pa_attention_workspace_size", "pa_attention",
+            "pa_last_error", "pa_get_device_error", "pa_set_timing_events", "pa_version")
+
+_DTYPES = {torch.float16: PA_F16, torch.int32: PA_I32, torch.int64: PA_I64}
+
+
+class PATensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 5), ("stride", ctypes.c_int64 * 5)]
+
+
+class PABatchHint(ctypes.Structure):
+    _fields_ = [("max_query_len", ctypes.c_int32), ("max_seq_len", ctypes.c_int32)]
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load (once) the CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m paged_kv_cache_290_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(path)
+        P = ctypes.POINTER(PATensor)
+        lib.pa_reshape_and_cache.restype = ctypes.c_int
+        lib.pa_reshape_and_cache.argtypes = [P, P, P, P, P, ctypes.c_void_p]
+        lib.pa_attention_workspace_size.restype = ctypes.c_size_t
+        lib.pa_attention_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int64,
+                                                    ctypes.c_int64, ctypes.c_int32]
+        lib.pa_attention.restype = ctypes.c_int
+        lib.pa_attention.argtypes = [P, P, P, P, P, P, ctypes.c_float, P,
+                                     ctypes.POINTER(PABatchHint), ctypes.c_void_p, ctypes.c_size_t,
+                                     ctypes.c_void_p]
+        lib.pa_last_error.restype = ctypes.c_char_p
+        lib.pa_get_device_error.restype = ctypes.c_int
+        lib.pa_get_device_error.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+        lib.pa_version.restype = ctypes.c_int
+        lib.pa_set_timing_events.restype = ctypes.c_int
+        lib.pa_set_timing_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        _lib = lib
+    return _lib
+
+
+def describe(t: torch.Tensor) -> PATensor:
+    """pa_tensor view of a torch tensor (no copy; strides in elements)."""
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() > 5:
+        raise ValueError("rank above 5")
+    d = PATensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(status: int) -> None:
+    if status != PA_OK:
+        msg = load_library().pa_last_error()
+        raise PAError(status, msg.decode() if msg else "")
+
+
+def last_error() -> str:
+    return load_library().pa_last_error().decode()
+
+
+def version() -> int:
+    return load_library().pa_version()
+
+
+def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None) -> None:
+    """``pa_reshape_and_cache``: write new K/V tokens [T, Hkv, d] into pool slots (in place)."""
+    lib = load_library()
+    args = [ctypes.byref(describe(x)) for x in (k, v, k_cache, v_cache, slot_mapping)]
+    _check(lib.pa_reshape_and_cache(*args, _stream_handle(stream)))
+
+
+def workspace_size(num_tokens: int, num_q_heads: int, head_dim: int, max_seq_len: int) -> int:
+    return int(load_library().pa_attention_workspace_size(num_tokens, num_q_heads, head_dim,
+                                                          max_seq_len))
+
+
+def attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale: float, out,
+              max_query_len: int, max_seq_len: int, workspace: Optional[torch.Tensor] = None,
+              stream=None) -> torch.Tensor:
+    """``pa_attention`` for one mixed batch; writes ``out`` [T, Hq, d] and returns it.
+
+    ``workspace`` is a caller-owned uint8 device tensor of at least ``workspace_size(...)``
+    bytes (allocated here when omitted)."""
+    lib = load_library()
+    need = workspace_size(q.shape[0], q.shape[1], q.shape[2], max_seq_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wptr = workspace.data_ptr() if workspace is not None and workspace.numel() else None
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    hint = PABatchHint(int(max_query_len), int(max_seq_len))
+    descs = [describe(x) for x in (q, k_cache, v_cache, block_tables, seq_lens, query_start_loc)]
+    _check(lib.pa_attention(*[ctypes.byref(d) for d in descs], ctypes.c_float(scale),
+                            ctypes.byref(describe(out)), ctypes.byref(hint), wptr, wbytes,
+                            _stream_handle(stream)))
+    return out
+
+
+def set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
+    """Record ``start``/``stop`` around every later decode-partition kernel launch on this
+    thread (``None, None`` turns it off).  Measurement only; no work changes."""
+    lib = load_library()
+    if start is None or stop is None:
+        lib.pa_set_timing_events(None, None)
+    else:
+        lib.pa_set_timing_events(start.cuda_event, stop.cuda_event)
+
+
+def get_device_error(stream=None):
+    """Synchronise the stream and return (status, bits) of the device error word (cleared)."""
+    lib = load_library()
+    bits = ctypes.c_uint32(0)
+    st = lib.pa_get_device_error(_stream_handle(stream), ctypes.byref(bits))
+    return st, int(bits.value)
+
+
+@dataclass
+class BatchDescriptor:
+    """The scheduler-facing description of one continuous-batching step, on the device.
+
+    Sequences may mix prefill chunks (several query rows) and decode steps (one row) in any
+    order ("vLLM: LLM Inference That Doesn't Waste Your GPU", "Continuous batching").
+    ``slot_mapping`` addresses the cache slots of this step's new tokens; ``max_query_len`` and
+    ``max_seq_len`` are the host-side hint the launch is planned from.
+    """
+
+    query_start_loc: torch.Tensor
+    seq_lens: torch.Tensor
+    block_tables: torch.Tensor
+    slot_mapping: torch.Tensor
+    max_query_len: int
+    max_seq_len: int
+
+    @classmethod
+    def from_host(cls, seq_lens, query_lens, block_tables, block_size: int, device="cuda",
+                  non_blocking: bool = False) -> "BatchDescriptor":
+        """Build from host lists: ``seq_lens[s]`` keys after the step, ``query_lens[s]`` new
+        rows (the last ones of the sequence), ``block_tables`` int32 [N, MB]."""
+        sl = torch.as_tensor(seq_lens, dtype=torch.int32)
+        ql = torch.as_tensor(query_lens, dtype=torch.int64)
+        if (ql < 0).any() or (ql > sl.to(torch.int64)).any():
+            raise ValueError("need 0 <= query_len <= seq_len")
+        qsl = torch.zeros(len(sl) + 1, dtype=torch.int32)
+        qsl[1:] = torch.cumsum(ql, 0).to(torch.int32)
+        bt = torch.as_tensor(block_tables, dtype=torch.int32)
+        slots = []
+        for s in range(len(sl)):
+            for p in range(int(sl[s]) - int(ql[s]), int(sl[s])):
+                slots.append(int(bt[s, p // block_size]) * block_size + p % block_size)
+        sm = torch.tensor(slots, dtype=torch.int64)
+        dev = lambda x: x.to(device, non_blocking=non_blocking)
+        return cls(dev(qsl), dev(sl), dev(bt), dev(sm), int(ql.max()) if len(ql) else 0,
+                   int(sl.max()) if len(sl) else 0)

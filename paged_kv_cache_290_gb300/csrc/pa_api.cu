@@ -1,0 +1,362 @@
+// C ABI of the paged-attention library: argument checks, launch planning and status codes.
+// See include/pa.h for the contract of every entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "pa.h"
+#include "pa_common.cuh"
+#include "pa_kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local cudaEvent_t g_time_start = nullptr;
+thread_local cudaEvent_t g_time_stop = nullptr;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// The device error word.  Kernels get its device address; pa_get_device_error reads it.
+__device__ unsigned g_device_error_word;
+
+constexpr int kMaxDevices = 256;
+std::mutex g_err_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
+
+// Address of the error word on the current device (looked up once per device).
+cudaError_t device_error_word(unsigned** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error_word);
+    if (e != cudaSuccess) return e;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view of a pool [NB, Hkv, bs, d] as rows of d fp16 values; TMA box = 16 rows x 64 values
+// (128 B) with the 128-byte swizzle the kernels' fragment loads expect.
+int make_pool_map(CUtensorMap* m, void* base, int64_t rows, int d) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
+  return PA_OK;
+}
+
+const char* dtype_name(int dt) {
+  switch (dt) {
+    case PA_F16: return "float16";
+    case PA_I32: return "int32";
+    case PA_I64: return "int64";
+    default: return "unknown";
+  }
+}
+
+// Rank, dtype, non-negative shape, unit innermost stride, non-null data when non-empty.
+int check_tensor(const pa_tensor* t, const char* name, int dtype, int ndim) {
+  if (!t) return fail(PA_ERR_INVALID_ARG, std::string(name) + " is NULL");
+  if (t->ndim != ndim)
+    return fail(PA_ERR_INVALID_ARG, std::string(name) + " must have rank " + std::to_string(ndim) +
+                                        ", got " + std::to_string(t->ndim));
+  if (t->dtype != dtype)
+    return fail(PA_ERR_INVALID_ARG, std::string(name) + " must be " + dtype_name(dtype) + ", got " +
+                                        dtype_name(t->dtype));
+  int64_t numel = 1;
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0) return fail(PA_ERR_INVALID_ARG, std::string(name) + " has a negative dim");
+    if (t->stride[i] < 0) return fail(PA_ERR_INVALID_ARG, std::string(name) + " has a negative stride");
+    numel *= t->shape[i];
+  }
+  if (numel > 0) {
+    if (!t->data) return fail(PA_ERR_INVALID_ARG, std::string(name) + " data is NULL");
+    if (t->shape[ndim - 1] > 1 && t->stride[ndim - 1] != 1)
+      return fail(PA_ERR_INVALID_ARG, std::string(name) + " innermost dim must be contiguous");
+  }
+  return PA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_contiguous(const pa_tensor* t, const char* name) {
+  int64_t expect = 1;
+  for (int i = t->ndim - 1; i >= 0; --i) {
+    if (t->shape[i] > 1 && t->stride[i] != expect)
+      return fail(PA_ERR_INVALID_ARG, std::string(name) + " must be contiguous");
+    expect *= t->shape[i];
+  }
+  return PA_OK;
+}
+
+// Pool [NB, Hkv, bs, d] checks shared by both entry points.
+int check_pool(const pa_tensor* kc, const pa_tensor* vc) {
+  int rc;
+  if ((rc = check_tensor(kc, "k_cache", PA_F16, 4))) return rc;
+  if ((rc = check_tensor(vc, "v_cache", PA_F16, 4))) return rc;
+  for (int i = 0; i < 4; ++i)
+    if (kc->shape[i] != vc->shape[i])
+      return fail(PA_ERR_INVALID_ARG, "k_cache and v_cache shapes differ");
+  if ((rc = check_contiguous(kc, "k_cache"))) return rc;
+  if ((rc = check_contiguous(vc, "v_cache"))) return rc;
+  const int64_t d = kc->shape[3], bs = kc->shape[2];
+  if (d != 64 && d != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim " + std::to_string(d) + " not built (64, 128)");
+  if (bs != 16 && bs != 32)
+    return fail(PA_ERR_UNSUPPORTED, "block_size " + std::to_string(bs) + " not built (16, 32)");
+  if (kc->shape[1] < 1 || kc->shape[1] > 65535)
+    return fail(PA_ERR_INVALID_ARG, "num_kv_heads must be in 1..65535");
+  if (kc->shape[0] * kc->shape[1] * bs >= (int64_t(1) << 31))
+    return fail(PA_ERR_UNSUPPORTED, "pool has 2^31 or more token rows");
+  if (kc->shape[0] > 0 && (!aligned16(kc->data) || !aligned16(vc->data)))
+    return fail(PA_ERR_INVALID_ARG, "k_cache / v_cache must be 16-byte aligned");
+  return PA_OK;
+}
+
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WorkspaceLayout {
+  size_t o_bytes, m_off, l_off, total;
+};
+
+WorkspaceLayout workspace_layout(int64_t t, int64_t hq, int64_t d, int32_t max_seq_len) {
+  WorkspaceLayout w{0, 0, 0, 0};
+  const int64_t parts = max_seq_len > 0 ? (max_seq_len + PA_PARTITION_TOKENS - 1) / PA_PARTITION_TOKENS : 0;
+  if (parts <= 1 || t <= 0) return w;
+  const size_t rows = static_cast<size_t>(t) * hq * parts;
+  w.o_bytes = align_up(rows * d * sizeof(float), 256);
+  w.m_off = w.o_bytes;
+  w.l_off = w.m_off + align_up(rows * sizeof(float), 256);
+  w.total = w.l_off + align_up(rows * sizeof(float), 256);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_last_error(void) { return g_last_error.c_str(); }
+
+int pa_version(void) { return PA_VERSION; }
+
+size_t pa_attention_workspace_size(int64_t num_tokens, int64_t num_q_heads, int64_t head_dim,
+                                   int32_t max_seq_len) {
+  return workspace_layout(num_tokens, num_q_heads, head_dim, max_seq_len).total;
+}
+
+int pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_tensor* k_cache,
+                         const pa_tensor* v_cache, const pa_tensor* slot_mapping, void* stream) {
+  g_last_error.clear();
+  int rc;
+  if ((rc = check_pool(k_cache, v_cache))) return rc;
+  if ((rc = check_tensor(k, "k", PA_F16, 3))) return rc;
+  if ((rc = check_tensor(v, "v", PA_F16, 3))) return rc;
+  if ((rc = check_tensor(slot_mapping, "slot_mapping", PA_I64, 1))) return rc;
+  const int64_t t = k->shape[0], hkv = k_cache->shape[1], d = k_cache->shape[3];
+  for (const pa_tensor* x : {k, v}) {
+    if (x->shape[0] != t || x->shape[1] != hkv || x->shape[2] != d)
+      return fail(PA_ERR_INVALID_ARG, "k and v must be [T_new, num_kv_heads, head_dim] matching the pool");
+    if (t > 0 && ((x->shape[1] > 1 && x->stride[1] != d) || x->stride[0] < hkv * d ||
+                  x->stride[0] % 8 != 0 || !aligned16(x->data)))
+      return fail(PA_ERR_INVALID_ARG,
+                  "k / v need head stride head_dim, token stride >= heads*head_dim and a multiple "
+                  "of 8, and 16-byte alignment");
+  }
+  if (slot_mapping->shape[0] != t)
+    return fail(PA_ERR_INVALID_ARG, "slot_mapping must have T_new entries");
+  if (t == 0) return PA_OK;
+
+  pa::CacheArgs a{};
+  a.k = static_cast<const __half*>(k->data);
+  a.v = static_cast<const __half*>(v->data);
+  a.k_stride = k->stride[0];
+  a.v_stride = v->stride[0];
+  a.k_cache = static_cast<__half*>(k_cache->data);
+  a.v_cache = static_cast<__half*>(v_cache->data);
+  a.slot_mapping = static_cast<const int64_t*>(slot_mapping->data);
+  a.num_tokens = t;
+  a.num_kv_heads = static_cast<int>(hkv);
+  a.head_dim = static_cast<int>(d);
+  a.block_size = static_cast<int>(k_cache->shape[2]);
+  a.num_blocks = k_cache->shape[0];
+  cudaError_t e = device_error_word(&a.err);
+  if (e != cudaSuccess) return cuda_fail(e, "error word");
+  e = pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+  return PA_OK;
+}
+
+int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                 const pa_tensor* block_tables, const pa_tensor* seq_lens,
+                 const pa_tensor* query_start_loc, float scale, const pa_tensor* out,
+                 const pa_batch_hint* hint, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  g_last_error.clear();
+  int rc;
+  if ((rc = check_pool(k_cache, v_cache))) return rc;
+  if ((rc = check_tensor(q, "q", PA_F16, 3))) return rc;
+  if ((rc = check_tensor(out, "out", PA_F16, 3))) return rc;
+  if ((rc = check_tensor(block_tables, "block_tables", PA_I32, 2))) return rc;
+  if ((rc = check_tensor(seq_lens, "seq_lens", PA_I32, 1))) return rc;
+  if ((rc = check_tensor(query_start_loc, "query_start_loc", PA_I32, 1))) return rc;
+  if (!hint) return fail(PA_ERR_INVALID_ARG, "hint is NULL");
+  const int64_t t = q->shape[0], hq = q->shape[1], d = q->shape[2];
+  const int64_t hkv = k_cache->shape[1];
+  const int64_t n = seq_lens->shape[0];
+  if (d != k_cache->shape[3]) return fail(PA_ERR_INVALID_ARG, "q head_dim differs from the pool's");
+  if (hq < 1 || hq % hkv != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+  const int64_t group = hq / hkv;
+  if (group > 16) return fail(PA_ERR_UNSUPPORTED, "GQA group size above 16 not built");
+  if (out->shape[0] != t || out->shape[1] != hq || out->shape[2] != d)
+    return fail(PA_ERR_INVALID_ARG, "out must be [T, num_q_heads, head_dim] like q");
+  if ((rc = check_contiguous(out, "out"))) return rc;
+  if (t > 0 && ((hq > 1 && q->stride[1] != d) || q->stride[0] < hq * d || q->stride[0] % 8 != 0 ||
+                !aligned16(q->data) || !aligned16(out->data)))
+    return fail(PA_ERR_INVALID_ARG,
+                "q needs head stride head_dim, token stride >= heads*head_dim and a multiple of 8; "
+                "q and out need 16-byte alignment");
+  if (query_start_loc->shape[0] != n + 1)
+    return fail(PA_ERR_INVALID_ARG, "query_start_loc must have num_seqs + 1 entries");
+  if (block_tables->shape[0] != n)
+    return fail(PA_ERR_INVALID_ARG, "block_tables must have num_seqs rows");
+  if (n > 65535) return fail(PA_ERR_UNSUPPORTED, "more than 65535 sequences in one call");
+  if (block_tables->shape[1] < 1 && n > 0)
+    return fail(PA_ERR_INVALID_ARG, "block_tables needs at least one column");
+  if (block_tables->shape[1] > INT32_MAX || block_tables->stride[0] < block_tables->shape[1])
+    return fail(PA_ERR_INVALID_ARG, "block_tables row stride must cover its columns");
+  if (hint->max_query_len < 0 || hint->max_seq_len < 0)
+    return fail(PA_ERR_INVALID_ARG, "hint values must be non-negative");
+  if (hint->max_query_len > hint->max_seq_len)
+    return fail(PA_ERR_INVALID_ARG, "hint max_query_len exceeds max_seq_len");
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN");
+  const WorkspaceLayout ws = workspace_layout(t, hq, d, hint->max_seq_len);
+  if (ws.total > 0) {
+    if (!workspace || workspace_bytes < ws.total)
+      return fail(PA_ERR_WORKSPACE, "workspace needs " + std::to_string(ws.total) + " bytes");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(PA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  }
+  if (t == 0 || n == 0 || hint->max_query_len == 0) return PA_OK;
+
+  pa::AttnArgs a{};
+  a.q = static_cast<const __half*>(q->data);
+  a.q_stride = q->stride[0];
+  a.out = static_cast<__half*>(out->data);
+  a.block_tables = static_cast<const int32_t*>(block_tables->data);
+  a.bt_stride = block_tables->stride[0];
+  a.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+  a.query_start_loc = static_cast<const int32_t*>(query_start_loc->data);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  a.part_o = ws.total ? reinterpret_cast<float*>(wsb) : nullptr;
+  a.part_m = ws.total ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+  a.part_l = ws.total ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
+  a.num_seqs = static_cast<int>(n);
+  a.num_tokens = t;
+  a.num_q_heads = static_cast<int>(hq);
+  a.num_kv_heads = static_cast<int>(hkv);
+  a.group = static_cast<int>(group);
+  a.head_dim = static_cast<int>(d);
+  a.block_size = static_cast<int>(k_cache->shape[2]);
+  a.max_blocks = static_cast<int>(block_tables->shape[1]);
+  a.num_blocks = k_cache->shape[0];
+  a.max_parts = static_cast<int>(
+      std::max<int64_t>(1, (hint->max_seq_len + PA_PARTITION_TOKENS - 1) / PA_PARTITION_TOKENS));
+  a.max_query_len = hint->max_query_len;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e = device_error_word(&a.err);
+  if (e != cudaSuccess) return cuda_fail(e, "error word");
+
+  const int64_t rows = k_cache->shape[0] * hkv * k_cache->shape[2];
+  CUtensorMap kmap, vmap;
+  if ((rc = make_pool_map(&kmap, k_cache->data, rows, static_cast<int>(d)))) return rc;
+  if ((rc = make_pool_map(&vmap, v_cache->data, rows, static_cast<int>(d)))) return rc;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool timed = g_time_start && g_time_stop;
+  if (timed && (e = cudaEventRecord(g_time_start, st)) != cudaSuccess)
+    return cuda_fail(e, "timing event");
+  e = pa::launch_decode(a, kmap, vmap, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (timed && (e = cudaEventRecord(g_time_stop, st)) != cudaSuccess)
+    return cuda_fail(e, "timing event");
+  if (hint->max_query_len > 1) {
+    e = pa::launch_prefill(a, kmap, vmap, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  }
+  if (a.max_parts > 1) {
+    e = pa::launch_merge(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
+  return PA_OK;
+}
+
+int pa_set_timing_events(void* start, void* stop) {
+  g_time_start = static_cast<cudaEvent_t>(start);
+  g_time_stop = static_cast<cudaEvent_t>(stop);
+  if (!g_time_start || !g_time_stop) g_time_start = g_time_stop = nullptr;
+  return PA_OK;
+}
+
+int pa_get_device_error(void* stream, uint32_t* bits) {
+  g_last_error.clear();
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  unsigned* p = nullptr;
+  e = device_error_word(&p);
+  if (e != cudaSuccess) return cuda_fail(e, "error word");
+  unsigned w = 0;
+  e = cudaMemcpy(&w, p, sizeof(w), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  const unsigned zero = 0;
+  e = cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  if (bits) *bits = w;
+  if (w & pa::kErrTimeout) return fail(PA_ERR_TIMEOUT, "a device wait timed out");
+  if (w & (pa::kErrSlotRange | pa::kErrBlockRange))
+    return fail(PA_ERR_OUT_OF_RANGE, "a slot or block id outside the pool was skipped");
+  if (w & (pa::kErrDescriptor | pa::kErrHint))
+    return fail(PA_ERR_DESCRIPTOR, "a sequence's descriptor was invalid or exceeded the hint");
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// KV scatter-write: put this step's new K/V tokens into their paged-cache slots.
+//
+// "vLLM: LLM Inference That Doesn't Waste Your GPU", "KV cache, in one picture": each processed
+// token's K/V is stored once and reused by every later token; "Local_LLM_03_vLLM_Architecture",
+// paged-KV slide: that store is a pool of fixed-size blocks.  Token t with slot = blk*bs + off
+// goes to k_cache[blk][h][off][:] for every kv head h (pool layout [NB][Hkv][bs][d]).
+//
+// One thread moves one 16-byte chunk of K and the matching chunk of V; consecutive threads
+// cover consecutive chunks of a (token, head) row, so both the reads and the writes of a row are
+// full 128-byte-line transactions.  Pure copy: the cache receives the exact bit patterns.
+#include "pa_common.cuh"
+#include "pa_kernels.h"
+
+namespace pa {
+namespace {
+
+template <int D>
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheArgs a) {
+  constexpr int kChunks = D / 8;  // 16-byte chunks per (token, head) row
+  const int64_t total = a.num_tokens * a.num_kv_heads * kChunks;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int ch = static_cast<int>(idx % kChunks);
+    const int64_t row = idx / kChunks;
+    const int h = static_cast<int>(row % a.num_kv_heads);
+    const int64_t t = row / a.num_kv_heads;
+    const int64_t slot = a.slot_mapping[t];
+    if (slot < 0) continue;  // padding token
+    if (slot >= a.num_blocks * a.block_size) {
+      atomicOr(a.err, kErrSlotRange);
+      continue;
+    }
+    const int64_t blk = slot / a.block_size;
+    const int64_t off = slot % a.block_size;
+    const int64_t dst = ((blk * a.num_kv_heads + h) * a.block_size + off) * D + ch * 8;
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(a.k + t * a.k_stride + h * D + ch * 8));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(a.v + t * a.v_stride + h * D + ch * 8));
+    *reinterpret_cast<uint4*>(a.k_cache + dst) = kv;
+    *reinterpret_cast<uint4*>(a.v_cache + dst) = vv;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const CacheArgs& a, cudaStream_t stream) {
+  const int64_t total = a.num_tokens * a.num_kv_heads * (a.head_dim / 8);
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 152 * 64 ? want : 152 * 64);
+  if (a.head_dim == 128)
+    reshape_and_cache_kernel<128><<<blocks, threads, 0, stream>>>(a);
+  else
+    reshape_and_cache_kernel<64><<<blocks, threads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,419 @@
+// Decode attention over a paged KV cache: split-context partition kernel + log-sum-exp merge.
+//
+// Work item = one CTA = (sequence s, kv head g, partition p of 512 keys) for every sequence
+// whose step has exactly one query row.  The CTA serves all G query heads of the GQA group
+// from a single read of the group's K/V ("Local_LLM_03_vLLM_Architecture", KV-sizing slide:
+// GQA-8; paged-KV slide: the kernel gathers K/V from scattered physical blocks).
+//
+// Data path per CTA (4 warps, each with a private ring of shared-memory stages):
+//   * the partition's block ids are read from the block table once (block -> TMA row),
+//   * each 16-token unit of K and of V (one or two 128-byte swizzled boxes per token row) is
+//     fetched by a 2-D TMA tensor load that completes on the stage's mbarrier; warp w takes
+//     units w, w+4, w+8, ... so one partition keeps 4 x stages loads in flight per CTA,
+//   * S^T = K Q^T on tensor cores (m16n8k16: 16 tokens x 8 heads x 16 dims), scores scaled by
+//     scale*log2(e), masked past seq_len with a select (never arithmetic), online softmax
+//     (running max / sum per head, exp2), P^T moved into the B-operand layout by movmatrix,
+//     O^T += V^T P^T on tensor cores with V^T fed by ldmatrix.trans and V rows past seq_len
+//     zeroed in the fragment (0 * NaN would poison the sum),
+//   * the 4 warps' (m, l, O) are combined in shared memory; a single-partition sequence writes
+//     fp16 output directly, otherwise the partition writes fp32 (m, l, O/l) partials that the
+//     merge kernel combines:  M = max m_p,  w_p = 2^(m_p - M) l_p,  out = sum w_p o_p / sum w_p.
+#include <algorithm>
+
+#include "pa_common.cuh"
+#include "pa_kernels.h"
+
+namespace pa {
+namespace {
+
+template <int D, int BS, int NT>
+struct DecodeCfg {
+  static constexpr int kWarps = 4;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kHalves = D / 64;                // 128-byte boxes per token row
+  static constexpr int kBoxBytes = 16 * 128;            // 16 token rows x 128 B
+  static constexpr int kKBytes = kHalves * kBoxBytes;   // K of one 16-token unit
+  static constexpr int kStageBytes = 2 * kKBytes;       // K + V
+  static constexpr int kStages = (64 * 1024) / (kWarps * kStageBytes);
+  static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+  static constexpr int kUnitsPerPart = kPartitionTokens / 16;
+  static constexpr int kDK = D / 16;
+  static constexpr int kHeads = NT * 8;
+  static constexpr int kMergeBytes = kWarps * kHeads * (D + 2) * 4;
+  static constexpr int kSmemBytes = (kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes) + 1024;
+  static_assert(kStages >= 1, "stage ring");
+  static_assert(BS % 16 == 0, "block size must be a multiple of the 16-token unit");
+};
+
+__device__ __forceinline__ uint32_t ldg_u32(const __half* p) {
+  return __ldg(reinterpret_cast<const unsigned int*>(p));
+}
+
+template <int D, int BS, int NT>
+__global__ void __launch_bounds__(DecodeCfg<D, BS, NT>::kThreads)
+    decode_partition_kernel(const __grid_constant__ CUtensorMap kmap,
+                            const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
+  using C = DecodeCfg<D, BS, NT>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[C::kWarps][C::kStages];
+  __shared__ int32_t unit_row[C::kUnitsPerPart];
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int part = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int row0 = a.query_start_loc[s];
+  const int q_len = a.query_start_loc[s + 1] - row0;
+  if (q_len != 1) return;  // prefill chunks and idle sequences are not decode work
+  if (row0 < 0 || row0 + q_len > a.num_tokens) {
+    if (part == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
+    return;
+  }
+  const int L = a.seq_lens[s];
+  const int nparts = (L + kPartitionTokens - 1) / kPartitionTokens;
+  if (L < 1 || (L + BS - 1) / BS > a.max_blocks) {
+    if (part == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
+    return;
+  }
+  if (nparts > static_cast<int>(gridDim.x)) {
+    if (part == 0 && tid == 0) atomicOr(a.err, kErrHint);
+    return;
+  }
+  if (part >= nparts) return;
+
+  const int tok_begin = part * kPartitionTokens;
+  const int tok_end = min(L, tok_begin + kPartitionTokens);
+  const int nunits = (tok_end - tok_begin + 15) >> 4;
+
+  // Block table -> TMA row of every unit of the partition; ids outside the pool stop the CTA.
+  int bad = 0;
+  for (int u = tid; u < nunits; u += C::kThreads) {
+    const int tok = tok_begin + u * 16;
+    const int32_t blk = a.block_tables[static_cast<int64_t>(s) * a.bt_stride + tok / BS];
+    int y = 0;
+    if (blk >= 0 && blk < a.num_blocks)
+      y = (blk * a.num_kv_heads + g) * BS + (tok % BS);
+    else
+      bad = 1;
+    unit_row[u] = y;
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < C::kStages; ++st) mbar_init(smem_addr(&bars[warp][st]), 1);
+    mbar_init_fence();
+  }
+  if (__syncthreads_or(bad)) {
+    if (tid == 0) atomicOr(a.err, kErrBlockRange);
+    return;
+  }
+
+  const int my_n = warp < nunits ? (nunits - warp + C::kWarps - 1) / C::kWarps : 0;
+  const uint32_t ring = smem_addr(smem + warp * (C::kStages * C::kStageBytes));
+  const uint32_t bar0 = smem_addr(&bars[warp][0]);
+
+  auto issue = [&](int i) {  // lane 0: fetch unit i of this warp into stage i % kStages
+    const int u = warp + i * C::kWarps;
+    const int st = i % C::kStages;
+    const uint32_t bar = bar0 + st * 8;
+    const uint32_t kdst = ring + st * C::kStageBytes;
+    const int y = unit_row[u];
+    mbar_arrive_expect_tx(bar, C::kStageBytes);
+#pragma unroll
+    for (int h = 0; h < C::kHalves; ++h) {
+      tma_load_2d(kdst + h * C::kBoxBytes, &kmap, h * 64, y, bar);
+      tma_load_2d(kdst + C::kKBytes + h * C::kBoxBytes, &vmap, h * 64, y, bar);
+    }
+  };
+  if (lane == 0) {
+    const int n0 = my_n < C::kStages ? my_n : C::kStages;
+    for (int i = 0; i < n0; ++i) issue(i);
+  }
+
+  // Q^T as the B operand (k = head_dim, n = the group's heads), kept in registers.
+  const int gq = lane >> 2, cq = lane & 3;
+  uint32_t qf[NT][C::kDK][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hg = nt * 8 + gq;
+    const bool hv = hg < a.group;
+    const __half* qrow = a.q + static_cast<int64_t>(row0) * a.q_stride +
+                         static_cast<int64_t>(g * a.group + (hv ? hg : 0)) * D;
+#pragma unroll
+    for (int j = 0; j < C::kDK; ++j) {
+      qf[nt][j][0] = hv ? ldg_u32(qrow + j * 16 + 2 * cq) : 0u;
+      qf[nt][j][1] = hv ? ldg_u32(qrow + j * 16 + 8 + 2 * cq) : 0u;
+    }
+  }
+
+  float o[NT][C::kDK][4];
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int dt = 0; dt < C::kDK; ++dt) o[nt][dt][0] = o[nt][dt][1] = o[nt][dt][2] = o[nt][dt][3] = 0.f;
+    m_run[nt][0] = m_run[nt][1] = -INFINITY;
+    l_run[nt][0] = l_run[nt][1] = 0.f;
+  }
+
+  const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix index and row of this lane
+  int failed_at = -1;
+  for (int i = 0; i < my_n; ++i) {
+    const int st = i % C::kStages;
+    const bool ok = mbar_wait(bar0 + st * 8, (i / C::kStages) & 1, a.err);
+    if (__any_sync(0xffffffffu, !ok)) {
+      failed_at = i;
+      break;
+    }
+    const int u = warp + i * C::kWarps;
+    const int nvalid = min(16, tok_end - (tok_begin + u * 16));
+    const uint32_t kb = ring + st * C::kStageBytes;
+    const uint32_t vb = kb + C::kKBytes;
+
+    // ---- S^T[16 tokens][8 heads] = K Q^T
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+    for (int j = 0; j < C::kDK; ++j) {
+      const int tok = mr + ((mi & 1) << 3);
+      const int chunk = 2 * j + (mi >> 1);
+      uint32_t af[4];
+      ldsm_x4(kb + (chunk >> 3) * C::kBoxBytes + swz128(tok, chunk & 7), af);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[nt], af, qf[nt][j][0], qf[nt][j][1]);
+    }
+
+    // ---- online softmax over the unit (per head; this lane holds heads 2cq, 2cq+1)
+    const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
+    uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float s00 = v0 ? sacc[nt][0] * a.scale_log2 : -INFINITY;
+      const float s01 = v0 ? sacc[nt][1] * a.scale_log2 : -INFINITY;
+      const float s10 = v1 ? sacc[nt][2] * a.scale_log2 : -INFINITY;
+      const float s11 = v1 ? sacc[nt][3] * a.scale_log2 : -INFINITY;
+      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+      mx0 = warp_max_xor(mx0, 4);
+      mx1 = warp_max_xor(mx1, 4);
+      mx0 = warp_max_xor(mx0, 8);
+      mx1 = warp_max_xor(mx1, 8);
+      mx0 = warp_max_xor(mx0, 16);
+      mx1 = warp_max_xor(mx1, 16);
+      const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+      const float al0 = exp2f(m_run[nt][0] - mn0), al1 = exp2f(m_run[nt][1] - mn1);
+      m_run[nt][0] = mn0;
+      m_run[nt][1] = mn1;
+      const float p00 = exp2f(s00 - mn0), p10 = exp2f(s10 - mn0);
+      const float p01 = exp2f(s01 - mn1), p11 = exp2f(s11 - mn1);
+      l_run[nt][0] = l_run[nt][0] * al0 + (p00 + p10);
+      l_run[nt][1] = l_run[nt][1] * al1 + (p01 + p11);
+#pragma unroll
+      for (int dt = 0; dt < C::kDK; ++dt) {
+        o[nt][dt][0] *= al0;
+        o[nt][dt][1] *= al1;
+        o[nt][dt][2] *= al0;
+        o[nt][dt][3] *= al1;
+      }
+      pb0[nt] = movmatrix_trans(pack_half2(p00, p01));  // P^T[tok 2cq..2cq+1][head gq]
+      pb1[nt] = movmatrix_trans(pack_half2(p10, p11));  // P^T[tok 2cq+8..][head gq]
+    }
+
+    // ---- O^T[d][heads] += V^T[d][16 tokens] P^T
+    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+    if (nvalid < 16) {
+      vm0 = (2 * cq < nvalid ? 0x0000ffffu : 0u) | (2 * cq + 1 < nvalid ? 0xffff0000u : 0u);
+      vm1 = (2 * cq + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * cq + 9 < nvalid ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int dt = 0; dt < C::kDK; ++dt) {
+      const int tok = mr + ((mi >> 1) << 3);
+      const int chunk = 2 * dt + (mi & 1);
+      uint32_t af[4];
+      ldsm_x4_trans(vb + (chunk >> 3) * C::kBoxBytes + swz128(tok, chunk & 7), af);
+      af[0] &= vm0;
+      af[1] &= vm0;
+      af[2] &= vm1;
+      af[3] &= vm1;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][dt], af, pb0[nt], pb1[nt]);
+    }
+
+    __syncwarp();
+    if (lane == 0 && i + C::kStages < my_n) {
+      fence_proxy_async();
+      issue(i + C::kStages);
+    }
+  }
+
+  if (failed_at >= 0) {
+    // A copy never arrived: let whatever is still in flight land (bounded) before leaving.
+    if (lane == 0) {
+      const int issued = min(my_n, failed_at + C::kStages);
+      for (int i = failed_at + 1; i < issued; ++i)
+        mbar_wait(bar0 + (i % C::kStages) * 8, (i / C::kStages) & 1, a.err);
+    }
+  }
+
+  // ---- combine the warps' partial softmax states
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float l = l_run[nt][e];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      l_run[nt][e] = l;
+    }
+  }
+  __syncthreads();  // every warp is done with its ring: reuse it for the merge
+  constexpr int H = C::kHeads;
+  float* sm_m = reinterpret_cast<float*>(smem);
+  float* sm_l = sm_m + C::kWarps * H;
+  float* sm_o = sm_l + C::kWarps * H;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int h = nt * 8 + 2 * cq + e;
+      if (gq == 0) {
+        sm_m[warp * H + h] = m_run[nt][e];
+        sm_l[warp * H + h] = l_run[nt][e];
+      }
+      float* dst = sm_o + (warp * H + h) * D;
+#pragma unroll
+      for (int dt = 0; dt < C::kDK; ++dt) {
+        dst[dt * 16 + gq] = o[nt][dt][e];
+        dst[dt * 16 + gq + 8] = o[nt][dt][2 + e];
+      }
+    }
+  }
+  // A warp that timed out has set the error word; the whole CTA then leaves its outputs alone.
+  if (__syncthreads_or(failed_at >= 0)) return;
+
+  for (int idx = tid; idx < a.group * D; idx += C::kThreads) {
+    const int h = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, sm_m[w * H + h]);
+    float wsum = 0.f, osum = 0.f;
+#pragma unroll
+    for (int w = 0; w < C::kWarps; ++w) {
+      const float f = exp2f(sm_m[w * H + h] - M);
+      wsum += f * sm_l[w * H + h];
+      osum += f * sm_o[(w * H + h) * D + d];
+    }
+    const int hq = g * a.group + h;
+    const int64_t orow = static_cast<int64_t>(row0) * a.num_q_heads + hq;
+    if (nparts == 1) {
+      a.out[orow * D + d] = __float2half_rn(osum / wsum);
+    } else {
+      const int64_t pidx = orow * a.max_parts + part;
+      a.part_o[pidx * D + d] = osum / wsum;
+      if (d == 0) {
+        a.part_m[pidx] = M;
+        a.part_l[pidx] = wsum;
+      }
+    }
+  }
+}
+
+// One warp per (decode row, query head): combine the row's partitions.
+template <int D>
+__global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a) {
+  const int s = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hq = blockIdx.x * 4 + warp;
+  if (hq >= a.num_q_heads) return;
+  const int row0 = a.query_start_loc[s];
+  if (a.query_start_loc[s + 1] - row0 != 1 || row0 < 0 || row0 + 1 > a.num_tokens) return;
+  const int L = a.seq_lens[s];
+  const int nparts = (L + kPartitionTokens - 1) / kPartitionTokens;
+  if (nparts <= 1 || nparts > a.max_parts || (L + a.block_size - 1) / a.block_size > a.max_blocks)
+    return;
+  const int64_t base = (static_cast<int64_t>(row0) * a.num_q_heads + hq) * a.max_parts;
+
+  float M = -INFINITY;
+  for (int p = lane; p < nparts; p += 32) M = fmaxf(M, a.part_m[base + p]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  constexpr int V = D / 32;  // output elements per lane
+  float acc[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  for (int p0 = 0; p0 < nparts; p0 += 32) {
+    const int p = p0 + lane;
+    const float w = p < nparts ? exp2f(a.part_m[base + p] - M) * a.part_l[base + p] : 0.f;
+    const int n = min(32, nparts - p0);
+    for (int j = 0; j < n; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      wsum += wj;
+      const float* op = a.part_o + (base + p0 + j) * D + lane * V;
+      if constexpr (V == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(op);
+        acc[0] += wj * x.x;
+        acc[1] += wj * x.y;
+        acc[2] += wj * x.z;
+        acc[3] += wj * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(op);
+        acc[0] += wj * x.x;
+        acc[1] += wj * x.y;
+      }
+    }
+  }
+  __half* dst = a.out + (static_cast<int64_t>(row0) * a.num_q_heads + hq) * D + lane * V;
+  const float inv = 1.f / wsum;
+  if constexpr (V == 4) {
+    uint2 pk;
+    pk.x = pack_half2(acc[0] * inv, acc[1] * inv);
+    pk.y = pack_half2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+template <int D, int BS, int NT>
+cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            cudaStream_t stream) {
+  using C = DecodeCfg<D, BS, NT>;
+  auto kern = decode_partition_kernel<D, BS, NT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
+  return cudaGetLastError();
+}
+
+template <int D, int BS>
+cudaError_t launch_decode_g(const AttnArgs& a, const CUtensorMap& k, const CUtensorMap& v,
+                            cudaStream_t st) {
+  return a.group <= 8 ? launch_decode_t<D, BS, 1>(a, k, v, st) : launch_decode_t<D, BS, 2>(a, k, v, st);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream) {
+  if (a.head_dim == 128)
+    return a.block_size == 16 ? launch_decode_g<128, 16>(a, kmap, vmap, stream)
+                              : launch_decode_g<128, 32>(a, kmap, vmap, stream);
+  return a.block_size == 16 ? launch_decode_g<64, 16>(a, kmap, vmap, stream)
+                            : launch_decode_g<64, 32>(a, kmap, vmap, stream);
+}
+
+cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream) {
+  dim3 grid((a.num_q_heads + 3) / 4, a.num_seqs);
+  if (a.head_dim == 128)
+    merge_partitions_kernel<128><<<grid, 128, 0, stream>>>(a);
+  else
+    merge_partitions_kernel<64><<<grid, 128, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

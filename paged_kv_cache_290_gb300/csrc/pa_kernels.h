@@ -1,0 +1,60 @@
+// Host-side launch interface between the C ABI (pa_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct CacheArgs {
+  const __half* k;
+  const __half* v;
+  int64_t k_stride;  // elements between consecutive tokens of k
+  int64_t v_stride;
+  __half* k_cache;
+  __half* v_cache;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int64_t num_blocks;
+  unsigned* err;
+};
+
+struct AttnArgs {
+  const __half* q;
+  int64_t q_stride;  // elements between consecutive query tokens
+  __half* out;       // [T, Hq, d] contiguous
+  const int32_t* block_tables;
+  int64_t bt_stride;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  float* part_o;  // [T, Hq, P, d]
+  float* part_m;  // [T, Hq, P]
+  float* part_l;  // [T, Hq, P]
+  int num_seqs;
+  int64_t num_tokens;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int head_dim;
+  int block_size;
+  int max_blocks;  // columns of block_tables
+  int64_t num_blocks;
+  int max_parts;   // P = ceil(max_seq_len / 512) (>= 1)
+  int max_query_len;
+  float scale_log2;  // scale * log2(e)
+  unsigned* err;
+};
+
+cudaError_t launch_reshape_and_cache(const CacheArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream);
+cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           cudaStream_t stream);
+
+}  // namespace pa

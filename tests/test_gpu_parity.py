@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on seeded inputs.
+
+Bars: reshape_and_cache is bit-exact over the whole pool (NaN sentinels and untouched bytes
+included); fp16 attention output has max |err| <= 2e-3 and ||err||_2 / ||ref||_2 <= 1e-3
+against the fp64 oracle.  Invariants that hold exactly on the GPU too: re-permuting physical
+blocks and un-aliasing a shared prefix give bit-identical outputs, and a 1-token context returns
+V exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_290_gb300 as pa
+from paged_kv_cache_290_gb300 import workloads as W
+from _cases import small_decode, small_mixed, small_prefix
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 2e-3
+MAX_REL_L2 = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_290_gb300 import build
+    build.build()
+    pa.load_library()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.init()
+    pa.get_device_error()  # start from a clear device error word
+
+
+def _u16(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def gpu_step(b, write=True, pool=None):
+    """reshape_and_cache (pre-step pool + new tokens) then attention, like one serving step."""
+    dev = "cuda"
+    if pool is None:
+        kc = (b.k_cache_pre if write else b.k_cache).to(dev)
+        vc = (b.v_cache_pre if write else b.v_cache).to(dev)
+    else:
+        kc, vc = pool
+    if write:
+        pa.reshape_and_cache(b.k_new.to(dev), b.v_new.to(dev), kc, vc, b.slot_mapping.to(dev))
+    q = b.q.to(dev)
+    out = torch.full_like(q, float("nan"))
+    pa.attention(q, kc, vc, b.block_tables.to(dev), b.seq_lens.to(dev),
+                 b.query_start_loc.to(dev), b.scale, out, b.max_query_len, b.max_seq_len)
+    st, bits = pa.get_device_error()
+    assert st == 0, (st, bits, pa.last_error())
+    return kc, vc, out
+
+
+def assert_close(out, ref, rows=None):
+    o = out.detach().cpu().double().numpy()
+    if rows is not None:
+        o, ref = o[rows], ref[rows]
+    assert np.isfinite(o).all(), "non-finite output"
+    err = np.abs(o - ref)
+    rel = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-30)
+    assert err.max() <= MAX_ABS, f"max abs err {err.max():.3e}"
+    assert rel <= MAX_REL_L2, f"rel L2 err {rel:.3e}"
+    return err.max(), rel
+
+
+SMALL = {
+    "tiny_decode": W.tiny_decode,
+    "decode_d128_bs16_g4": lambda: small_decode(),
+    "decode_d128_bs32_g8": lambda: small_decode(bs=32, hq=64, hkv=8, seed=9104),
+    "decode_d64_bs16_g1": lambda: small_decode(d=64, hq=4, hkv=4, seed=9105),
+    "decode_d64_bs32_g16": lambda: small_decode(d=64, bs=32, hq=32, hkv=2, seed=9106),
+    "decode_d128_bs16_g7": lambda: small_decode(hq=28, hkv=4, seed=9107),
+    "decode_d128_bs16_g12": lambda: small_decode(hq=24, hkv=2, seed=9108),
+    "mixed_d128_bs16_g4": lambda: small_mixed(),
+    "mixed_d128_bs32_g8": lambda: small_mixed(bs=32, hq=16, hkv=2, seed=9207),
+    "mixed_d64_bs16_g7": lambda: small_mixed(d=64, hq=28, hkv=4, seed=9208),
+    "mixed_d64_bs32_g1": lambda: small_mixed(d=64, bs=32, hq=4, hkv=4, seed=9209),
+    "mixed_d128_bs16_g16": lambda: small_mixed(hq=32, hkv=2, seed=9210),
+    "prefix_d128_bs16": lambda: small_prefix(),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_cases_match_oracle(name):
+    b = SMALL[name]()
+    kc, vc, out = gpu_step(b)
+    rk, rv = oracle.reshape_and_cache(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
+                                      b.slot_mapping)
+    assert np.array_equal(_u16(kc), rk), "k_cache bytes differ"
+    assert np.array_equal(_u16(vc), rv), "v_cache bytes differ"
+    ref = oracle.attention_batch(b)
+    assert_close(out, ref)
+
+
+@pytest.mark.parametrize("name", ["decode_d128_bs16_g4", "mixed_d128_bs32_g8", "prefix_d128_bs16"])
+def test_block_placement_is_bit_invariant(name):
+    b = SMALL[name]()
+    _, _, o1 = gpu_step(b, write=False)
+    _, _, o2 = gpu_step(W.repermute(b, seed=5), write=False)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_aliased_prefix_equals_private_copies_bitwise():
+    b = small_prefix()
+    _, _, o1 = gpu_step(b, write=False)
+    _, _, o2 = gpu_step(W.unalias_prefix(b), write=False)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_one_token_context_returns_v_exactly():
+    for d, bs, hq, hkv in [(64, 16, 8, 2), (128, 32, 64, 8), (128, 16, 28, 4)]:
+        b = W.build_batch("one", [W.SeqSpec(1, 1)] * 5, num_q_heads=hq, num_kv_heads=hkv,
+                          head_dim=d, block_size=bs, seed_base=9600 + d + bs)
+        _, _, out = gpu_step(b)
+        want = b.v_new.repeat_interleave(hq // hkv, dim=1)
+        assert torch.equal(out.cpu().view(torch.int16), want.view(torch.int16))
+
+
+def test_padding_slots_and_reuse_of_output_buffer():
+    """Padding tokens (slot -1) write nothing; rows of idle sequences (q_len 0) are untouched."""
+    b = small_mixed(seed=9211)
+    kc, vc, out = gpu_step(b)
+    assert np.isfinite(out.cpu().double().numpy()).all()
+    rk, _ = oracle.reshape_and_cache(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
+                                     b.slot_mapping)
+    assert np.array_equal(_u16(kc), rk)
+
+
+def test_bad_block_id_is_skipped_and_reported():
+    """A block id outside the pool is caught by the kernels' own bounds check before any copy:
+    the work item is skipped and the device error word reports it."""
+    b = small_mixed(seed=9212)
+    bt = b.block_tables.clone()
+    s = next(i for i, x in enumerate(b.seqs) if x.query_len == 1)
+    bt[s, 0] = b.num_blocks + 7
+    dev = "cuda"
+    kc, vc = b.k_cache.to(dev), b.v_cache.to(dev)
+    out = torch.zeros_like(b.q, device=dev)
+    pa.attention(b.q.to(dev), kc, vc, bt.to(dev), b.seq_lens.to(dev), b.query_start_loc.to(dev),
+                 b.scale, out, b.max_query_len, b.max_seq_len)
+    st, bits = pa.get_device_error()
+    assert st == pa.binding.PA_ERR_OUT_OF_RANGE and bits & 4
+    st, bits = pa.get_device_error()
+    assert st == 0 and bits == 0
+
+
+def test_slot_past_pool_is_skipped_and_reported():
+    b = W.tiny_decode()
+    dev = "cuda"
+    kc, vc = b.k_cache_pre.to(dev), b.v_cache_pre.to(dev)
+    sm = b.slot_mapping.clone()
+    sm[1] = b.num_blocks * b.block_size + 3
+    pa.reshape_and_cache(b.k_new.to(dev), b.v_new.to(dev), kc, vc, sm.to(dev))
+    st, bits = pa.get_device_error()
+    assert st == pa.binding.PA_ERR_OUT_OF_RANGE and bits & 2
+    rk, _ = oracle.reshape_and_cache(b.k_new[[0, 2, 3]], b.v_new[[0, 2, 3]], b.k_cache_pre,
+                                     b.v_cache_pre, b.slot_mapping[[0, 2, 3]])
+    assert np.array_equal(_u16(kc), rk)
+
+
+def test_hint_too_small_is_reported():
+    b = small_decode(seed=9109)
+    dev = "cuda"
+    out = torch.zeros_like(b.q, device=dev)
+    need = pa.workspace_size(b.num_tokens, b.num_q_heads, b.head_dim, 600)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    pa.attention(b.q.to(dev), b.k_cache.to(dev), b.v_cache.to(dev), b.block_tables.to(dev),
+                 b.seq_lens.to(dev), b.query_start_loc.to(dev), b.scale, out, 1, 600,
+                 workspace=ws)
+    st, bits = pa.get_device_error()
+    assert st == pa.binding.PA_ERR_DESCRIPTOR and bits & 16
+
+
+# ------------------------------------------------------------------ the five full-size workloads
+
+def _full(name, sample_prefill_rows=None):
+    b = W.WORKLOADS[name]()
+    kc, vc, out = gpu_step(b)
+    rk, rv = oracle.reshape_and_cache(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
+                                      b.slot_mapping)
+    assert np.array_equal(_u16(kc), rk)
+    assert np.array_equal(_u16(vc), rv)
+    mask = None
+    if sample_prefill_rows:
+        # every decode row, plus the first, last and a seeded sample of each prefill chunk's rows
+        g = torch.Generator().manual_seed(4242)
+        mask = np.zeros(b.num_tokens, dtype=np.uint8)
+        for s, spec in enumerate(b.seqs):
+            r0 = int(b.query_start_loc[s])
+            if spec.query_len == 1:
+                mask[r0] = 1
+            elif spec.query_len > 1:
+                pick = torch.randperm(spec.query_len, generator=g)[:sample_prefill_rows].tolist()
+                for i in set(pick) | {0, spec.query_len - 1}:
+                    mask[r0 + i] = 1
+    ref = oracle.attention_batch(b, row_mask=mask)
+    rows = None if mask is None else np.nonzero(mask)[0]
+    return assert_close(out, ref, rows)
+
+
+def test_full_tiny_decode():
+    _full("tiny_decode")
+
+
+def test_full_llama8b_decode():
+    _full("llama8b_decode")
+
+
+def test_full_llama70b_32x8k_decode():
+    _full("llama70b_32x8k_decode")
+
+
+def test_full_prefix_shared_decode():
+    _full("prefix_shared_decode")
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_full_mixed_step(bs):
+    _full(f"mixed_step_bs{bs}", sample_prefill_rows=24)
