@@ -231,6 +231,10 @@ def run_ours(args, world, rank, local):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
+    for _, _, k0, k1 in ev:  # torch creates an event on its first record(); the library then
+        k0.record(stream)    # re-records these handles around the decode-partition kernel
+        k1.record(stream)
+    torch.cuda.synchronize()
     uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", ""))
     clocks = ClockSampler(uuid)
     clocks.start()

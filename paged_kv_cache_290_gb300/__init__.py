@@ -5,7 +5,9 @@ names exported here are its thin Python binding.  ``workloads`` holds the seeded
 inputs used by tests and the benchmark.
 """
 from .binding import (PAError, BatchDescriptor, attention, get_device_error, last_error,
-                      load_library, reshape_and_cache, version, workspace_size)
+                      load_library, reshape_and_cache, set_timing_events, version,
+                      workspace_size)
 
 __all__ = ["PAError", "BatchDescriptor", "attention", "get_device_error", "last_error",
-           "load_library", "reshape_and_cache", "version", "workspace_size"]
+           "load_library", "reshape_and_cache", "set_timing_events", "version",
+           "workspace_size"]

@@ -328,11 +328,12 @@ def llama8b_decode(**kw) -> PagedBatch:
                        spare_frac=0.10, **kw)
 
 
-def llama70b_decode(**kw) -> PagedBatch:
-    """32 decode sequences of 8192 keys, 64 q / 8 kv heads, d 128, bs 16, 64 spare blocks."""
+def llama70b_decode(num_seqs: int = 32, **kw) -> PagedBatch:
+    """32 decode sequences of 8192 keys, 64 q / 8 kv heads, d 128, bs 16, 64 spare blocks.
+    ``num_seqs`` shrinks the batch (same shapes) for profiler captures."""
     s = _seed(3)
-    n, L, bs = 32, 8192, 16
-    return build_batch("llama70b_32x8k_decode", [SeqSpec(L, 1)] * n, num_q_heads=64,
+    n, L, bs = num_seqs, 8192, 16
+    return build_batch(f"llama70b_{n}x8k_decode", [SeqSpec(L, 1)] * n, num_q_heads=64,
                        num_kv_heads=8, head_dim=128, block_size=bs, seed_base=s,
                        pool_blocks=n * L // bs + 64, **kw)
 
@@ -365,6 +366,7 @@ WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama8b_decode": llama8b_decode,
     "llama70b_32x8k_decode": llama70b_decode,
+    "llama70b_8x8k_decode": lambda **kw: llama70b_decode(8, **kw),
     "prefix_shared_decode": prefix_shared_decode,
     "mixed_step_bs16": lambda **kw: mixed_step(16, **kw),
     "mixed_step_bs32": lambda **kw: mixed_step(32, **kw),
