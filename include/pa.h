@@ -136,6 +136,30 @@ int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
                  const pa_batch_hint* hint, void* workspace, size_t workspace_bytes,
                  void* stream);
 
+/*
+ * pa_attention_static_scratch -- pa_attention without a caller-provided workspace, for callers
+ * that cannot allocate device memory (no paper counterpart: the pages describe no such call).
+ *
+ * Some callers may not call cudaMalloc at all: plugins inside a host program whose own pool
+ * owns all device memory, or code on a serving path where allocating is not allowed because
+ * cudaMalloc may block or synchronise and cudaFree synchronises the device.  This call takes the
+ * same arguments as pa_attention minus the workspace and uses a fixed 32 MiB array in the
+ * library's device memory for the split-context partials instead.  It allocates nothing.
+ *   - Every GPU that loads the library holds the 32 MiB until the process exits.
+ *   - A batch needing more than 32 MiB of scratch (pa_attention_workspace_size(T, Hq, d,
+ *     hint->max_seq_len) > 32 MiB) is rejected with PA_ERR_WORKSPACE and a message; nothing runs.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current) and caches it; make that first call before any stream capture.
+ *   - All calls on a device share the array, which keeps the last call's contents; nothing in it
+ *     needs to start at zero.  Calls that overlap on the GPU race on it: order them.
+ * Results are those of pa_attention on the same inputs.
+ */
+int pa_attention_static_scratch(const pa_tensor* q, const pa_tensor* k_cache,
+                                const pa_tensor* v_cache, const pa_tensor* block_tables,
+                                const pa_tensor* seq_lens, const pa_tensor* query_start_loc,
+                                float scale, const pa_tensor* out, const pa_batch_hint* hint,
+                                void* stream);
+
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 const char* pa_last_error(void);
 

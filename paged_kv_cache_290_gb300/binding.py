@@ -30,7 +30,8 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3:
 PA_F16, PA_I32, PA_I64 = 0, 1, 2
 PARTITION_TOKENS = 512
 EXPORTED = ("pa_reshape_and_cache", "pa_attention_workspace_size", "pa_attention",
-            "pa_last_error", "pa_get_device_error", "pa_set_timing_events", "pa_version")
+            "pa_last_error", "pa_get_device_error", "pa_set_timing_events", "pa_version",
+            "pa_attention_static_scratch")
 
 _DTYPES = {torch.float16: PA_F16, torch.int32: PA_I32, torch.int64: PA_I64}
 
@@ -75,6 +76,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_get_device_error.restype = ctypes.c_int
         lib.pa_get_device_error.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
         lib.pa_version.restype = ctypes.c_int
+        lib.pa_attention_static_scratch.restype = ctypes.c_int
+        lib.pa_attention_static_scratch.argtypes = [P, P, P, P, P, P, ctypes.c_float, P,
+                                                    ctypes.POINTER(PABatchHint), ctypes.c_void_p]
         lib.pa_set_timing_events.restype = ctypes.c_int
         lib.pa_set_timing_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
         _lib = lib

@@ -172,6 +172,10 @@ WorkspaceLayout workspace_layout(int64_t t, int64_t hq, int64_t d, int32_t max_s
 
 }  // namespace
 
+namespace pa {
+int set_last_error(int status, const std::string& message) { return fail(status, message); }
+}  // namespace pa
+
 extern "C" {
 
 const char* pa_last_error(void) { return g_last_error.c_str(); }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 namespace pa {
 
 struct CacheArgs {
@@ -49,6 +51,9 @@ struct AttnArgs {
   float scale_log2;  // scale * log2(e)
   unsigned* err;
 };
+
+// Sets the message pa_last_error() returns on this host thread; returns `status`.
+int set_last_error(int status, const std::string& message);
 
 cudaError_t launch_reshape_and_cache(const CacheArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
