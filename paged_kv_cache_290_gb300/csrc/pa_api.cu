@@ -323,13 +323,13 @@ int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (timed && (e = cudaEventRecord(g_time_stop, st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
-  if (hint->max_query_len > 1) {
-    e = pa::launch_prefill(a, kmap, vmap, st);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-  }
   if (a.max_parts > 1) {
     e = pa::launch_merge(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
+  if (hint->max_query_len > 1) {
+    e = pa::launch_prefill(a, kmap, vmap, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   return PA_OK;
 }

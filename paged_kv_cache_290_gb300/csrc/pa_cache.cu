@@ -17,6 +17,9 @@ namespace {
 template <int D>
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheArgs a) {
   constexpr int kChunks = D / 8;  // 16-byte chunks per (token, head) row
+  // The attention kernel that follows is a programmatic dependent: let it start setting up
+  // now; it waits for this grid to finish (griddepcontrol.wait) before reading anything.
+  grid_launch_dependents();
   const int64_t total = a.num_tokens * a.num_kv_heads * kChunks;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {

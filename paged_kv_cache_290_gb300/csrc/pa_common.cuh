@@ -34,6 +34,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Optional self-checks (compiled in with -DPA_SELFCHECK for fault hunting only): a failed
+// check sets bit 8 + id of the device error word and the guarded access is skipped.
+#ifdef PA_SELFCHECK
+__device__ __forceinline__ bool selfcheck(bool ok, int id, unsigned* err) {
+  if (!ok) atomicOr(err, 1u << (8 + (id & 15)));
+  return ok;
+}
+#define PA_CHECK(cond, id) (::pa::selfcheck((cond), (id), a.err))
+#else
+#define PA_CHECK(cond, id) (true)
+#endif
+
 // ---------------------------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -82,6 +94,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   }
   atomicOr(err, kErrTimeout);
   return false;
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Wait until the grids this one depends on have completed and their writes are visible
+// (a no-op when the kernel was not launched as a programmatic dependent).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next programmatically dependent grid on the stream to begin launching.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------------- TMA

@@ -18,6 +18,8 @@
 //   * the 4 warps' (m, l, O) are combined in shared memory; a single-partition sequence writes
 //     fp16 output directly, otherwise the partition writes fp32 (m, l, O/l) partials that the
 //     merge kernel combines:  M = max m_p,  w_p = 2^(m_p - M) l_p,  out = sum w_p o_p / sum w_p.
+// Both kernels are programmatic dependents of what precedes them on the stream: they may be
+// scheduled early but read nothing from global memory before griddepcontrol.wait.
 #include <algorithm>
 
 #include "pa_common.cuh"
@@ -62,6 +64,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT>::kThreads)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int part = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  grid_dependency_wait();  // everything the previous kernels wrote is visible from here on
+  grid_launch_dependents();
 
   const int row0 = a.query_start_loc[s];
   const int q_len = a.query_start_loc[s + 1] - row0;
@@ -322,6 +326,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT>::kThreads)
 // One warp per (decode row, query head): combine the row's partitions.
 template <int D>
 __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a) {
+  grid_dependency_wait();  // the partials come from the decode kernel just before
+  grid_launch_dependents();
   const int s = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.x * 4 + warp;
@@ -386,8 +392,17 @@ cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CU
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
 template <int D, int BS>
@@ -408,12 +423,17 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
 }
 
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream) {
-  dim3 grid((a.num_q_heads + 3) / 4, a.num_seqs);
-  if (a.head_dim == 128)
-    merge_partitions_kernel<128><<<grid, 128, 0, stream>>>(a);
-  else
-    merge_partitions_kernel<64><<<grid, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.num_q_heads + 3) / 4, a.num_seqs);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return a.head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_partitions_kernel<128>, a)
+                           : cudaLaunchKernelEx(&cfg, merge_partitions_kernel<64>, a);
 }
 
 }  // namespace pa

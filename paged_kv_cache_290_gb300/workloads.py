@@ -348,17 +348,19 @@ def prefix_shared_decode(**kw) -> PagedBatch:
                        seed_base=s, shared_prefix_len=2048, spare_frac=0.10, **kw)
 
 
-def mixed_step(block_size: int = 16, **kw) -> PagedBatch:
+def mixed_step(block_size: int = 16, num_decode: int = 128, **kw) -> PagedBatch:
     """4 prefill chunks of 512 queries over a paged context uniform in [0, 7488] plus 128 decode
-    sequences with lengths uniform in [256, 8000], in one seeded order; 32 q / 8 kv, d 128."""
+    sequences with lengths uniform in [256, 8000], in one seeded order; 32 q / 8 kv, d 128.
+    ``num_decode`` keeps only the first decode sequences (for profiler captures)."""
     s = _seed(5)
     g = _gen(s + 0)
     ctx = torch.randint(0, 7489, (4,), generator=g).tolist()
-    dec = torch.randint(256, 8001, (128,), generator=g).tolist()
+    dec = torch.randint(256, 8001, (128,), generator=g).tolist()[:num_decode]
     seqs = [SeqSpec(c + 512, 512) for c in ctx] + [SeqSpec(L, 1) for L in dec]
     order = torch.randperm(len(seqs), generator=_gen(s + 5)).tolist()
     seqs = [seqs[i] for i in order]
-    return build_batch(f"mixed_step_bs{block_size}", seqs, num_q_heads=32, num_kv_heads=8,
+    name = f"mixed_step_bs{block_size}" + ("" if num_decode == 128 else f"_{num_decode}dec")
+    return build_batch(name, seqs, num_q_heads=32, num_kv_heads=8,
                        head_dim=128, block_size=block_size, seed_base=s, spare_frac=0.10, **kw)
 
 
@@ -370,4 +372,5 @@ WORKLOADS = {
     "prefix_shared_decode": prefix_shared_decode,
     "mixed_step_bs16": lambda **kw: mixed_step(16, **kw),
     "mixed_step_bs32": lambda **kw: mixed_step(32, **kw),
+    "mixed_step_bs16_8dec": lambda **kw: mixed_step(16, num_decode=8, **kw),
 }

@@ -174,6 +174,17 @@ def test_hint_too_small_is_reported():
     assert st == pa.binding.PA_ERR_DESCRIPTOR and bits & 16
 
 
+def test_prefill_longer_than_hint_is_reported():
+    """A prefill chunk with more rows than the hint's max_query_len is skipped and reported."""
+    b = small_mixed(seed=9213)
+    dev = "cuda"
+    out = torch.zeros_like(b.q, device=dev)
+    pa.attention(b.q.to(dev), b.k_cache.to(dev), b.v_cache.to(dev), b.block_tables.to(dev),
+                 b.seq_lens.to(dev), b.query_start_loc.to(dev), b.scale, out, 16, b.max_seq_len)
+    st, bits = pa.get_device_error()
+    assert st == pa.binding.PA_ERR_DESCRIPTOR and bits & 16
+
+
 # ------------------------------------------------------------------ the five full-size workloads
 
 def _full(name, sample_prefill_rows=None):
