@@ -335,13 +335,18 @@ def run_ours(args, world, rank, local):
 
 
 def load_traffic(workload):
-    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if any."""
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if any, and
+    only while the kernel source is the one the counters were taken on (else None)."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    data = json.load(open(path))
-    entry = data.get(workload)
-    return entry.get("dram_bytes_per_launch") if entry else None
+    entry = json.load(open(path)).get(workload)
+    if not entry:
+        return None
+    src = os.path.join(ROOT, "paged_kv_cache_290_gb300", "csrc", "pa_decode.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return entry["dram_bytes_per_launch"] if digest == entry.get("source_sha256_16") else None
 
 
 # ------------------------------------------------------------------------------ CPU oracle

@@ -346,28 +346,39 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a)
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
 
   constexpr int V = D / 32;  // output elements per lane
+  constexpr int kBatch = 16;  // partitions whose loads are all in flight at once
   float acc[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
   float wsum = 0.f;
-  for (int p0 = 0; p0 < nparts; p0 += 32) {
-    const int p = p0 + lane;
-    const float w = p < nparts ? exp2f(a.part_m[base + p] - M) * a.part_l[base + p] : 0.f;
-    const int n = min(32, nparts - p0);
-    for (int j = 0; j < n; ++j) {
+  for (int p0 = 0; p0 < nparts; p0 += kBatch) {
+    const int n = min(kBatch, nparts - p0);
+    const float w = lane < n ? exp2f(a.part_m[base + p0 + lane] - M) * a.part_l[base + p0 + lane] : 0.f;
+    float x[kBatch][V];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (j < n) {
+        const float* op = a.part_o + (base + p0 + j) * D + lane * V;
+        if constexpr (V == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(op);
+          x[j][0] = t.x;
+          x[j][1] = t.y;
+          x[j][2] = t.z;
+          x[j][3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(op);
+          x[j][0] = t.x;
+          x[j][1] = t.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
       const float wj = __shfl_sync(0xffffffffu, w, j);
-      wsum += wj;
-      const float* op = a.part_o + (base + p0 + j) * D + lane * V;
-      if constexpr (V == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(op);
-        acc[0] += wj * x.x;
-        acc[1] += wj * x.y;
-        acc[2] += wj * x.z;
-        acc[3] += wj * x.w;
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(op);
-        acc[0] += wj * x.x;
-        acc[1] += wj * x.y;
+      if (j < n) {
+        wsum += wj;
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] += wj * x[j][e];
       }
     }
   }

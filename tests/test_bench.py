@@ -1,0 +1,79 @@
+"""CPU tests of bench.py's bookkeeping: algorithmic bytes, launch counts and the multi-rank
+(max-over-ranks) reduction, the latter with two gloo ranks on the CPU."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+from paged_kv_cache_290_gb300 import workloads as W
+from _cases import small_mixed, small_prefix
+
+
+def test_70b_step_bytes_match_the_hand_count():
+    """32 x 8192 keys x 8 kv heads x 128 x 2 B x (K+V) + Q/out + table entries + descriptor."""
+    b = W.llama70b_decode(keep_contiguous=False, keep_pre=False)
+    n = bench.algorithmic_bytes(b)
+    kv = 32 * 8192 * 8 * 128 * 2 * 2
+    qo = 2 * 32 * 64 * 128 * 2
+    table = 32 * 512 * 4
+    desc = 32 * 4 + 33 * 4
+    assert n["kv_logical"] == n["kv_unique"] == kv == 2 ** 30
+    assert n["attention_logical"] == kv + qo + table + desc == 1_074_856_196
+    assert n["decode_rows"] == 32
+    assert n["flops"] == 4 * 64 * 128 * 32 * 8192
+    assert bench.launches_per_step(b) == 3  # scatter-write, decode partitions, merge
+
+
+def test_aliased_prefix_counts_unique_blocks_once():
+    b = small_prefix()
+    n = bench.algorithmic_bytes(b)
+    row = b.num_kv_heads * b.head_dim * 4
+    shared = b.meta["shared_prefix_len"]
+    assert n["kv_logical"] == sum(s.seq_len for s in b.seqs) * row
+    assert n["kv_unique"] == (shared + sum(s.seq_len - shared for s in b.seqs)) * row
+
+
+def test_mixed_step_counts_prefill_launch():
+    b = small_mixed()
+    assert bench.launches_per_step(b) == 4
+    n = bench.algorithmic_bytes(b)
+    assert n["decode_rows"] == sum(1 for s in b.seqs if s.query_len == 1)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.reduce_max(1.5 + rank, world)
+        bench.barrier(world)
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    results = sorted(q.get(timeout=10) for _ in range(2))
+    assert results == [(0, 2.5), (1, 2.5)]
+
+
+def test_single_rank_reduction_is_identity():
+    assert bench.reduce_max(3.25, 1) == 3.25

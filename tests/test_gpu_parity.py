@@ -174,6 +174,24 @@ def test_hint_too_small_is_reported():
     assert st == pa.binding.PA_ERR_DESCRIPTOR and bits & 16
 
 
+def test_workspace_reused_and_never_cleared():
+    """Partition tickets carry a per-call tag: a workspace full of random bytes, reused by three
+    calls in a row, gives the oracle's result every time."""
+    b = small_decode(seed=9110)
+    dev = "cuda"
+    need = pa.workspace_size(b.num_tokens, b.num_q_heads, b.head_dim, b.max_seq_len)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device=dev)
+    ref = oracle.attention_batch(b)
+    args = [x.to(dev) for x in (b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                                b.query_start_loc)]
+    for _ in range(3):
+        out = torch.full_like(args[0], float("nan"))
+        pa.attention(*args, b.scale, out, b.max_query_len, b.max_seq_len, workspace=ws)
+        st, bits = pa.get_device_error()
+        assert st == 0, (st, bits)
+        assert_close(out, ref)
+
+
 def test_prefill_longer_than_hint_is_reported():
     """A prefill chunk with more rows than the hint's max_query_len is skipped and reported."""
     b = small_mixed(seed=9213)
