@@ -1,56 +1,72 @@
-// Chunked-prefill attention over a paged KV cache.
+// Chunked-prefill attention over a paged KV cache on the 5th-generation tensor cores.
 //
 // A prefill chunk of q_len rows for a sequence of seq_len keys sits at absolute positions
 // ctx .. ctx + q_len - 1 with ctx = seq_len - q_len; row i attends to keys 0 .. ctx + i
 // ("Local_LLM_03_vLLM_Architecture", chunked-prefill slide: a long prefill is cut into chunks,
 // e.g. 512 tokens, interleaved with decodes; the chunk sees the paged context written before).
 //
-// Work item = one CTA = (q tile, sequence s, kv head g).  The tile's 128 rows are
-// (query token, head of the GQA group) pairs, so one K/V tile in shared memory serves every
-// head of the group.  A producer warp streams 64-key K and V tiles (four 16-token units,
-// each one or two 128-byte-swizzled TMA boxes, gathered through the block table) into a
-// two-stage ring; eight consumer warps each own 16 rows and run S = Q K^T and O += P V on
-// tensor cores (m16n8k16, fp16 in, fp32 accumulate) with an online softmax in exp2.
+// Work item = one CTA = (q tile, kv head g, sequence s).  Its 128 rows are (query token, head of
+// the GQA group) pairs, so one K/V tile serves every head of the group.  Warp roles:
+//   * producers (warps 8 and 9): stream 128-key K and V tiles (8 units of 16 tokens gathered
+//     through the block table, 128-byte-swizzled TMA boxes) into separate 2-stage rings; a K
+//     stage is released as soon as its S = Q K^T is done, a V stage after its P V,
+//   * MMA (warp 10, one thread): S_j = Q K_j^T into one of two TMEM buffers (M 128, N 128, K d,
+//     both operands K-major) and O += P_j V_j into TMEM (A = P K-major, B = V MN-major);
+//     tcgen05.commit signals completion on mbarriers; S_{j+1} is issued before P_j V_j so the
+//     tensor cores work while the softmax warps run,
+//   * softmax (warps 0-7; a TMEM lane is a row, split between two threads that take 64 columns
+//     each and trade their maxima through shared memory): read S_j with tcgen05.ld, scale by
+//     scale*log2(e), causal mask with a select, online softmax in exp2, write P_j (fp16) to
+//     swizzled shared memory.  The running max is only raised (and O rescaled in TMEM) when it
+//     grows by more than 8 in log2 units, so P stays <= 256, well inside fp16.
+// V rows past the last visible key of the chunk are zeroed in shared memory before the last
+// P V product (0 * NaN would poison the sum).  Every wait is bounded.
 #include "pa_common.cuh"
 #include "pa_kernels.h"
 
 namespace pa {
 namespace {
 
-template <int D, int BS>
+template <int D>
 struct PrefillCfg {
-  static constexpr int kConsumers = 8;
-  static constexpr int kThreads = (kConsumers + 1) * 32;
-  static constexpr int kRows = kConsumers * 16;
-  static constexpr int kKeys = 64;
+  static constexpr int kRows = 128;  // MMA M: (query token, head) rows of the tile
+  static constexpr int kKeys = 128;  // keys per K/V tile: N of S, K of P V
   static constexpr int kUnits = kKeys / 16;
-  static constexpr int kHalves = D / 64;
-  static constexpr int kBoxBytes = 16 * 128;
-  static constexpr int kUnitBytes = kHalves * kBoxBytes;
-  static constexpr int kTileBytes = kUnits * kUnitBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = 2;
-  static constexpr int kDK = D / 16;
-  static constexpr int kDN = D / 8;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
-  static_assert(BS % 16 == 0, "block size must be a multiple of the 16-token unit");
+  static constexpr int kHalves = D / 64;                  // 128-byte column chunks of a row
+  static constexpr int kHalfBytes = kRows * 128;          // one 64-column chunk of a 128-row tile
+  static constexpr int kQBytes = kHalves * kHalfBytes;    // [half][row][128 B]
+  static constexpr int kKVBytes = kHalves * kKeys * 128;  // K (or V) tile, [half][key][128 B]
+  static constexpr int kStages = 2;                       // per ring (K and V separately)
+  static constexpr int kPBytes = 2 * kHalfBytes;          // P: 128 keys = 2 key chunks
+  static constexpr int kSmemBytes = kQBytes + 2 * kStages * kKVBytes + kPBytes + 1024;
+  static constexpr int kSoftmax = 256;                    // 8 softmax warps: 2 per row quarter
+  static constexpr int kThreads = kSoftmax + 3 * 32;      // + K producer, V producer, MMA
+  static constexpr uint32_t kTmemCols = 512;              // S0 [0,128) S1 [128,256) O [256,+d)
+  static constexpr uint32_t kOCol = 256;
+  static constexpr float kRescaleLog2 = 8.f;              // raise the max only past 2^8
 };
 
-__device__ __forceinline__ uint32_t ldg_u32(const __half* p) {
-  return __ldg(reinterpret_cast<const unsigned int*>(p));
-}
-
 template <int D, int BS>
-__global__ void __launch_bounds__(PrefillCfg<D, BS>::kThreads, 1)
-    prefill_chunk_kernel(const __grid_constant__ CUtensorMap kmap,
-                         const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
-  using C = PrefillCfg<D, BS>;
+__global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
+    prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
+  using C = PrefillCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[C::kStages];
-  __shared__ __align__(8) uint64_t empty_bar[C::kStages];
+  __shared__ __align__(8) uint64_t k_full[C::kStages], k_empty[C::kStages];
+  __shared__ __align__(8) uint64_t v_full[C::kStages], v_empty[C::kStages];
+  __shared__ __align__(8) uint64_t s_full[2], s_free[2];
+  __shared__ __align__(8) uint64_t q_full, p_full, o_done, drain;
+  __shared__ uint32_t tmem_base;
+  __shared__ float red_max[2][2][128];  // [tile parity][column half][row]
+  __shared__ float red_l[2][128];
+  __shared__ int softmax_stop;  // set by a softmax thread whose wait gave up
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t q_s = smem_addr(smem);
+  const uint32_t k_s = q_s + C::kQBytes;                 // K ring
+  const uint32_t v_s = k_s + C::kStages * C::kKVBytes;   // V ring
+  const uint32_t p_s = v_s + C::kStages * C::kKVBytes;
   const int qt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -71,229 +87,336 @@ __global__ void __launch_bounds__(PrefillCfg<D, BS>::kThreads, 1)
   }
   if (qbase >= q_len) return;
   const int ctx = L - q_len;
-  const int q_hi = min(q_len, qbase + tile_q);  // rows [qbase, q_hi) of the chunk
-  const int kend = ctx + q_hi;                  // keys [0, kend) are visible to some row
+  const int q_hi = min(q_len, qbase + tile_q);
+  const int kend = ctx + q_hi;  // keys [0, kend) are visible to some row of the tile
   const int ntiles = (kend + C::kKeys - 1) / C::kKeys;
 
-  // Validate every block id the CTA will read before any copy is issued.
+  // Every block id the CTA will read is checked before any copy is issued.
   int bad = 0;
   const int nblk = (kend + BS - 1) / BS;
   for (int j = tid; j < nblk; j += C::kThreads) {
     const int32_t blk = a.block_tables[static_cast<int64_t>(s) * a.bt_stride + j];
     if (blk < 0 || blk >= a.num_blocks) bad = 1;
   }
-  if (tid == 0) {
-#pragma unroll
-    for (int st = 0; st < C::kStages; ++st) {
-      mbar_init(smem_addr(&full_bar[st]), 1);
-      mbar_init(smem_addr(&empty_bar[st]), C::kConsumers);
-    }
-    mbar_init_fence();
-  }
   if (__syncthreads_or(bad)) {
     if (tid == 0) atomicOr(a.err, kErrBlockRange);
     return;
   }
-  const uint32_t ring = smem_addr(smem);
 
-  if (warp == C::kConsumers) {
-    // ------------------------------------------------------------ producer warp
-    if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < ntiles; ++i) {
-        const int st = i % C::kStages;
-        if (i >= C::kStages && !mbar_wait(smem_addr(&empty_bar[st]), ((i / C::kStages) - 1) & 1, a.err))
-          break;
-        const int key0 = i * C::kKeys;
-        const int units = min(C::kUnits, (kend - key0 + 15) >> 4);
-        const uint32_t bar = smem_addr(&full_bar[st]);
-        mbar_arrive_expect_tx(bar, units * 2 * C::kUnitBytes);
-        const uint32_t kdst = ring + st * C::kStageBytes;
-        for (int u = 0; u < units; ++u) {
-          const int tok = key0 + u * 16;
-          const int32_t blk = a.block_tables[static_cast<int64_t>(s) * a.bt_stride + tok / BS];
-          const int y = (blk * a.num_kv_heads + g) * BS + (tok % BS);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_base)),
+                 "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int st = 0; st < C::kStages; ++st) {
+      mbar_init(smem_addr(&k_full[st]), 1);
+      mbar_init(smem_addr(&k_empty[st]), 1);
+      mbar_init(smem_addr(&v_full[st]), 1);
+      mbar_init(smem_addr(&v_empty[st]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&s_full[b]), 1);
+      mbar_init(smem_addr(&s_free[b]), C::kSoftmax);
+    }
+    mbar_init(smem_addr(&q_full), C::kSoftmax);
+    mbar_init(smem_addr(&p_full), C::kSoftmax);
+    mbar_init(smem_addr(&o_done), 1);
+    mbar_init(smem_addr(&drain), 1);
+    mbar_init_fence();
+    softmax_stop = 0;
+  }
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  constexpr int kKWarp = C::kSoftmax / 32, kVWarp = kKWarp + 1, kMmaWarp = kKWarp + 2;
+  if (warp == kKWarp || warp == kVWarp) {
+    // ============================================================== producer warps (K, V)
+    const bool is_v = warp == kVWarp;
+    uint64_t* full = is_v ? v_full : k_full;
+    uint64_t* empty = is_v ? v_empty : k_empty;
+    const uint32_t ring = is_v ? v_s : k_s;
+    const CUtensorMap* map = is_v ? &vmap : &kmap;
+    int issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      bool ok = true;
+      if (lane == 0 && j >= C::kStages)
+        ok = mbar_wait(smem_addr(&empty[st]), ((j >> 1) - 1) & 1, a.err);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      const int key0 = j * C::kKeys;
+      const int units = min(C::kUnits, (kend - key0 + 15) >> 4);
+      const int id = lane < units
+                         ? a.block_tables[static_cast<int64_t>(s) * a.bt_stride + (key0 + 16 * lane) / BS]
+                         : 0;
+      const uint32_t bar = smem_addr(&full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(bar, units * C::kHalves * 2048);
+      const uint32_t dst = ring + st * C::kKVBytes;
+      for (int u = 0; u < units; ++u) {
+        const int blk = __shfl_sync(0xffffffffu, id, u);
+        if (lane == 0) {
+          const int y = (blk * a.num_kv_heads + g) * BS + ((key0 + 16 * u) % BS);
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h) {
-            tma_load_2d(kdst + u * C::kUnitBytes + h * C::kBoxBytes, &kmap, h * 64, y, bar);
-            tma_load_2d(kdst + C::kTileBytes + u * C::kUnitBytes + h * C::kBoxBytes, &vmap,
-                        h * 64, y, bar);
-          }
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_2d(dst + h * (C::kKeys * 128) + u * 2048, map, h * 64, y, bar);
         }
-        issued = i + 1;
       }
-      // Let the last copies land before the CTA can retire (bounded).
-      for (int i = max(0, issued - C::kStages); i < issued; ++i)
-        mbar_wait(smem_addr(&full_bar[i % C::kStages]), (i / C::kStages) & 1, a.err);
+      issued = j + 1;
     }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumer warps
-  const int gq = lane >> 2, cq = lane & 3;
-  const int mi = lane >> 3, mr = lane & 7;
-  // Rows owned by this lane: R0 = warp*16 + gq and R1 = R0 + 8 -> (query token, head).
-  int qi[2], hg[2], pos[2];
-  bool rv[2];
+    // No copy may land after the CTA retires: wait (bounded) for the last tiles issued.
+    if (lane == 0)
+      for (int j = max(0, issued - C::kStages); j < issued; ++j)
+        mbar_wait(smem_addr(&full[j & 1]), (j >> 1) & 1, a.err);
+  } else if (warp == kMmaWarp) {
+    // ============================================================== MMA warp (one thread)
+    constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0);
+    constexpr uint32_t kIdO = umma_idesc_f16(C::kRows, D, 0, 1);
+    auto wait1 = [&](uint64_t* bar, int parity) {  // lane 0 waits, the warp learns the outcome
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(smem_addr(bar), parity, a.err);
+      return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    };
+    auto issue_s = [&](int j) {  // S_j = Q K_j^T into TMEM buffer j & 1; frees K stage j & 1
+      if (lane == 0) {
+        const uint32_t kst = k_s + (j & 1) * C::kKVBytes;
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int R = warp * 16 + gq + 8 * e;
-    qi[e] = R / a.group;
-    hg[e] = R % a.group;
-    rv[e] = qi[e] < tile_q && qbase + qi[e] < q_len;
-    pos[e] = ctx + (rv[e] ? qbase + qi[e] : qbase);  // padding rows mirror the first row
-  }
-  // Q as the A operand (row-major 16 x 16 per k step), kept in registers.
-  uint32_t qa[C::kDK][4];
-  {
-    const __half* qp[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-      qp[e] = a.q + static_cast<int64_t>(row0 + qbase + (rv[e] ? qi[e] : 0)) * a.q_stride +
-              static_cast<int64_t>(g * a.group + hg[e]) * D;
-#pragma unroll
-    for (int j = 0; j < C::kDK; ++j) {
-      qa[j][0] = rv[0] ? ldg_u32(qp[0] + j * 16 + 2 * cq) : 0u;
-      qa[j][1] = rv[1] ? ldg_u32(qp[1] + j * 16 + 2 * cq) : 0u;
-      qa[j][2] = rv[0] ? ldg_u32(qp[0] + j * 16 + 8 + 2 * cq) : 0u;
-      qa[j][3] = rv[1] ? ldg_u32(qp[1] + j * 16 + 8 + 2 * cq) : 0u;
-    }
-  }
-
-  float o[C::kDN][4];
-#pragma unroll
-  for (int dn = 0; dn < C::kDN; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  const int min_pos = ctx + qbase;  // keys up to here are visible to every row of the tile
-  bool failed = false;
-
-  for (int i = 0; i < ntiles; ++i) {
-    const int st = i % C::kStages;
-    const bool ok = mbar_wait(smem_addr(&full_bar[st]), (i / C::kStages) & 1, a.err);
-    if (__any_sync(0xffffffffu, !ok)) {
-      failed = true;
-      break;
-    }
-    const uint32_t kb = ring + st * C::kStageBytes;
-    const uint32_t vb = kb + C::kTileBytes;
-    const int key0 = i * C::kKeys;
-
-    // ---- S[16 rows][64 keys] = Q K^T
-    float sacc[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-#pragma unroll
-    for (int j = 0; j < C::kDK; ++j) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int row = mr + ((mi >> 1) << 3);  // key within the 16-key unit np
-        const int chunk = 2 * j + (mi & 1);
-        uint32_t bf[4];
-        ldsm_x4(kb + np * C::kUnitBytes + (chunk >> 3) * C::kBoxBytes + swz128(row, chunk & 7), bf);
-        mma_f16_16816(sacc[2 * np], qa[j], bf[0], bf[1]);
-        mma_f16_16816(sacc[2 * np + 1], qa[j], bf[2], bf[3]);
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * C::kHalfBytes + (k & 3) * 32;
+          umma_f16(tmem + (j & 1) * 128, umma_sdesc(q_s + off, 16, 1024),
+                   umma_sdesc(kst + (k >> 2) * (C::kKeys * 128) + (k & 3) * 32, 16, 1024), kIdS,
+                   k > 0);
+        }
+        umma_commit(smem_addr(&s_full[j & 1]));
+        umma_commit(smem_addr(&k_empty[j & 1]));
       }
+      __syncwarp();
+    };
+    bool ok = wait1(&q_full, 0) && wait1(&k_full[0], 0);
+    if (ok) {
+      tmem_fence_after_sync();
+      issue_s(0);
     }
-
-    // ---- causal mask + online softmax (rows gq and gq+8 of this warp)
-    const bool need_mask = key0 + C::kKeys - 1 > min_pos;
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int e = c >> 1;
-        const int key = key0 + nt * 8 + 2 * cq + (c & 1);
-        float v = sacc[nt][c] * a.scale_log2;
-        if (need_mask) v = key <= pos[e] ? v : -INFINITY;
-        sacc[nt][c] = v;
-        mx[e] = fmaxf(mx[e], v);
+    for (int j = 0; ok && j < ntiles; ++j) {
+      if (j + 1 < ntiles) {
+        const int j1 = j + 1;
+        ok = wait1(&k_full[j1 & 1], (j1 >> 1) & 1) &&
+             (j1 < 2 || wait1(&s_free[j1 & 1], ((j1 >> 1) - 1) & 1));
+        if (!ok) break;
+        tmem_fence_after_sync();
+        issue_s(j1);
       }
-    }
-    float al[2];
+      ok = wait1(&p_full, j & 1) && wait1(&v_full[j & 1], (j >> 1) & 1);
+      if (!ok) break;
+      tmem_fence_after_sync();
+      if (lane == 0) {
+        const uint32_t vst = v_s + (j & 1) * C::kKVBytes;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      mx[e] = warp_max_xor(mx[e], 1);
-      mx[e] = warp_max_xor(mx[e], 2);
-      const float mn = fmaxf(m_run[e], mx[e]);
-      al[e] = exp2f(m_run[e] - mn);
-      m_run[e] = mn;
-    }
-    float ls[2] = {0.f, 0.f};
-    uint32_t pa[4][4];  // P as the A operand for the 4 k-steps of 16 keys
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const float p0 = exp2f(sacc[nt][0] - m_run[0]);
-      const float p1 = exp2f(sacc[nt][1] - m_run[0]);
-      const float p2 = exp2f(sacc[nt][2] - m_run[1]);
-      const float p3 = exp2f(sacc[nt][3] - m_run[1]);
-      ls[0] += p0 + p1;
-      ls[1] += p2 + p3;
-      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_half2(p0, p1);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_half2(p2, p3);
-    }
-    l_run[0] = l_run[0] * al[0] + ls[0];
-    l_run[1] = l_run[1] * al[1] + ls[1];
-#pragma unroll
-    for (int dn = 0; dn < C::kDN; ++dn) {
-      o[dn][0] *= al[0];
-      o[dn][1] *= al[0];
-      o[dn][2] *= al[1];
-      o[dn][3] *= al[1];
-    }
-
-    // ---- O[16 rows][d] += P V ; V rows at or past kend are zeroed (they may hold NaN)
-    const bool tail = key0 + C::kKeys > kend;
-#pragma unroll
-    for (int kt = 0; kt < 4; ++kt) {
-      uint32_t m_lo = 0xffffffffu, m_hi = 0xffffffffu;
-      if (tail) {
-        const int k_lo = key0 + kt * 16 + 2 * cq, k_hi = k_lo + 8;
-        m_lo = (k_lo < kend ? 0x0000ffffu : 0u) | (k_lo + 1 < kend ? 0xffff0000u : 0u);
-        m_hi = (k_hi < kend ? 0x0000ffffu : 0u) | (k_hi + 1 < kend ? 0xffff0000u : 0u);
+        for (int k = 0; k < C::kKeys / 16; ++k) {
+          const uint32_t poff = (k >> 2) * C::kHalfBytes + (k & 3) * 32;
+          umma_f16(tmem + C::kOCol, umma_sdesc(p_s + poff, 16, 1024),
+                   umma_sdesc(vst + k * 16 * 128, C::kKeys * 128, 1024), kIdO, (j > 0 || k > 0));
+        }
+        umma_commit(smem_addr(&o_done));
+        umma_commit(smem_addr(&v_empty[j & 1]));
       }
-#pragma unroll
-      for (int dp = 0; dp < C::kDK; ++dp) {
-        const int row = mr + ((mi & 1) << 3);
-        const int chunk = 2 * dp + (mi >> 1);
-        uint32_t bf[4];
-        ldsm_x4_trans(vb + kt * C::kUnitBytes + (chunk >> 3) * C::kBoxBytes + swz128(row, chunk & 7), bf);
-        bf[0] &= m_lo;
-        bf[1] &= m_hi;
-        bf[2] &= m_lo;
-        bf[3] &= m_hi;
-        mma_f16_16816(o[2 * dp], pa[kt], bf[0], bf[1]);
-        mma_f16_16816(o[2 * dp + 1], pa[kt], bf[2], bf[3]);
-      }
+      __syncwarp();
+    }
+    // Every MMA this thread issued has finished before the CTA tears down (bounded).
+    if (lane == 0) {
+      umma_commit(smem_addr(&drain));
+      mbar_wait(smem_addr(&drain), 0, a.err);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[st]));
-  }
-  if (failed) return;
+  } else {
+    // ============================================================== softmax warps 0-7
+    // Warps w and w+4 share TMEM lanes 32(w%4) .. +31 (one row per lane); warp w takes the
+    // row's columns half ch = w / 4 of S, P and O.  The two halves of a row exchange their
+    // maxima through shared memory, so both take identical rescale decisions.
+    constexpr int kHalfCols = C::kKeys / 2;   // S / P columns per thread
+    constexpr int kOHalf = D / 2;             // O columns per thread
+    const int ch = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;     // TMEM lane = tile row
+    const int qi = r / a.group, hg = r % a.group;
+    const bool rv = qi < tile_q && qbase + qi < q_len;
+    const int pos = ctx + (rv ? qbase + qi : qbase);  // padding rows mirror the first row
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    auto sync_softmax = [] { asm volatile("bar.sync 1, %0;" ::"n"(C::kSoftmax) : "memory"); };
 
+    // This thread's half of the Q row -> shared memory, 128B-swizzled K-major.
+    {
+      const __half* qrow = a.q + static_cast<int64_t>(row0 + qbase + (rv ? qi : 0)) * a.q_stride +
+                           static_cast<int64_t>(g * a.group + hg) * D;
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 1);
-    l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 2);
+      for (int cc = 0; cc < D / 16; ++cc) {
+        const int c = ch * (D / 16) + cc;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (rv) v = __ldg(reinterpret_cast<const uint4*>(qrow + c * 8));
+        const uint32_t dst = q_s + (c >> 3) * C::kHalfBytes + swz128(r, c & 7);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+      }
+      fence_proxy_async();
+      mbar_arrive(smem_addr(&q_full));
+    }
+
+    // A failed (timed-out) wait sets softmax_stop; every softmax thread still reaches the next
+    // named barrier and all of them leave the loop together after it, so none is left waiting.
+    auto note = [&](bool ok) {
+      if (!ok) softmax_stop = 1;
+    };
+    float m_run = -INFINITY, l_run = 0.f;
+    const int min_pos = ctx + qbase;
+    for (int j = 0; j < ntiles; ++j) {
+      const int b = j & 1;
+      note(mbar_wait(smem_addr(&s_full[b]), (j >> 1) & 1, a.err));
+      tmem_fence_after_sync();
+      uint32_t sv[kHalfCols / 32][32];
+#pragma unroll
+      for (int qq = 0; qq < kHalfCols / 32; ++qq)
+        tmem_ld32(tmem + lane_addr + b * 128 + ch * kHalfCols + qq * 32, sv[qq]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int qq = 0; qq < kHalfCols / 32; ++qq) tmem_regs_ready(sv[qq]);
+      tmem_fence_before_sync();
+      mbar_arrive(smem_addr(&s_free[b]));  // buffer b may take S_{j+2}
+
+      const int key0 = j * C::kKeys + ch * kHalfCols;
+      const bool masked = key0 + kHalfCols - 1 > min_pos;
+      float x[kHalfCols];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kHalfCols; ++c) {
+        float v = __uint_as_float(sv[c >> 5][c & 31]) * a.scale_log2;
+        if (masked) v = key0 + c <= pos ? v : -INFINITY;
+        x[c] = v;
+        mx = fmaxf(mx, v);
+      }
+      red_max[b][ch][r] = mx;
+      sync_softmax();
+      if (*reinterpret_cast<volatile int*>(&softmax_stop)) break;
+      mx = fmaxf(mx, red_max[b][ch ^ 1][r]);
+      float alpha = 1.f;
+      if (m_run == -INFINITY || mx > m_run + C::kRescaleLog2) {
+        const float m_new = fmaxf(m_run, mx);
+        alpha = exp2f(m_run - m_new);  // 0 on the first tile
+        m_run = m_new;
+      }
+
+      // P_{j-1} V_{j-1} must be done before P is overwritten or O rescaled.
+      if (j > 0) {
+        note(mbar_wait(smem_addr(&o_done), (j - 1) & 1, a.err));
+        tmem_fence_after_sync();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c0 = 0; c0 < kOHalf; c0 += 32) {
+            uint32_t t[32];
+            const uint32_t ta = tmem + lane_addr + C::kOCol + ch * kOHalf + c0;
+            tmem_ld32(ta, t);
+            tmem_wait_ld();
+            tmem_regs_ready(t);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) t[c] = __float_as_uint(__uint_as_float(t[c]) * alpha);
+            tmem_st32(ta, t);
+          }
+          tmem_wait_st();
+        }
+      }
+
+      // This half of P_j (fp16) -> shared memory (key chunk ch); l keeps the unrounded p.
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kHalfCols / 8; ++c) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = exp2f(x[c * 8 + e] - m_run);
+          psum += p[e];
+        }
+        const uint32_t dst = p_s + ch * C::kHalfBytes + swz128(r, c);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                     "r"(pack_half2(p[0], p[1])), "r"(pack_half2(p[2], p[3])),
+                     "r"(pack_half2(p[4], p[5])), "r"(pack_half2(p[6], p[7]))
+                     : "memory");
+      }
+      l_run = l_run * alpha + psum;
+
+      const int tile0 = j * C::kKeys;
+      if (j == ntiles - 1 && tile0 + C::kKeys > kend) {
+        // The last tile: V rows at or past kend may be stale or NaN; zero them once the tile
+        // has landed (the MMA reads V only after p_full below).  Thread (r, ch) clears the
+        // 64-column chunks h with h % 2 == ch of V row r.
+        const bool landed = mbar_wait(smem_addr(&v_full[j & 1]), (j >> 1) & 1, a.err);
+        note(landed);
+        if (landed && tile0 + r >= kend) {
+          const uint32_t vrow = v_s + (j & 1) * C::kKVBytes + r * 128;
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h) {
+            if ((h & 1) != ch) continue;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               vrow + h * (C::kKeys * 128) + c * 16),
+                           "r"(0u), "r"(0u), "r"(0u), "r"(0u)
+                           : "memory");
+          }
+        }
+      }
+      fence_proxy_async();
+      tmem_fence_before_sync();
+      mbar_arrive(smem_addr(&p_full));
+    }
+
+    // l of the whole row = the two halves' partial sums (same max, same rescales).
+    red_l[ch][r] = l_run;
+    sync_softmax();
+    const float l_row = l_run + red_l[ch ^ 1][r];
+    bool ok = !*reinterpret_cast<volatile int*>(&softmax_stop);
+    if (ok) ok = mbar_wait(smem_addr(&o_done), (ntiles - 1) & 1, a.err);
+    if (!__any_sync(0xffffffffu, !ok)) {
+      tmem_fence_after_sync();
+      const float inv = 1.f / l_row;
+      __half* dst = a.out + (static_cast<int64_t>(row0 + qbase + qi) * a.num_q_heads +
+                             g * a.group + hg) * D + ch * kOHalf;
+#pragma unroll
+      for (int c0 = 0; c0 < kOHalf; c0 += 32) {
+        uint32_t t[32];
+        tmem_ld32(tmem + lane_addr + C::kOCol + ch * kOHalf + c0, t);
+        tmem_wait_ld();
+        tmem_regs_ready(t);
+        if (rv) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 v;
+            v.x = pack_half2(__uint_as_float(t[c]) * inv, __uint_as_float(t[c + 1]) * inv);
+            v.y = pack_half2(__uint_as_float(t[c + 2]) * inv, __uint_as_float(t[c + 3]) * inv);
+            v.z = pack_half2(__uint_as_float(t[c + 4]) * inv, __uint_as_float(t[c + 5]) * inv);
+            v.w = pack_half2(__uint_as_float(t[c + 6]) * inv, __uint_as_float(t[c + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c0 + c) = v;
+          }
+        }
+      }
+    }
   }
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    if (!rv[e]) continue;
-    const float inv = 1.f / l_run[e];
-    __half* dst = a.out + (static_cast<int64_t>(row0 + qbase + qi[e]) * a.num_q_heads +
-                           g * a.group + hg[e]) * D;
-#pragma unroll
-    for (int dn = 0; dn < C::kDN; ++dn)
-      *reinterpret_cast<uint32_t*>(dst + dn * 8 + 2 * cq) =
-          pack_half2(o[dn][2 * e] * inv, o[dn][2 * e + 1] * inv);
-  }
+
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::kTmemCols)
+                 : "memory");
 }
 
 template <int D, int BS>
 cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
-  using C = PrefillCfg<D, BS>;
-  auto kern = prefill_chunk_kernel<D, BS>;
+  using C = PrefillCfg<D>;
+  auto kern = prefill_umma_kernel<D, BS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
