@@ -8,17 +8,21 @@
 // Work item = one CTA = (q tile, kv head g, sequence s).  Its 128 rows are (query token, head of
 // the GQA group) pairs, so one K/V tile serves every head of the group.  Warp roles:
 //   * producers (warps 8 and 9): stream 128-key K and V tiles (8 units of 16 tokens gathered
-//     through the block table, 128-byte-swizzled TMA boxes) into separate 2-stage rings; a K
-//     stage is released as soon as its S = Q K^T is done, a V stage after its P V,
-//   * MMA (warp 10, one thread): S_j = Q K_j^T into one of two TMEM buffers (M 128, N 128, K d,
-//     both operands K-major) and O += P_j V_j into TMEM (A = P K-major, B = V MN-major);
-//     tcgen05.commit signals completion on mbarriers; S_{j+1} is issued before P_j V_j so the
-//     tensor cores work while the softmax warps run,
+//     through the block table, 128-byte-swizzled TMA boxes) into separate rings (3 K stages,
+//     2 V stages); a K stage is released as soon as its S = Q K^T is done, a V stage after P V,
+//   * MMA (warp 10, one thread): S_j = Q K_j^T into TMEM buffer j % 2 (M 128, N 128, K d, both
+//     operands K-major from shared memory), and O += P_j V_j with P_j read from TMEM (it
+//     overwrites the first 64 columns of S_j's buffer, two fp16 per column) and V_j MN-major
+//     from shared memory.  The issue order S_0, S_1, PV_0, S_2, PV_1, S_3, ... lets the tensor
+//     pipe work on S_{j+1} and P_{j-1} V_{j-1} while the softmax warps handle tile j, and since
+//     tcgen05 MMAs of one thread run in issue order, S_{j+2} never overwrites P_j before P_j V_j
+//     has read it,
 //   * softmax (warps 0-7; a TMEM lane is a row, split between two threads that take 64 columns
 //     each and trade their maxima through shared memory): read S_j with tcgen05.ld, scale by
-//     scale*log2(e), causal mask with a select, online softmax in exp2, write P_j (fp16) to
-//     swizzled shared memory.  The running max is only raised (and O rescaled in TMEM) when it
-//     grows by more than 8 in log2 units, so P stays <= 256, well inside fp16.
+//     scale*log2(e), causal mask with a select, online softmax in base 2, write P_j (fp16) back
+//     to TMEM.  The running max is only raised (and O rescaled in TMEM) when it grows by more
+//     than 8 in log2 units, so P stays <= 256, well inside fp16; only then does the softmax
+//     wait for the previous P V product.
 // V rows past the last visible key of the chunk are zeroed in shared memory before the last
 // P V product (0 * NaN would poison the sum).  Every wait is bounded.
 #include "pa_common.cuh"
@@ -36,12 +40,12 @@ struct PrefillCfg {
   static constexpr int kHalfBytes = kRows * 128;          // one 64-column chunk of a 128-row tile
   static constexpr int kQBytes = kHalves * kHalfBytes;    // [half][row][128 B]
   static constexpr int kKVBytes = kHalves * kKeys * 128;  // K (or V) tile, [half][key][128 B]
-  static constexpr int kStages = 2;                       // per ring (K and V separately)
-  static constexpr int kPBytes = 2 * kHalfBytes;          // P: 128 keys = 2 key chunks
-  static constexpr int kSmemBytes = kQBytes + 2 * kStages * kKVBytes + kPBytes + 1024;
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 2;
+  static constexpr int kSmemBytes = kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
   static constexpr int kSoftmax = 256;                    // 8 softmax warps: 2 per row quarter
   static constexpr int kThreads = kSoftmax + 3 * 32;      // + K producer, V producer, MMA
-  static constexpr uint32_t kTmemCols = 512;              // S0 [0,128) S1 [128,256) O [256,+d)
+  static constexpr uint32_t kTmemCols = 512;              // S/P 0 [0,128) S/P 1 [128,256) O [256,+d)
   static constexpr uint32_t kOCol = 256;
   static constexpr float kRescaleLog2 = 8.f;              // raise the max only past 2^8
 };
@@ -52,9 +56,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                         const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
   using C = PrefillCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t k_full[C::kStages], k_empty[C::kStages];
-  __shared__ __align__(8) uint64_t v_full[C::kStages], v_empty[C::kStages];
-  __shared__ __align__(8) uint64_t s_full[2], s_free[2];
+  __shared__ __align__(8) uint64_t k_full[C::kKStages], k_empty[C::kKStages];
+  __shared__ __align__(8) uint64_t v_full[C::kVStages], v_empty[C::kVStages];
+  __shared__ __align__(8) uint64_t s_full[2];
   __shared__ __align__(8) uint64_t q_full, p_full, o_done, drain;
   __shared__ uint32_t tmem_base;
   __shared__ float red_max[2][2][128];  // [tile parity][column half][row]
@@ -64,10 +68,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t q_s = smem_addr(smem);
-  const uint32_t k_s = q_s + C::kQBytes;                 // K ring
-  const uint32_t v_s = k_s + C::kStages * C::kKVBytes;   // V ring
-  const uint32_t p_s = v_s + C::kStages * C::kKVBytes;
-  const int qt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const uint32_t k_s = q_s + C::kQBytes;                  // K ring
+  const uint32_t v_s = k_s + C::kKStages * C::kKVBytes;   // V ring
+  // Later q tiles of a chunk see more keys: dispatch them first so the grid's tail is short.
+  const int qt = gridDim.x - 1 - blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int row0 = a.query_start_loc[s];
@@ -111,16 +115,16 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    for (int st = 0; st < C::kStages; ++st) {
+    for (int st = 0; st < C::kKStages; ++st) {
       mbar_init(smem_addr(&k_full[st]), 1);
       mbar_init(smem_addr(&k_empty[st]), 1);
+    }
+    for (int st = 0; st < C::kVStages; ++st) {
       mbar_init(smem_addr(&v_full[st]), 1);
       mbar_init(smem_addr(&v_empty[st]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_addr(&s_full[b]), 1);
-      mbar_init(smem_addr(&s_free[b]), C::kSoftmax);
-    }
+    mbar_init(smem_addr(&s_full[0]), 1);
+    mbar_init(smem_addr(&s_full[1]), 1);
     mbar_init(smem_addr(&q_full), C::kSoftmax);
     mbar_init(smem_addr(&p_full), C::kSoftmax);
     mbar_init(smem_addr(&o_done), 1);
@@ -137,16 +141,16 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   if (warp == kKWarp || warp == kVWarp) {
     // ============================================================== producer warps (K, V)
     const bool is_v = warp == kVWarp;
+    const int stages = is_v ? C::kVStages : C::kKStages;
     uint64_t* full = is_v ? v_full : k_full;
     uint64_t* empty = is_v ? v_empty : k_empty;
     const uint32_t ring = is_v ? v_s : k_s;
     const CUtensorMap* map = is_v ? &vmap : &kmap;
     int issued = 0;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j & 1;
+      const int st = j % stages, round = j / stages;
       bool ok = true;
-      if (lane == 0 && j >= C::kStages)
-        ok = mbar_wait(smem_addr(&empty[st]), ((j >> 1) - 1) & 1, a.err);
+      if (lane == 0 && round > 0) ok = mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       const int key0 = j * C::kKeys;
       const int units = min(C::kUnits, (kend - key0 + 15) >> 4);
@@ -169,8 +173,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     }
     // No copy may land after the CTA retires: wait (bounded) for the last tiles issued.
     if (lane == 0)
-      for (int j = max(0, issued - C::kStages); j < issued; ++j)
-        mbar_wait(smem_addr(&full[j & 1]), (j >> 1) & 1, a.err);
+      for (int j = max(0, issued - stages); j < issued; ++j)
+        mbar_wait(smem_addr(&full[j % stages]), (j / stages) & 1, a.err);
   } else if (warp == kMmaWarp) {
     // ============================================================== MMA warp (one thread)
     constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0);
@@ -180,9 +184,13 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       if (lane == 0) ok = mbar_wait(smem_addr(bar), parity, a.err);
       return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     };
-    auto issue_s = [&](int j) {  // S_j = Q K_j^T into TMEM buffer j & 1; frees K stage j & 1
+    // S_j = Q K_j^T into TMEM buffer j % 2; frees K stage j % 3 once done.
+    auto issue_s = [&](int j) {
+      const int st = j % C::kKStages;
+      if (!wait1(&k_full[st], (j / C::kKStages) & 1)) return false;
+      tmem_fence_after_sync();
       if (lane == 0) {
-        const uint32_t kst = k_s + (j & 1) * C::kKVBytes;
+        const uint32_t kst = k_s + st * C::kKVBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * C::kHalfBytes + (k & 3) * 32;
@@ -191,41 +199,31 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                    k > 0);
         }
         umma_commit(smem_addr(&s_full[j & 1]));
-        umma_commit(smem_addr(&k_empty[j & 1]));
+        umma_commit(smem_addr(&k_empty[st]));
       }
       __syncwarp();
+      return true;
     };
-    bool ok = wait1(&q_full, 0) && wait1(&k_full[0], 0);
-    if (ok) {
-      tmem_fence_after_sync();
-      issue_s(0);
-    }
+    bool ok = wait1(&q_full, 0) && issue_s(0) && (ntiles < 2 || issue_s(1));
     for (int j = 0; ok && j < ntiles; ++j) {
-      if (j + 1 < ntiles) {
-        const int j1 = j + 1;
-        ok = wait1(&k_full[j1 & 1], (j1 >> 1) & 1) &&
-             (j1 < 2 || wait1(&s_free[j1 & 1], ((j1 >> 1) - 1) & 1));
-        if (!ok) break;
-        tmem_fence_after_sync();
-        issue_s(j1);
-      }
-      ok = wait1(&p_full, j & 1) && wait1(&v_full[j & 1], (j >> 1) & 1);
+      const int vst = j % C::kVStages;
+      ok = wait1(&p_full, j & 1) && wait1(&v_full[vst], (j / C::kVStages) & 1);
       if (!ok) break;
       tmem_fence_after_sync();
       if (lane == 0) {
-        const uint32_t vst = v_s + (j & 1) * C::kKVBytes;
+        const uint32_t vb = v_s + vst * C::kKVBytes;
 #pragma unroll
-        for (int k = 0; k < C::kKeys / 16; ++k) {
-          const uint32_t poff = (k >> 2) * C::kHalfBytes + (k & 3) * 32;
-          umma_f16(tmem + C::kOCol, umma_sdesc(p_s + poff, 16, 1024),
-                   umma_sdesc(vst + k * 16 * 128, C::kKeys * 128, 1024), kIdO, (j > 0 || k > 0));
-        }
+        for (int k = 0; k < C::kKeys / 16; ++k)
+          umma_f16_tmem_a(tmem + C::kOCol, tmem + (j & 1) * 128 + k * 8,
+                          umma_sdesc(vb + k * 16 * 128, C::kKeys * 128, 1024), kIdO,
+                          (j > 0 || k > 0));
         umma_commit(smem_addr(&o_done));
-        umma_commit(smem_addr(&v_empty[j & 1]));
+        umma_commit(smem_addr(&v_empty[vst]));
       }
       __syncwarp();
+      if (j + 2 < ntiles) ok = issue_s(j + 2);
     }
-    // Every MMA this thread issued has finished before the CTA tears down (bounded).
+    // Every MMA this thread issued has finished before O is read or the CTA tears down.
     if (lane == 0) {
       umma_commit(smem_addr(&drain));
       mbar_wait(smem_addr(&drain), 0, a.err);
@@ -234,9 +232,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   } else {
     // ============================================================== softmax warps 0-7
     // Warps w and w+4 share TMEM lanes 32(w%4) .. +31 (one row per lane); warp w takes the
-    // row's columns half ch = w / 4 of S, P and O.  The two halves of a row exchange their
-    // maxima through shared memory, so both take identical rescale decisions.
-    constexpr int kHalfCols = C::kKeys / 2;   // S / P columns per thread
+    // row's columns half ch = w / 4 of S and O.  The two halves of a row exchange their maxima
+    // through shared memory, so both take identical rescale decisions.
+    constexpr int kHalfCols = C::kKeys / 2;   // S columns per thread
     constexpr int kOHalf = D / 2;             // O columns per thread
     const int ch = warp >> 2;
     const int r = (warp & 3) * 32 + lane;     // TMEM lane = tile row
@@ -271,78 +269,87 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     };
     float m_run = -INFINITY, l_run = 0.f;
     const int min_pos = ctx + qbase;
+    const bool prescale = !(a.scale_log2 > 0.f);
+    const float mul = prescale ? 1.f : a.scale_log2;  // exponent = fma(score, mul, -m)
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
+      const uint32_t sbuf = tmem + lane_addr + b * 128;
       note(mbar_wait(smem_addr(&s_full[b]), (j >> 1) & 1, a.err));
       tmem_fence_after_sync();
       uint32_t sv[kHalfCols / 32][32];
 #pragma unroll
-      for (int qq = 0; qq < kHalfCols / 32; ++qq)
-        tmem_ld32(tmem + lane_addr + b * 128 + ch * kHalfCols + qq * 32, sv[qq]);
+      for (int qq = 0; qq < kHalfCols / 32; ++qq) tmem_ld32(sbuf + ch * kHalfCols + qq * 32, sv[qq]);
       tmem_wait_ld();
 #pragma unroll
       for (int qq = 0; qq < kHalfCols / 32; ++qq) tmem_regs_ready(sv[qq]);
-      tmem_fence_before_sync();
-      mbar_arrive(smem_addr(&s_free[b]));  // buffer b may take S_{j+2}
 
+      // Scores stay raw where scale > 0 (the max commutes with the scale, which is folded into
+      // the exponent's FMA below); otherwise they are scaled here.  Masked keys become -inf.
       const int key0 = j * C::kKeys + ch * kHalfCols;
       const bool masked = key0 + kHalfCols - 1 > min_pos;
-      float x[kHalfCols];
-      float mx = -INFINITY;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (prescale || masked) {
 #pragma unroll
-      for (int c = 0; c < kHalfCols; ++c) {
-        float v = __uint_as_float(sv[c >> 5][c & 31]) * a.scale_log2;
-        if (masked) v = key0 + c <= pos ? v : -INFINITY;
-        x[c] = v;
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < kHalfCols; ++c) {
+          float v = __uint_as_float(sv[c >> 5][c & 31]);
+          if (prescale) v *= a.scale_log2;
+          if (masked && key0 + c > pos) v = -INFINITY;
+          sv[c >> 5][c & 31] = __float_as_uint(v);
+          m4[c & 3] = fmaxf(m4[c & 3], v);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kHalfCols; ++c)
+          m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c >> 5][c & 31]));
       }
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mul;
       red_max[b][ch][r] = mx;
+      // Both halves' S loads are complete before either half writes P over them.
+      tmem_fence_before_sync();
       sync_softmax();
+      tmem_fence_after_sync();
       if (*reinterpret_cast<volatile int*>(&softmax_stop)) break;
       mx = fmaxf(mx, red_max[b][ch ^ 1][r]);
       float alpha = 1.f;
       if (m_run == -INFINITY || mx > m_run + C::kRescaleLog2) {
         const float m_new = fmaxf(m_run, mx);
-        alpha = exp2f(m_run - m_new);  // 0 on the first tile
+        alpha = ex2_approx(m_run - m_new);  // 0 on the first tile
         m_run = m_new;
       }
 
-      // P_{j-1} V_{j-1} must be done before P is overwritten or O rescaled.
-      if (j > 0) {
+      // Rescaling O needs P_{j-1} V_{j-1} to be complete (o_done's phase j-1; S_j's completion
+      // already implies P_{j-2} V_{j-2}, so the parity is unambiguous).
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         note(mbar_wait(smem_addr(&o_done), (j - 1) & 1, a.err));
         tmem_fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int c0 = 0; c0 < kOHalf; c0 += 32) {
-            uint32_t t[32];
-            const uint32_t ta = tmem + lane_addr + C::kOCol + ch * kOHalf + c0;
-            tmem_ld32(ta, t);
-            tmem_wait_ld();
-            tmem_regs_ready(t);
+        for (int c0 = 0; c0 < kOHalf; c0 += 32) {
+          uint32_t t[32];
+          const uint32_t ta = tmem + lane_addr + C::kOCol + ch * kOHalf + c0;
+          tmem_ld32(ta, t);
+          tmem_wait_ld();
+          tmem_regs_ready(t);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) t[c] = __float_as_uint(__uint_as_float(t[c]) * alpha);
-            tmem_st32(ta, t);
-          }
-          tmem_wait_st();
+          for (int c = 0; c < 32; ++c) t[c] = __float_as_uint(__uint_as_float(t[c]) * alpha);
+          tmem_st32(ta, t);
         }
       }
 
-      // This half of P_j (fp16) -> shared memory (key chunk ch); l keeps the unrounded p.
-      float psum = 0.f;
+      // This half of P_j (fp16, keys ch*64 ..) -> TMEM columns ch*32 .. of buffer b; l keeps
+      // the unrounded p.
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[32];
+      const float neg_m = -m_run;
 #pragma unroll
-      for (int c = 0; c < kHalfCols / 8; ++c) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = exp2f(x[c * 8 + e] - m_run);
-          psum += p[e];
-        }
-        const uint32_t dst = p_s + ch * C::kHalfBytes + swz128(r, c);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                     "r"(pack_half2(p[0], p[1])), "r"(pack_half2(p[2], p[3])),
-                     "r"(pack_half2(p[4], p[5])), "r"(pack_half2(p[6], p[7]))
-                     : "memory");
+      for (int c = 0; c < 32; ++c) {
+        const uint32_t* e = &sv[c >> 4][(2 * c) & 31];
+        const float p0 = ex2_approx(fmaf(__uint_as_float(e[0]), mul, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(e[1]), mul, neg_m));
+        ps[c & 3] += p0 + p1;
+        pk[c] = pack_half2(p0, p1);
       }
+      const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      tmem_st32(sbuf + ch * 32, pk);
       l_run = l_run * alpha + psum;
 
       const int tile0 = j * C::kKeys;
@@ -350,10 +357,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         // The last tile: V rows at or past kend may be stale or NaN; zero them once the tile
         // has landed (the MMA reads V only after p_full below).  Thread (r, ch) clears the
         // 64-column chunks h with h % 2 == ch of V row r.
-        const bool landed = mbar_wait(smem_addr(&v_full[j & 1]), (j >> 1) & 1, a.err);
+        const int vst = j % C::kVStages;
+        const bool landed = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err);
         note(landed);
         if (landed && tile0 + r >= kend) {
-          const uint32_t vrow = v_s + (j & 1) * C::kKVBytes + r * 128;
+          const uint32_t vrow = v_s + vst * C::kKVBytes + r * 128;
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h) {
             if ((h & 1) != ch) continue;
@@ -365,8 +373,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                            : "memory");
           }
         }
+        fence_proxy_async();
       }
-      fence_proxy_async();
+      tmem_wait_st();
       tmem_fence_before_sync();
       mbar_arrive(smem_addr(&p_full));
     }
@@ -376,7 +385,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     sync_softmax();
     const float l_row = l_run + red_l[ch ^ 1][r];
     bool ok = !*reinterpret_cast<volatile int*>(&softmax_stop);
-    if (ok) ok = mbar_wait(smem_addr(&o_done), (ntiles - 1) & 1, a.err);
+    if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err);
     if (!__any_sync(0xffffffffu, !ok)) {
       tmem_fence_after_sync();
       const float inv = 1.f / l_row;

@@ -95,6 +95,20 @@ def test_small_cases_match_oracle(name):
     assert_close(out, ref)
 
 
+@pytest.mark.parametrize("sign", [0.0, -1.0])
+@pytest.mark.parametrize("d", [128, 64])
+def test_zero_and_negative_scale_match_oracle(sign, d):
+    """The prefill softmax folds a positive scale into the exponent and pre-scales otherwise;
+    scale 0 turns every visible key's weight into 1 (the mean of V), scale -1/sqrt(d) flips
+    which key dominates.  Both, on decode and prefill rows, must agree with the oracle.  (Much
+    larger |scale| makes single keys dominate, and the fp16 rounding of outputs of magnitude 2-4
+    alone then reaches the 2e-3 bar.)"""
+    b = small_mixed(d=d, hq=16, hkv=4, seed=9230 + d)
+    b.scale = sign / float(np.sqrt(d))
+    _, _, out = gpu_step(b)
+    assert_close(out, oracle.attention_batch(b))
+
+
 @pytest.mark.parametrize("name", ["decode_d128_bs16_g4", "mixed_d128_bs32_g8", "prefix_d128_bs16"])
 def test_block_placement_is_bit_invariant(name):
     b = SMALL[name]()
