@@ -217,7 +217,7 @@ def run_ours(args, world, rank, local):
     def step(q_, k_, v_, s_, bt_, sl_, qsl_, out_):
         pa.reshape_and_cache(k_, v_, kc, vc, s_)
         pa.attention(q_, kc, vc, bt_, sl_, qsl_, b.scale, out_, b.max_query_len, b.max_seq_len,
-                     workspace=ws)
+                     workspace=ws, num_prefill_seqs=b.num_prefill_seqs)
 
     for i in range(args.warmup):
         flush.fill_(i & 255)

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PA_VERSION 1
+#define PA_VERSION 2
 #define PA_PARTITION_TOKENS 512 /* keys per split-context partition */
 #define PA_MAX_DIMS 5
 
@@ -68,8 +68,12 @@ typedef struct pa_tensor {
 /* Host-side facts about the batch the scheduler already knows.  Upper bounds are fine; a
  * sequence that exceeds them is skipped on the device and reported as PA_ERR_DESCRIPTOR. */
 typedef struct pa_batch_hint {
-  int32_t max_query_len; /* max over sequences of query_start_loc[s+1] - query_start_loc[s] */
-  int32_t max_seq_len;   /* max over sequences of seq_lens[s] */
+  int32_t max_query_len;    /* max over sequences of query_start_loc[s+1] - query_start_loc[s] */
+  int32_t max_seq_len;      /* max over sequences of seq_lens[s] */
+  int32_t num_prefill_seqs; /* count of sequences with more than one query row; 0 = not known,
+                               then the prefill launch covers every sequence.  A batch with more
+                               such sequences than this skips the extra ones and reports
+                               PA_ERR_DESCRIPTOR. */
 } pa_batch_hint;
 
 /*

@@ -42,7 +42,8 @@ class PATensor(ctypes.Structure):
 
 
 class PABatchHint(ctypes.Structure):
-    _fields_ = [("max_query_len", ctypes.c_int32), ("max_seq_len", ctypes.c_int32)]
+    _fields_ = [("max_query_len", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("num_prefill_seqs", ctypes.c_int32)]
 
 
 class PAError(RuntimeError):
@@ -135,18 +136,19 @@ def workspace_size(num_tokens: int, num_q_heads: int, head_dim: int, max_seq_len
 
 def attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale: float, out,
               max_query_len: int, max_seq_len: int, workspace: Optional[torch.Tensor] = None,
-              stream=None) -> torch.Tensor:
+              stream=None, num_prefill_seqs: int = 0) -> torch.Tensor:
     """``pa_attention`` for one mixed batch; writes ``out`` [T, Hq, d] and returns it.
 
     ``workspace`` is a caller-owned uint8 device tensor of at least ``workspace_size(...)``
-    bytes (allocated here when omitted)."""
+    bytes (allocated here when omitted).  ``num_prefill_seqs`` is the count of sequences with
+    more than one query row (0 = not known)."""
     lib = load_library()
     need = workspace_size(q.shape[0], q.shape[1], q.shape[2], max_seq_len)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wptr = workspace.data_ptr() if workspace is not None and workspace.numel() else None
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    hint = PABatchHint(int(max_query_len), int(max_seq_len))
+    hint = PABatchHint(int(max_query_len), int(max_seq_len), int(num_prefill_seqs))
     descs = [describe(x) for x in (q, k_cache, v_cache, block_tables, seq_lens, query_start_loc)]
     _check(lib.pa_attention(*[ctypes.byref(d) for d in descs], ctypes.c_float(scale),
                             ctypes.byref(describe(out)), ctypes.byref(hint), wptr, wbytes,
@@ -178,8 +180,8 @@ class BatchDescriptor:
 
     Sequences may mix prefill chunks (several query rows) and decode steps (one row) in any
     order ("vLLM: LLM Inference That Doesn't Waste Your GPU", "Continuous batching").
-    ``slot_mapping`` addresses the cache slots of this step's new tokens; ``max_query_len`` and
-    ``max_seq_len`` are the host-side hint the launch is planned from.
+    ``slot_mapping`` addresses the cache slots of this step's new tokens; ``max_query_len``,
+    ``max_seq_len`` and ``num_prefill_seqs`` are the host-side hint the launch is planned from.
     """
 
     query_start_loc: torch.Tensor
@@ -188,6 +190,7 @@ class BatchDescriptor:
     slot_mapping: torch.Tensor
     max_query_len: int
     max_seq_len: int
+    num_prefill_seqs: int = 0
 
     @classmethod
     def from_host(cls, seq_lens, query_lens, block_tables, block_size: int, device="cuda",
@@ -208,4 +211,4 @@ class BatchDescriptor:
         sm = torch.tensor(slots, dtype=torch.int64)
         dev = lambda x: x.to(device, non_blocking=non_blocking)
         return cls(dev(qsl), dev(sl), dev(bt), dev(sm), int(ql.max()) if len(ql) else 0,
-                   int(sl.max()) if len(sl) else 0)
+                   int(sl.max()) if len(sl) else 0, int((ql > 1).sum()))

@@ -268,7 +268,7 @@ int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
     return fail(PA_ERR_INVALID_ARG, "block_tables needs at least one column");
   if (block_tables->shape[1] > INT32_MAX || block_tables->stride[0] < block_tables->shape[1])
     return fail(PA_ERR_INVALID_ARG, "block_tables row stride must cover its columns");
-  if (hint->max_query_len < 0 || hint->max_seq_len < 0)
+  if (hint->max_query_len < 0 || hint->max_seq_len < 0 || hint->num_prefill_seqs < 0)
     return fail(PA_ERR_INVALID_ARG, "hint values must be non-negative");
   if (hint->max_query_len > hint->max_seq_len)
     return fail(PA_ERR_INVALID_ARG, "hint max_query_len exceeds max_seq_len");
@@ -306,6 +306,7 @@ int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   a.max_parts = static_cast<int>(
       std::max<int64_t>(1, (hint->max_seq_len + PA_PARTITION_TOKENS - 1) / PA_PARTITION_TOKENS));
   a.max_query_len = hint->max_query_len;
+  a.prefill_seqs = hint->num_prefill_seqs > 0 ? std::min<int>(hint->num_prefill_seqs, n) : n;
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaError_t e = device_error_word(&a.err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");

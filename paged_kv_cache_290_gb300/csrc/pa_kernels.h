@@ -48,6 +48,7 @@ struct AttnArgs {
   int64_t num_blocks;
   int max_parts;   // P = ceil(max_seq_len / 512) (>= 1)
   int max_query_len;
+  int prefill_seqs;  // sequences the prefill launch covers (<= num_seqs)
   float scale_log2;  // scale * log2(e)
   unsigned* err;
 };

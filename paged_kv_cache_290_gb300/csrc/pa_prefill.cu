@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   __shared__ float red_max[2][2][128];  // [tile parity][column half][row]
   __shared__ float red_l[2][128];
   __shared__ int softmax_stop;  // set by a softmax thread whose wait gave up
+  __shared__ int warp_count[PrefillCfg<D>::kThreads / 32];
+  __shared__ int chosen_seq;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -71,8 +73,36 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   const uint32_t k_s = q_s + C::kQBytes;                  // K ring
   const uint32_t v_s = k_s + C::kKStages * C::kKVBytes;   // V ring
   // Later q tiles of a chunk see more keys: dispatch them first so the grid's tail is short.
-  const int qt = gridDim.x - 1 - blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int qt = gridDim.x - 1 - blockIdx.x, g = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // Grid row z serves the z-th sequence with more than one query row (a block-wide ballot scan
+  // of query_start_loc), so decode rows cost the launch nothing.  Rows past the last such
+  // sequence have no work; more such sequences than rows is a hint error.
+  if (tid == 0) chosen_seq = -1;
+  int found = 0;  // prefill sequences seen so far
+  for (int s0 = 0; s0 < a.num_seqs; s0 += C::kThreads) {
+    const int si = s0 + tid;
+    const bool pf = si < a.num_seqs && a.query_start_loc[si + 1] - a.query_start_loc[si] > 1;
+    const unsigned bal = __ballot_sync(0xffffffffu, pf);
+    if (lane == 0) warp_count[warp] = __popc(bal);
+    __syncthreads();
+    int rank = found + __popc(bal & ((1u << lane) - 1u)), total = 0;
+#pragma unroll
+    for (int w = 0; w < C::kThreads / 32; ++w) {
+      rank += w < warp ? warp_count[w] : 0;
+      total += warp_count[w];
+    }
+    if (pf && rank == static_cast<int>(blockIdx.z)) chosen_seq = si;
+    found += total;
+    __syncthreads();
+  }
+  __syncthreads();
+  if (found > static_cast<int>(gridDim.z) && blockIdx.x == 0 && blockIdx.y == 0 &&
+      blockIdx.z == 0 && tid == 0)
+    atomicOr(a.err, kErrHint);
+  const int s = chosen_seq;
+  if (s < 0) return;
 
   const int row0 = a.query_start_loc[s];
   const int q_len = a.query_start_loc[s + 1] - row0;
@@ -430,7 +460,7 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const C
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int tile_q = C::kRows / a.group;
-  dim3 grid((a.max_query_len + tile_q - 1) / tile_q, a.num_kv_heads, a.num_seqs);
+  dim3 grid((a.max_query_len + tile_q - 1) / tile_q, a.num_kv_heads, a.prefill_seqs);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
   return cudaGetLastError();
 }

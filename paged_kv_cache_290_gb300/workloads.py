@@ -110,6 +110,10 @@ class PagedBatch:
     def max_query_len(self) -> int:
         return max((s.query_len for s in self.seqs), default=0)
 
+    @property
+    def num_prefill_seqs(self) -> int:
+        return sum(1 for s in self.seqs if s.query_len > 1)
+
 
 def build_batch(
     name: str,

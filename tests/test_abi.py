@@ -33,7 +33,7 @@ def test_header_declares_the_abi():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.pa_version() == 1
+    assert lib.pa_version() == 2
 
 
 # --------------------------------------------------------------- hand-made descriptors (no GPU)
@@ -98,6 +98,7 @@ def msg(lib):
     (dict(kc=T(B.PA_F16, [40, 2, 16, 64], data=0)), B.PA_ERR_INVALID_ARG, "NULL"),
     (dict(hint=None), B.PA_ERR_INVALID_ARG, "hint"),
     (dict(hint=(-1, 10)), B.PA_ERR_INVALID_ARG, "non-negative"),
+    (dict(hint=(1, 10, -2)), B.PA_ERR_INVALID_ARG, "non-negative"),
     (dict(hint=(20, 10)), B.PA_ERR_INVALID_ARG, "max_query_len"),
     (dict(hint=(1, 1000)), B.PA_ERR_WORKSPACE, "workspace"),
     (dict(hint=(1, 1000), ws=FAKE + 16, wsb=1 << 30), B.PA_ERR_WORKSPACE, "aligned"),
@@ -165,4 +166,4 @@ def test_batch_descriptor_from_host():
                                      block_size=16, device="cpu")
     assert d.query_start_loc.tolist() == [0, 5, 6, 8]
     assert d.slot_mapping.tolist() == [48, 49, 50, 51, 52, 4 * 16 + 7, 7 * 16 + 15, 6 * 16 + 0]
-    assert d.max_query_len == 5 and d.max_seq_len == 40
+    assert d.max_query_len == 5 and d.max_seq_len == 40 and d.num_prefill_seqs == 2

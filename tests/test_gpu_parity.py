@@ -48,7 +48,8 @@ def gpu_step(b, write=True, pool=None):
     q = b.q.to(dev)
     out = torch.full_like(q, float("nan"))
     pa.attention(q, kc, vc, b.block_tables.to(dev), b.seq_lens.to(dev),
-                 b.query_start_loc.to(dev), b.scale, out, b.max_query_len, b.max_seq_len)
+                 b.query_start_loc.to(dev), b.scale, out, b.max_query_len, b.max_seq_len,
+                 num_prefill_seqs=b.num_prefill_seqs)
     st, bits = pa.get_device_error()
     assert st == 0, (st, bits, pa.last_error())
     return kc, vc, out
@@ -189,8 +190,8 @@ def test_hint_too_small_is_reported():
 
 
 def test_workspace_reused_and_never_cleared():
-    """Partition tickets carry a per-call tag: a workspace full of random bytes, reused by three
-    calls in a row, gives the oracle's result every time."""
+    """Every partial is written before it is read: a workspace full of random bytes, reused by
+    three calls in a row, gives the oracle's result every time."""
     b = small_decode(seed=9110)
     dev = "cuda"
     need = pa.workspace_size(b.num_tokens, b.num_q_heads, b.head_dim, b.max_seq_len)
@@ -215,6 +216,31 @@ def test_prefill_longer_than_hint_is_reported():
                  b.seq_lens.to(dev), b.query_start_loc.to(dev), b.scale, out, 16, b.max_seq_len)
     st, bits = pa.get_device_error()
     assert st == pa.binding.PA_ERR_DESCRIPTOR and bits & 16
+
+
+def test_prefill_sequence_count_hint():
+    """num_prefill_seqs = 0 (not known) covers every sequence; the exact count gives the same
+    bits; a count below the batch's is reported, and the chunks it covers are still exact."""
+    b = small_mixed(seed=9214)
+    dev = "cuda"
+    assert b.num_prefill_seqs == 4
+    args = [x.to(dev) for x in (b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                                b.query_start_loc)]
+    outs = {}
+    for n in (0, 4, 2):
+        out = torch.full_like(args[0], float("nan"))
+        pa.attention(*args, b.scale, out, b.max_query_len, b.max_seq_len, num_prefill_seqs=n)
+        outs[n] = (out, pa.get_device_error())
+    assert outs[0][1] == (0, 0) and outs[4][1] == (0, 0)
+    assert torch.equal(outs[0][0], outs[4][0])
+    assert_close(outs[4][0], oracle.attention_batch(b))
+    st, bits = outs[2][1]
+    assert st == pa.binding.PA_ERR_DESCRIPTOR and bits & 16
+    # the first two prefill chunks (in batch order) and every decode row are still computed
+    covered = [s for s, spec in enumerate(b.seqs) if spec.query_len > 1][:2]
+    rows = [r for s, spec in enumerate(b.seqs) if spec.query_len == 1 or s in covered
+            for r in range(int(b.query_start_loc[s]), int(b.query_start_loc[s + 1]))]
+    assert torch.equal(outs[2][0][rows], outs[4][0][rows])
 
 
 # ------------------------------------------------------------------ the five full-size workloads
