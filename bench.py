@@ -65,24 +65,51 @@ def algorithmic_bytes(b) -> dict:
     t_new = int(b.k_new.shape[0])
     cache = 2 * t_new * hkv * d * 2 * 2 + t_new * 8
     attn = q_bytes + out_bytes + table + desc
+
+    def flops(sel):
+        return int(sum(4 * b.num_q_heads * d * (s.seq_len * s.query_len -
+                                                 s.query_len * (s.query_len - 1) // 2)
+                       for s, keep in zip(b.seqs, sel) if keep))
+
+    def kernel_bytes(sel):
+        """Unique K/V slots of the selected sequences, their Q/out rows and table entries."""
+        idx = np.nonzero(sel)[0]
+        if idx.size == 0:
+            return 0
+        uniq = np.unique(np.concatenate([slots[int(np.nonzero(np.nonzero(active)[0] == s)[0][0])]
+                                         for s in idx])).size * row_kv
+        rows = int(qlens[idx].sum())
+        return (uniq + 2 * rows * b.num_q_heads * d * 2 +
+                int(((lens[idx] + bs - 1) // bs).sum()) * 4 + desc)
+
+    dec, pre = qlens == 1, qlens > 1
     return {
         "kv_logical": kv_logical, "kv_unique": kv_unique,
         "attention_logical": kv_logical + attn, "attention_unique": kv_unique + attn,
         "reshape_and_cache": cache,
         "step_logical": kv_logical + attn + cache,
-        "decode_rows": int((qlens == 1).sum()),
-        "flops": int(sum(4 * b.num_q_heads * d * (s.seq_len * s.query_len -
-                                                   s.query_len * (s.query_len - 1) // 2)
-                         for s in b.seqs)),
+        "decode_rows": int(dec.sum()),
+        "flops": flops(active),
+        # what each attention kernel must move / compute: the decode-partition kernel serves the
+        # one-row sequences, the chunked-prefill kernel the sequences with several rows
+        "decode_kernel_bytes": kernel_bytes(dec),
+        "prefill_kernel_bytes": kernel_bytes(pre),
+        "prefill_kernel_flops": flops(pre),
     }
+
+
+def all_prefill(b) -> bool:
+    """Every sequence has several query rows: pa_attention then makes no decode launches."""
+    return b.max_query_len > 1 and b.num_prefill_seqs == b.num_seqs
 
 
 def launches_per_step(b) -> int:
     parts = max(1, math.ceil(b.max_seq_len / 512))
+    decode = not all_prefill(b)
     n = 1 if b.k_new.shape[0] > 0 else 0        # reshape_and_cache
-    n += 1                                        # decode partitions
+    n += 1 if decode else 0                       # decode partitions
     n += 1 if b.max_query_len > 1 else 0          # chunked-prefill tiles
-    n += 1 if parts > 1 else 0                    # log-sum-exp merge
+    n += 1 if parts > 1 and decode else 0         # log-sum-exp merge
     return n
 
 
@@ -111,12 +138,21 @@ def barrier(world: int):
         dist.barrier()
 
 
-def load_peaks():
+def load_peaks() -> dict:
+    """HBM and dense fp16 tensor peaks: the measured ones when MEASURED_PEAKS.json is present
+    (a STREAM-style copy; a cuBLAS bf16 GEMM burst, and fp16 has bf16's nominal rate), else the
+    fallback figures of one earlier GB300 measurement."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         p = json.load(open(path))
-        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
-    return 6800.0, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+        return {"hbm_gbs": float(p["hbm_gbs"]),
+                "hbm_src": "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)",
+                "tflops": float(p["bf16_tflops"]),
+                "tflops_src": "measured (MEASURED_PEAKS.json bf16_tflops burst; fp16 = bf16 "
+                              "nominal rate)"}
+    return {"hbm_gbs": 6800.0, "hbm_src": "fallback (6.8 TB/s, one earlier GB300 measurement)",
+            "tflops": 1900.0, "tflops_src": "fallback (1.9 PFLOP/s bf16 burst, one earlier GB300 "
+                                            "measurement; fp16 = bf16 nominal rate)"}
 
 
 # ------------------------------------------------------------------------------ clocks
@@ -228,12 +264,13 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device error after warm-up: status {st} bits {bits}")
 
     # -------- device-resident timed region
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for _, _, k0, k1 in ev:  # torch creates an event on its first record(); the library then
-        k0.record(stream)    # re-records these handles around the decode-partition kernel
-        k1.record(stream)
+    timed = ([] if all_prefill(b) else ["decode"]) + (["prefill"] if b.max_query_len > 1 else [])
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(mk(), mk(), {k: (mk(), mk()) for k in timed}) for _ in range(args.steps)]
+    for _, _, kev in ev:      # torch creates an event on its first record(); the library then
+        for k0, k1 in kev.values():  # re-records these handles around the kernels it launches
+            k0.record(stream)
+            k1.record(stream)
     torch.cuda.synchronize()
     uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", ""))
     clocks = ClockSampler(uuid)
@@ -243,24 +280,26 @@ def run_ours(args, world, rank, local):
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 255)
-        s0, s1, k0, k1 = ev[i]
-        pa.set_timing_events(k0, k1)
+        s0, s1, kev = ev[i]
+        for k, (k0, k1) in kev.items():
+            pa.set_timing_events(k0, k1, kernel=k)
         s0.record(stream)
         step(q, k_new, v_new, slots, bt, sl, qsl, out)
         s1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(world)
-    pa.set_timing_events(None, None)
+    for k in timed:
+        pa.set_timing_events(None, None, kernel=k)
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(c) for a, c, _, _ in ev]
-    kern_ms = [k0.elapsed_time(k1) for _, _, k0, k1 in ev]
+    step_ms = [a.elapsed_time(c) for a, c, _ in ev]
+    kern_ms = {k: statistics.mean(kev[k][0].elapsed_time(kev[k][1]) for _, _, kev in ev)
+               for k in timed}
     st, bits = pa.get_device_error()
     if st != 0:
         raise RuntimeError(f"device error in timed region: status {st} bits {bits}")
     ms = statistics.mean(step_ms)
     ms_max = reduce_max(ms, world)
-    kern_mean = statistics.mean(kern_ms)
 
     # -------- end to end through the public API from pinned host buffers
     e2e = None
@@ -296,8 +335,12 @@ def run_ours(args, world, rank, local):
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": n_e2e}
 
-    peak, peak_src = load_peaks()
-    achieved = nbytes["attention_unique"] / (kern_mean * 1e-3) / 1e9
+    peaks = load_peaks()
+    peak, peak_src = peaks["hbm_gbs"], peaks["hbm_src"]
+    kernels = kernel_rooflines(nbytes, kern_ms, peaks)
+    if "decode" in kernels:
+        kernels["decode"]["traffic"] = load_traffic(args.workload)
+    dominant = max(kernels, key=lambda k: kernels[k]["ms_per_launch"])
     value = world * nbytes["step_logical"] / (ms_max * 1e-3) / 1e9
     tok_s = world * nbytes["decode_rows"] / (ms_max * 1e-3)
     result = {
@@ -314,11 +357,8 @@ def run_ours(args, world, rank, local):
         "decode_tok_s_per_layer": tok_s,
         "hbm_roofline_frac_step": (nbytes["step_logical"] / (ms * 1e-3) / 1e9) / peak,
         "bytes": nbytes,
-        "roofline": {"kernel": "decode_partition_kernel", "bound": "hbm", "achieved": achieved,
-                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_src, "traffic": None,
-                     "ms_per_launch": kern_mean,
-                     "bytes_per_launch": nbytes["attention_unique"]},
+        "roofline": kernels[dominant],
+        "roofline_kernels": kernels,
         "gpu_launches": launches_per_step(b) * args.steps,
         "wall_ms_per_step": wall * 1e3 / args.steps,
         "clocks": clk,
@@ -328,10 +368,30 @@ def run_ours(args, world, rank, local):
         result["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(b, nbytes, budget_s=args.cpu_seconds)
-    traffic = load_traffic(args.workload)
-    if traffic is not None:
-        result["roofline"]["traffic"] = traffic
     return result
+
+
+def kernel_rooflines(nbytes, kern_ms, peaks) -> dict:
+    """Roofline of each timed attention kernel from its algorithmic bytes / flops and its mean
+    live launch time.  The bound is whichever roof the kernel's arithmetic intensity hits first
+    (HBM copy bandwidth vs fp16 dense tensor throughput, both measured)."""
+    out = {}
+    specs = {"decode": ("decode_partition_kernel", nbytes["decode_kernel_bytes"], 0),
+             "prefill": ("prefill_umma_kernel", nbytes["prefill_kernel_bytes"],
+                         nbytes["prefill_kernel_flops"])}
+    for k, ms in kern_ms.items():
+        name, nb, fl = specs[k]
+        t = ms * 1e-3
+        tensor = fl / (peaks["tflops"] * 1e12) > nb / (peaks["hbm_gbs"] * 1e9)
+        if tensor:
+            achieved, peak, unit, src = fl / t / 1e12, peaks["tflops"], "TFLOP/s", peaks["tflops_src"]
+        else:
+            achieved, peak, unit, src = nb / t / 1e9, peaks["hbm_gbs"], "GB/s", peaks["hbm_src"]
+        out[k] = {"kernel": name, "bound": "tensor" if tensor else "hbm", "achieved": achieved,
+                  "peak": peak, "unit": unit, "frac": achieved / peak, "peak_source": src,
+                  "traffic": None, "ms_per_launch": ms, "bytes_per_launch": nb,
+                  "flops_per_launch": fl}
+    return out
 
 
 def load_traffic(workload):

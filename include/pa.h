@@ -52,7 +52,8 @@ typedef enum pa_status {
   PA_ERR_TIMEOUT = 4,     /* device: a bounded wait gave up (reported by pa_get_device_error) */
   PA_ERR_OUT_OF_RANGE = 5,/* device: slot or block id outside the pool; access skipped */
   PA_ERR_WORKSPACE = 6,   /* workspace missing, misaligned or smaller than required */
-  PA_ERR_DESCRIPTOR = 7   /* device: query_len > seq_len, short block table, or hint exceeded */
+  PA_ERR_DESCRIPTOR = 7,  /* device: query_len > seq_len, short block table, or hint exceeded */
+  PA_ERR_NO_BLOCKS = 8    /* host block manager: too few free or evictable blocks */
 } pa_status;
 
 typedef enum pa_dtype { PA_F16 = 0, PA_I32 = 1, PA_I64 = 2 } pa_dtype;
@@ -73,7 +74,9 @@ typedef struct pa_batch_hint {
   int32_t num_prefill_seqs; /* count of sequences with more than one query row; 0 = not known,
                                then the prefill launch covers every sequence.  A batch with more
                                such sequences than this skips the extra ones and reports
-                               PA_ERR_DESCRIPTOR. */
+                               PA_ERR_DESCRIPTOR.  When it equals the number of sequences (and
+                               max_query_len > 1) the decode launches are skipped; a one-row
+                               sequence in such a batch is then reported the same way. */
 } pa_batch_hint;
 
 /*
@@ -176,13 +179,31 @@ const char* pa_last_error(void);
 int pa_get_device_error(void* stream, uint32_t* bits);
 
 /*
+ * pa_copy_blocks -- copy whole physical blocks of the pool: K and V of every kv head of block
+ * pairs[i][0] are copied to block pairs[i][1] ("Local_LLM_03_vLLM_Architecture", prefix-caching
+ * slide: shared blocks; a sequence that appends into a partial block it shares gets its own
+ * copy first, the copy-on-write the host block manager asks for).
+ *   k_cache, v_cache  fp16 [NB, Hkv, bs, d], contiguous, as for pa_attention.
+ *   pairs             int32 [n, 2] contiguous device array (src, dst).  Destinations must be
+ *                     distinct and never a source of the same call.
+ * A pair with an id outside the pool is skipped and reported as PA_ERR_OUT_OF_RANGE by
+ * pa_get_device_error.  n = 0 is a no-op.
+ */
+int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_tensor* pairs,
+                   void* stream);
+
+/*
  * pa_set_timing_events -- measurement hook.  When both are non-NULL (cudaEvent_t handles),
  * every later pa_attention call on this host thread records `start` on its stream just before
- * launching the decode-partition kernel and `stop` just after it, so a caller can time that
- * kernel with CUDA events inside a longer step.  No work is skipped or reordered.  Pass NULL,
- * NULL to turn it off.  Returns PA_OK.
+ * launching the selected kernel and `stop` just after it, so a caller can time that kernel with
+ * CUDA events inside a longer step: `kernel` is PA_TIMED_DECODE (the decode-partition kernel,
+ * launched by every call with rows) or PA_TIMED_PREFILL (the chunked-prefill kernel, launched
+ * when hint->max_query_len > 1).  No work is skipped or reordered.  Pass NULL, NULL to turn
+ * the selected hook off.  Returns PA_OK, or PA_ERR_INVALID_ARG for an unknown `kernel`.
  */
-int pa_set_timing_events(void* start, void* stop);
+#define PA_TIMED_DECODE 0
+#define PA_TIMED_PREFILL 1
+int pa_set_timing_events(int kernel, void* start, void* stop);
 
 /* PA_VERSION of the built library. */
 int pa_version(void);

@@ -1,4 +1,5 @@
-"""Thin ctypes binding over the C ABI in ``include/pa.h`` (argument marshalling only).
+"""Thin ctypes binding over the C ABI in ``include/pa.h`` and ``include/pa_block_manager.h``
+(argument marshalling only).
 
 Every computation runs in the sm_103a kernels of ``libpa_gb300.so``; this module turns torch
 tensors into ``pa_tensor`` descriptors, passes the current CUDA stream and raises on a non-OK
@@ -24,14 +25,18 @@ PA_ERR_TIMEOUT = 4
 PA_ERR_OUT_OF_RANGE = 5
 PA_ERR_WORKSPACE = 6
 PA_ERR_DESCRIPTOR = 7
+PA_ERR_NO_BLOCKS = 8
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
                 4: "PA_ERR_TIMEOUT", 5: "PA_ERR_OUT_OF_RANGE", 6: "PA_ERR_WORKSPACE",
-                7: "PA_ERR_DESCRIPTOR"}
+                7: "PA_ERR_DESCRIPTOR", 8: "PA_ERR_NO_BLOCKS"}
 PA_F16, PA_I32, PA_I64 = 0, 1, 2
 PARTITION_TOKENS = 512
 EXPORTED = ("pa_reshape_and_cache", "pa_attention_workspace_size", "pa_attention",
             "pa_last_error", "pa_get_device_error", "pa_set_timing_events", "pa_version",
-            "pa_attention_static_scratch")
+            "pa_attention_static_scratch", "pa_copy_blocks",
+            "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_append",
+            "pa_bm_truncate", "pa_bm_fork", "pa_bm_free", "pa_bm_stats", "pa_bm_sequence",
+            "pa_bm_step_descriptor")
 
 _DTYPES = {torch.float16: PA_F16, torch.int32: PA_I32, torch.int64: PA_I64}
 
@@ -81,7 +86,26 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_attention_static_scratch.argtypes = [P, P, P, P, P, P, ctypes.c_float, P,
                                                     ctypes.POINTER(PABatchHint), ctypes.c_void_p]
         lib.pa_set_timing_events.restype = ctypes.c_int
-        lib.pa_set_timing_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        lib.pa_set_timing_events.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        lib.pa_copy_blocks.restype = ctypes.c_int
+        lib.pa_copy_blocks.argtypes = [P, P, P, ctypes.c_void_p]
+        I32, I64, VP = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+        PI32, PI64 = ctypes.POINTER(I32), ctypes.POINTER(I64)
+        for name, res, args in (
+                ("pa_bm_create", VP, [I32, I32, I32]),
+                ("pa_bm_destroy", None, [VP]),
+                ("pa_bm_add_sequence", ctypes.c_int, [VP, I64, PI32, I32, I64, PI32]),
+                ("pa_bm_append", ctypes.c_int, [VP, I64, PI32, I32, PI32, PI32]),
+                ("pa_bm_truncate", ctypes.c_int, [VP, I64, I32]),
+                ("pa_bm_fork", ctypes.c_int, [VP, I64, I64]),
+                ("pa_bm_free", ctypes.c_int, [VP, I64]),
+                ("pa_bm_stats", ctypes.c_int, [VP, PI32, PI32, PI32, PI32]),
+                ("pa_bm_sequence", ctypes.c_int, [VP, I64, PI32, PI32, I32, PI32]),
+                ("pa_bm_step_descriptor", ctypes.c_int,
+                 [VP, PI64, PI32, I32, I32, I32, PI32, PI32, PI32, PI64])):
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
         _lib = lib
     return _lib
 
@@ -156,14 +180,27 @@ def attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scal
     return out
 
 
-def set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
-    """Record ``start``/``stop`` around every later decode-partition kernel launch on this
-    thread (``None, None`` turns it off).  Measurement only; no work changes."""
+TIMED_KERNELS = {"decode": 0, "prefill": 1}
+
+
+def copy_blocks(k_cache, v_cache, pairs, stream=None):
+    """``pa_copy_blocks``: copy K and V of block ``pairs[i, 0]`` to block ``pairs[i, 1]``
+    (int32 [n, 2] device tensor), e.g. the copy-on-write pairs of the block manager."""
+    lib = load_library()
+    _check(lib.pa_copy_blocks(ctypes.byref(describe(k_cache)), ctypes.byref(describe(v_cache)),
+                              ctypes.byref(describe(pairs.contiguous())), _stream_handle(stream)))
+
+
+def set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event],
+                      kernel: str = "decode"):
+    """Record ``start``/``stop`` around every later launch of ``kernel`` ("decode": the
+    decode-partition kernel, "prefill": the chunked-prefill kernel) on this thread
+    (``None, None`` turns that hook off).  Measurement only; no work changes."""
     lib = load_library()
     if start is None or stop is None:
-        lib.pa_set_timing_events(None, None)
+        _check(lib.pa_set_timing_events(TIMED_KERNELS[kernel], None, None))
     else:
-        lib.pa_set_timing_events(start.cuda_event, stop.cuda_event)
+        _check(lib.pa_set_timing_events(TIMED_KERNELS[kernel], start.cuda_event, stop.cuda_event))
 
 
 def get_device_error(stream=None):

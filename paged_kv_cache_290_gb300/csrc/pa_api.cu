@@ -17,8 +17,8 @@
 namespace {
 
 thread_local std::string g_last_error;
-thread_local cudaEvent_t g_time_start = nullptr;
-thread_local cudaEvent_t g_time_stop = nullptr;
+thread_local cudaEvent_t g_time_start[2] = {nullptr, nullptr};  // [PA_TIMED_DECODE / _PREFILL]
+thread_local cudaEvent_t g_time_stop[2] = {nullptr, nullptr};
 
 int fail(int code, const std::string& msg) {
   g_last_error = msg;
@@ -229,6 +229,29 @@ int pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_tensor
   return PA_OK;
 }
 
+int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_tensor* pairs,
+                   void* stream) {
+  g_last_error.clear();
+  int rc;
+  if ((rc = check_pool(k_cache, v_cache))) return rc;
+  if ((rc = check_tensor(pairs, "pairs", PA_I32, 2))) return rc;
+  if (pairs->shape[1] != 2 || (pairs->shape[0] > 1 && pairs->stride[0] != 2))
+    return fail(PA_ERR_INVALID_ARG, "pairs must be a contiguous int32 [n, 2] array");
+  if (pairs->shape[0] == 0) return PA_OK;
+  pa::CopyArgs a{};
+  a.k_cache = static_cast<uint4*>(k_cache->data);
+  a.v_cache = static_cast<uint4*>(v_cache->data);
+  a.pairs = static_cast<const int32_t*>(pairs->data);
+  a.num_pairs = pairs->shape[0];
+  a.chunks_per_block = k_cache->shape[1] * k_cache->shape[2] * k_cache->shape[3] / 8;
+  a.num_blocks = k_cache->shape[0];
+  cudaError_t e = device_error_word(&a.err);
+  if (e != cudaSuccess) return cuda_fail(e, "error word");
+  e = pa::launch_copy_blocks(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return PA_OK;
+}
+
 int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                  const pa_tensor* block_tables, const pa_tensor* seq_lens,
                  const pa_tensor* query_start_loc, float scale, const pa_tensor* out,
@@ -307,6 +330,9 @@ int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
       std::max<int64_t>(1, (hint->max_seq_len + PA_PARTITION_TOKENS - 1) / PA_PARTITION_TOKENS));
   a.max_query_len = hint->max_query_len;
   a.prefill_seqs = hint->num_prefill_seqs > 0 ? std::min<int>(hint->num_prefill_seqs, n) : n;
+  // Every sequence has several rows (by the hint): no decode rows, so no decode or merge launch.
+  const bool all_prefill = hint->max_query_len > 1 && hint->num_prefill_seqs >= n;
+  a.decode_skipped = all_prefill ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaError_t e = device_error_word(&a.err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
@@ -317,28 +343,36 @@ int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   if ((rc = make_pool_map(&vmap, v_cache->data, rows, static_cast<int>(d)))) return rc;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool timed = g_time_start && g_time_stop;
-  if (timed && (e = cudaEventRecord(g_time_start, st)) != cudaSuccess)
-    return cuda_fail(e, "timing event");
-  e = pa::launch_decode(a, kmap, vmap, st);
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (timed && (e = cudaEventRecord(g_time_stop, st)) != cudaSuccess)
-    return cuda_fail(e, "timing event");
-  if (a.max_parts > 1) {
+  auto mark = [&](int kernel, bool stop) {
+    cudaEvent_t ev = stop ? g_time_stop[kernel] : g_time_start[kernel];
+    return ev ? cudaEventRecord(ev, st) : cudaSuccess;
+  };
+  if (!all_prefill) {
+    if ((e = mark(PA_TIMED_DECODE, false)) != cudaSuccess) return cuda_fail(e, "timing event");
+    e = pa::launch_decode(a, kmap, vmap, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    if ((e = mark(PA_TIMED_DECODE, true)) != cudaSuccess) return cuda_fail(e, "timing event");
+  }
+  if (a.max_parts > 1 && !all_prefill) {
     e = pa::launch_merge(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
   if (hint->max_query_len > 1) {
+    if ((e = mark(PA_TIMED_PREFILL, false)) != cudaSuccess) return cuda_fail(e, "timing event");
     e = pa::launch_prefill(a, kmap, vmap, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    if ((e = mark(PA_TIMED_PREFILL, true)) != cudaSuccess) return cuda_fail(e, "timing event");
   }
   return PA_OK;
 }
 
-int pa_set_timing_events(void* start, void* stop) {
-  g_time_start = static_cast<cudaEvent_t>(start);
-  g_time_stop = static_cast<cudaEvent_t>(stop);
-  if (!g_time_start || !g_time_stop) g_time_start = g_time_stop = nullptr;
+int pa_set_timing_events(int kernel, void* start, void* stop) {
+  g_last_error.clear();
+  if (kernel != PA_TIMED_DECODE && kernel != PA_TIMED_PREFILL)
+    return fail(PA_ERR_INVALID_ARG, "timed kernel must be PA_TIMED_DECODE or PA_TIMED_PREFILL");
+  const bool on = start && stop;
+  g_time_start[kernel] = on ? static_cast<cudaEvent_t>(start) : nullptr;
+  g_time_stop[kernel] = on ? static_cast<cudaEvent_t>(stop) : nullptr;
   return PA_OK;
 }
 

@@ -49,6 +49,7 @@ struct AttnArgs {
   int max_parts;   // P = ceil(max_seq_len / 512) (>= 1)
   int max_query_len;
   int prefill_seqs;  // sequences the prefill launch covers (<= num_seqs)
+  int decode_skipped;  // 1: the hint promised no one-row sequence, so no decode launch was made
   float scale_log2;  // scale * log2(e)
   unsigned* err;
 };
@@ -56,7 +57,19 @@ struct AttnArgs {
 // Sets the message pa_last_error() returns on this host thread; returns `status`.
 int set_last_error(int status, const std::string& message);
 
+// Whole-block copies (copy-on-write of shared blocks).
+struct CopyArgs {
+  uint4* k_cache;  // the pool as 16-byte chunks
+  uint4* v_cache;
+  const int32_t* pairs;  // [n][2] = (src, dst)
+  int64_t num_pairs;
+  int64_t chunks_per_block;  // Hkv * bs * d / 8
+  int64_t num_blocks;
+  unsigned* err;
+};
+
 cudaError_t launch_reshape_and_cache(const CacheArgs& a, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream);

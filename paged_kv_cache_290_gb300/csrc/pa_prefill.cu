@@ -83,8 +83,13 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   int found = 0;  // prefill sequences seen so far
   for (int s0 = 0; s0 < a.num_seqs; s0 += C::kThreads) {
     const int si = s0 + tid;
-    const bool pf = si < a.num_seqs && a.query_start_loc[si + 1] - a.query_start_loc[si] > 1;
+    const int ql = si < a.num_seqs ? a.query_start_loc[si + 1] - a.query_start_loc[si] : 0;
+    const bool pf = ql > 1;
     const unsigned bal = __ballot_sync(0xffffffffu, pf);
+    // A one-row sequence when the decode launch was skipped on the hint's word is an error.
+    if (a.decode_skipped && __any_sync(0xffffffffu, ql == 1) && lane == 0 && blockIdx.x == 0 &&
+        blockIdx.y == 0 && blockIdx.z == 0)
+      atomicOr(a.err, kErrHint);
     if (lane == 0) warp_count[warp] = __popc(bal);
     __syncthreads();
     int rank = found + __popc(bal & ((1u << lane) - 1u)), total = 0;

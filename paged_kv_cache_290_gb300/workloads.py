@@ -368,6 +368,20 @@ def mixed_step(block_size: int = 16, num_decode: int = 128, **kw) -> PagedBatch:
                        head_dim=128, block_size=block_size, seed_base=s, spare_frac=0.10, **kw)
 
 
+def spec_verify(**kw) -> PagedBatch:
+    """64 sequences each verifying k speculative draft tokens in one pass (k uniform in [1, 5],
+    so q_len = k + 1 in [2, 6] rows, causal among themselves), after a context uniform in
+    [512, 4096]; 32 q / 8 kv heads, d 128, bs 16.  ("Local_LLM_03_vLLM_Architecture",
+    speculative-decoding slide: the target model checks all drafted tokens in one forward pass,
+    and acceptance runs from 2 to 4 of 5 drafts.)"""
+    s = _seed(6)
+    ctx = torch.randint(512, 4097, (64,), generator=_gen(s + 0)).tolist()
+    k = torch.randint(1, 6, (64,), generator=_gen(s + 6)).tolist()
+    seqs = [SeqSpec(c + kk + 1, kk + 1) for c, kk in zip(ctx, k)]
+    return build_batch("spec_verify", seqs, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                       block_size=16, seed_base=s, spare_frac=0.10, **kw)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama8b_decode": llama8b_decode,
@@ -377,4 +391,5 @@ WORKLOADS = {
     "mixed_step_bs16": lambda **kw: mixed_step(16, **kw),
     "mixed_step_bs32": lambda **kw: mixed_step(32, **kw),
     "mixed_step_bs16_8dec": lambda **kw: mixed_step(16, num_decode=8, **kw),
+    "spec_verify": spec_verify,
 }

@@ -36,3 +36,12 @@ def small_prefix(seed=9300, n=6, prefix=64, d=128, bs=16):
     return build_batch("small_prefix", [SeqSpec(L, 1) for L in lens], num_q_heads=28,
                        num_kv_heads=4, head_dim=d, block_size=bs, seed_base=seed,
                        shared_prefix_len=prefix)
+
+
+def small_spec(d=128, bs=16, hq=32, hkv=4, seed=9400):
+    """Speculative-verify rows: q_len = k + 1 in [2, 6] over short ragged contexts (one with a
+    context shorter than its drafts, one crossing a 512-key boundary)."""
+    seqs = [SeqSpec(2, 2), SeqSpec(37, 3), SeqSpec(515, 6), SeqSpec(130, 4), SeqSpec(17, 5),
+            SeqSpec(96, 2), SeqSpec(1, 1), SeqSpec(260, 6)]
+    return build_batch(f"small_spec_d{d}_bs{bs}_g{hq // hkv}", seqs, num_q_heads=hq,
+                       num_kv_heads=hkv, head_dim=d, block_size=bs, seed_base=seed)

@@ -9,7 +9,8 @@ import pytest
 import paged_kv_cache_290_gb300 as pa
 from paged_kv_cache_290_gb300 import binding as B
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pa.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADERS = sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -20,9 +21,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(pa_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_abi():
@@ -107,6 +110,12 @@ def msg(lib):
 def test_attention_rejects_bad_arguments(lib, kw, status, text):
     assert call_attention(lib, **kw) == status
     assert text in msg(lib), msg(lib)
+
+
+def test_timing_hook_rejects_unknown_kernel(lib):
+    assert lib.pa_set_timing_events(7, None, None) == B.PA_ERR_INVALID_ARG
+    assert "PA_TIMED" in msg(lib)
+    assert lib.pa_set_timing_events(1, None, None) == B.PA_OK
 
 
 def test_attention_null_tensor(lib):

@@ -9,7 +9,7 @@ import torch.multiprocessing as mp
 
 import bench
 from paged_kv_cache_290_gb300 import workloads as W
-from _cases import small_mixed, small_prefix
+from _cases import small_mixed, small_prefix, small_spec
 
 
 def test_70b_step_bytes_match_the_hand_count():
@@ -41,6 +41,50 @@ def test_mixed_step_counts_prefill_launch():
     assert bench.launches_per_step(b) == 4
     n = bench.algorithmic_bytes(b)
     assert n["decode_rows"] == sum(1 for s in b.seqs if s.query_len == 1)
+
+
+def test_kernel_bytes_split_by_sequence_kind():
+    """The decode kernel serves one-row sequences, the prefill kernel the rest: on a decode-only
+    batch the decode kernel's bytes are the whole attention's; on a mixed batch the two add up
+    to it (plus the descriptor, which both kernels read)."""
+    b = W.llama70b_decode(keep_contiguous=False, keep_pre=False)
+    n = bench.algorithmic_bytes(b)
+    assert n["decode_kernel_bytes"] == n["attention_unique"]
+    assert n["prefill_kernel_bytes"] == 0 and n["prefill_kernel_flops"] == 0
+    m = small_mixed()
+    n = bench.algorithmic_bytes(m)
+    desc = m.num_seqs * 4 + (m.num_seqs + 1) * 4
+    assert n["decode_kernel_bytes"] + n["prefill_kernel_bytes"] == n["attention_unique"] + desc
+    # flops of the chunks: 4 Hq d per visible (query, key) pair, by brute force
+    pairs = sum(sum(s.seq_len - s.query_len + i + 1 for i in range(s.query_len))
+                for s in m.seqs if s.query_len > 1)
+    assert n["prefill_kernel_flops"] == 4 * m.num_q_heads * m.head_dim * pairs
+
+
+def test_roofline_bound_follows_arithmetic_intensity():
+    peaks = {"hbm_gbs": 6000.0, "hbm_src": "h", "tflops": 2000.0, "tflops_src": "t"}
+    n = {"decode_kernel_bytes": 10 ** 9, "prefill_kernel_bytes": 10 ** 8,
+         "prefill_kernel_flops": 2 * 10 ** 11}
+    r = bench.kernel_rooflines(n, {"decode": 0.2, "prefill": 0.25}, peaks)
+    assert r["decode"]["bound"] == "hbm" and r["decode"]["unit"] == "GB/s"
+    assert abs(r["decode"]["achieved"] - 5000.0) < 1e-6
+    assert r["prefill"]["bound"] == "tensor" and r["prefill"]["unit"] == "TFLOP/s"
+    assert abs(r["prefill"]["frac"] - 0.4) < 1e-9  # 800 TFLOP/s of 2000
+    # a few rows per sequence (speculative verify) stays on the HBM roof
+    n["prefill_kernel_flops"] = 10 ** 9
+    r = bench.kernel_rooflines(n, {"prefill": 0.02}, peaks)
+    assert r["prefill"]["bound"] == "hbm"
+
+
+def test_spec_verify_shapes_and_launches():
+    b = W.spec_verify(keep_contiguous=False, keep_pre=False)
+    q = [s.query_len for s in b.seqs]
+    assert len(q) == 64 and min(q) >= 2 and max(q) <= 6 and b.num_prefill_seqs == 64
+    assert all(512 + s.query_len <= s.seq_len <= 4096 + s.query_len for s in b.seqs)
+    assert bench.launches_per_step(b) == 2  # scatter, verify tiles (no decode rows: no decode/merge)
+    assert bench.algorithmic_bytes(b)["decode_rows"] == 0
+    sp = small_spec()
+    assert {s.query_len for s in sp.seqs if s.query_len > 1} == {2, 3, 4, 5, 6}
 
 
 def _free_port():

@@ -13,7 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_290_gb300 as pa
 from paged_kv_cache_290_gb300 import workloads as W
-from _cases import small_decode, small_mixed, small_prefix
+from _cases import small_decode, small_mixed, small_prefix, small_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -81,6 +81,9 @@ SMALL = {
     "mixed_d64_bs32_g1": lambda: small_mixed(d=64, bs=32, hq=4, hkv=4, seed=9209),
     "mixed_d128_bs16_g16": lambda: small_mixed(hq=32, hkv=2, seed=9210),
     "prefix_d128_bs16": lambda: small_prefix(),
+    "spec_d128_bs16_g8": lambda: small_spec(),
+    "spec_d64_bs32_g4": lambda: small_spec(d=64, bs=32, hq=16, hkv=4, seed=9401),
+    "spec_d128_bs32_g16": lambda: small_spec(bs=32, hq=32, hkv=2, seed=9402),
 }
 
 
@@ -227,7 +230,7 @@ def test_prefill_sequence_count_hint():
     args = [x.to(dev) for x in (b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
                                 b.query_start_loc)]
     outs = {}
-    for n in (0, 4, 2):
+    for n in (0, 4, 2, 8):
         out = torch.full_like(args[0], float("nan"))
         pa.attention(*args, b.scale, out, b.max_query_len, b.max_seq_len, num_prefill_seqs=n)
         outs[n] = (out, pa.get_device_error())
@@ -241,6 +244,13 @@ def test_prefill_sequence_count_hint():
     rows = [r for s, spec in enumerate(b.seqs) if spec.query_len == 1 or s in covered
             for r in range(int(b.query_start_loc[s]), int(b.query_start_loc[s + 1]))]
     assert torch.equal(outs[2][0][rows], outs[4][0][rows])
+    # a count equal to the number of sequences skips the decode launches: the batch's one-row
+    # sequences are then reported, and every prefill row is still exact
+    st, bits = outs[8][1]
+    assert st == pa.binding.PA_ERR_DESCRIPTOR and bits & 16
+    rows = [r for s, spec in enumerate(b.seqs) if spec.query_len > 1
+            for r in range(int(b.query_start_loc[s]), int(b.query_start_loc[s + 1]))]
+    assert torch.equal(outs[8][0][rows], outs[4][0][rows])
 
 
 # ------------------------------------------------------------------ the five full-size workloads
@@ -289,3 +299,7 @@ def test_full_prefix_shared_decode():
 @pytest.mark.parametrize("bs", [16, 32])
 def test_full_mixed_step(bs):
     _full(f"mixed_step_bs{bs}", sample_prefill_rows=24)
+
+
+def test_full_spec_verify():
+    _full("spec_verify")

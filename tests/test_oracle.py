@@ -16,7 +16,7 @@ import torch
 import oracle
 from paged_kv_cache_290_gb300 import workloads as W
 from _brute import brute_attention
-from _cases import small_decode, small_mixed, small_prefix
+from _cases import small_decode, small_mixed, small_prefix, small_spec
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -84,6 +84,26 @@ def test_reshape_and_cache_places_new_tokens(make):
     assert np.array_equal(kc, _bits(b.k_cache))
     assert np.array_equal(vc, _bits(b.v_cache))
     assert (b.slot_mapping < 0).sum() == (3 if "mixed" in b.name else 0)
+
+
+def test_copy_blocks_moves_whole_blocks_only():
+    """Block-level closed form: each destination equals its source as it was before the call,
+    every other block keeps its bytes, an out-of-pool pair is skipped, and copying a block to
+    a scratch block and back restores the pool."""
+    g = torch.Generator().manual_seed(77)
+    kc = torch.randint(0, 1 << 16, (9, 2, 16, 64), generator=g, dtype=torch.int32).to(torch.int16)
+    vc = torch.randint(0, 1 << 16, (9, 2, 16, 64), generator=g, dtype=torch.int32).to(torch.int16)
+    k0 = kc.numpy().view(np.uint16)
+    v0 = vc.numpy().view(np.uint16)
+    pairs = torch.tensor([[3, 7], [7, 1], [2, 99], [0, 5]], dtype=torch.int32)
+    k1, v1 = oracle.copy_blocks(kc, vc, pairs)
+    for blk in range(9):
+        src = {7: 3, 1: 7, 5: 0}.get(blk, blk)  # [7, 1] copies block 7's old contents
+        assert np.array_equal(k1[blk], k0[src]) and np.array_equal(v1[blk], v0[src])
+    k2, v2 = oracle.copy_blocks(torch.from_numpy(k1.view(np.int16)),
+                                torch.from_numpy(v1.view(np.int16)),
+                                torch.tensor([[1, 3]], dtype=torch.int32))
+    assert np.array_equal(k2[3], k0[7]) and np.array_equal(v2[3], v0[7])
 
 
 def test_reshape_and_cache_rejects_out_of_range_slot():
@@ -166,7 +186,8 @@ def test_identical_keys_give_mean_of_v():
 # ---------------------------------------------------------------- invariants of paging
 
 CASES = [W.tiny_decode, small_mixed, lambda: small_mixed(d=64, bs=32, hq=28, hkv=4, seed=9202),
-         small_prefix, lambda: small_decode(d=64, bs=32, hq=16, hkv=2, seed=9102)]
+         small_prefix, lambda: small_decode(d=64, bs=32, hq=16, hkv=2, seed=9102),
+         lambda: small_spec(d=64, bs=32, hq=16, hkv=2, seed=9403)]
 
 
 @pytest.mark.parametrize("make", CASES)
