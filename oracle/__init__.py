@@ -124,6 +124,20 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping):
     return kc, vc
 
 
+def copy_blocks(k_cache, v_cache, pairs):
+    """Return (k_cache', v_cache') as uint16 arrays: copies of the pools in which block
+    pairs[i][1] holds what block pairs[i][0] held before (all kv heads, K and V); pairs with an
+    id outside the pool are skipped.  Plain NumPy indexing."""
+    kc0, vc0 = _np(k_cache, np.uint16), _np(v_cache, np.uint16)
+    kc, vc = kc0.copy(), vc0.copy()
+    nb = kc.shape[0]
+    for src, dst in _np(pairs, np.int32).reshape(-1, 2).tolist():
+        if 0 <= src < nb and 0 <= dst < nb:
+            kc[dst] = kc0[src]
+            vc[dst] = vc0[src]
+    return kc, vc
+
+
 def _attn_args(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc):
     q16 = _np(q, np.uint16)
     kc, vc = _np(k_cache, np.uint16), _np(v_cache, np.uint16)

@@ -1,7 +1,8 @@
 """Build the sm_103a paged-attention library in-tree with nvcc (no cmake, no torch extension).
 
 Each .cu file compiles in parallel to an object with
-``-gencode arch=compute_103a,code=sm_103a``; the objects link into
+``-gencode arch=compute_103a,code=sm_103a`` (the host-only block manager, a .cpp file, goes
+through nvcc's host compiler); the objects link into
 ``paged_kv_cache_290_gb300/libpa_gb300.so`` with the CUDA runtime linked statically, so the
 library needs only the NVIDIA driver at run time.  ptxas register/spill reports go to
 ``_build/ptxas.log``.
@@ -19,7 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpa_gb300.so")
-SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode.cu", "pa_prefill.cu", "pa_noalloc.cu"]
+SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode.cu", "pa_prefill.cu", "pa_noalloc.cu",
+           "pa_block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -32,7 +34,7 @@ def _nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "pa.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     files.append(os.path.abspath(__file__))
     return files
 
@@ -53,7 +55,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
                     "-I", INCLUDE, "-I", CSRC]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -43,7 +43,36 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheArgs 
   }
 }
 
+// Copy-on-write of whole blocks: pair p (grid row y, strided) copies K and V of every kv head of
+// block src to block dst with 16-byte loads and stores; grid columns split a block's chunks.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyArgs a) {
+  for (int64_t p = blockIdx.y; p < a.num_pairs; p += gridDim.y) {
+    const int32_t src = a.pairs[2 * p], dst = a.pairs[2 * p + 1];
+    if (src < 0 || src >= a.num_blocks || dst < 0 || dst >= a.num_blocks) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.err, kErrBlockRange);
+      continue;
+    }
+    const int64_t s0 = src * a.chunks_per_block, d0 = dst * a.chunks_per_block;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+         c < a.chunks_per_block; c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const uint4 k = a.k_cache[s0 + c], v = a.v_cache[s0 + c];
+      a.k_cache[d0 + c] = k;
+      a.v_cache[d0 + c] = v;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream) {
+  if (a.num_pairs == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t cols = (a.chunks_per_block + threads - 1) / threads;
+  dim3 grid(static_cast<unsigned>(cols < 8 ? cols : 8),
+            static_cast<unsigned>(a.num_pairs < 65535 ? a.num_pairs : 65535));
+  copy_blocks_kernel<<<grid, threads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache(const CacheArgs& a, cudaStream_t stream) {
   const int64_t total = a.num_tokens * a.num_kv_heads * (a.head_dim / 8);
