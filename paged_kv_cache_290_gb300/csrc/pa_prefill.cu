@@ -5,24 +5,25 @@
 // ("Local_LLM_03_vLLM_Architecture", chunked-prefill slide: a long prefill is cut into chunks,
 // e.g. 512 tokens, interleaved with decodes; the chunk sees the paged context written before).
 //
-// Work item = one CTA = (q tile, kv head g, sequence s).  Its 128 rows are (query token, head of
-// the GQA group) pairs, so one K/V tile serves every head of the group.  Warp roles:
+// Work item = one CTA = (q tile, kv head g, prefill sequence).  Its 128 rows are (query token,
+// head of the GQA group) pairs, so one K/V tile serves every head of the group.  Warp roles:
 //   * producers (warps 8 and 9): stream 128-key K and V tiles (8 units of 16 tokens gathered
 //     through the block table, 128-byte-swizzled TMA boxes) into separate rings (3 K stages,
 //     2 V stages); a K stage is released as soon as its S = Q K^T is done, a V stage after P V,
 //   * MMA (warp 10, one thread): S_j = Q K_j^T into TMEM buffer j % 2 (M 128, N 128, K d, both
-//     operands K-major from shared memory), and O += P_j V_j with P_j read from TMEM (it
+//     operands K-major from shared memory), and O_{j%2} += P_j V_j with P_j read from TMEM (it
 //     overwrites the first 64 columns of S_j's buffer, two fp16 per column) and V_j MN-major
-//     from shared memory.  The issue order S_0, S_1, PV_0, S_2, PV_1, S_3, ... lets the tensor
-//     pipe work on S_{j+1} and P_{j-1} V_{j-1} while the softmax warps handle tile j, and since
-//     tcgen05 MMAs of one thread run in issue order, S_{j+2} never overwrites P_j before P_j V_j
-//     has read it,
-//   * softmax (warps 0-7; a TMEM lane is a row, split between two threads that take 64 columns
-//     each and trade their maxima through shared memory): read S_j with tcgen05.ld, scale by
-//     scale*log2(e), causal mask with a select, online softmax in base 2, write P_j (fp16) back
-//     to TMEM.  The running max is only raised (and O rescaled in TMEM) when it grows by more
-//     than 8 in log2 units, so P stays <= 256, well inside fp16; only then does the softmax
-//     wait for the previous P V product.
+//     from shared memory.  Issue order S_0, S_1, PV_0, S_2, PV_1, S_3, ...: the tensor pipe
+//     works on S_{j+1} and P_{j-1} V_{j-1} while tile j is in softmax, and since tcgen05 MMAs of
+//     one thread run in issue order, S_{j+2} never overwrites P_j before P_j V_j has read it,
+//   * softmax: warps 0-3 take the even key tiles and warps 4-7 the odd ones, one thread per
+//     row (TMEM lane) and all 128 columns.  Each parity runs its own online softmax (base 2,
+//     scale * log2(e) folded into the exponent) into its own accumulator O_even / O_odd, so the
+//     two warps sharing a TMEM lane quarter never wait for each other; the running max is only
+//     raised (and that O rescaled) when it grows by more than 8 in log2 units, which keeps
+//     P <= 256 in fp16.  S_j's completion implies P_{j-2} V_{j-2} (the previous product into
+//     the same O) is done, so no softmax step waits on a P V.  The epilogue merges the two
+//     halves of each row with the log-sum-exp rule.
 // V rows past the last visible key of the chunk are zeroed in shared memory before the last
 // P V product (0 * NaN would poison the sum).  Every wait is bounded.
 #include "pa_common.cuh"
@@ -44,8 +45,15 @@ struct PrefillCfg {
   static constexpr int kVStages = 2;
   static constexpr int kSmemBytes = kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
   static constexpr int kSoftmax = 256;                    // 8 softmax warps: 2 per row quarter
-  static constexpr int kThreads = kSoftmax + 3 * 32;      // + K producer, V producer, MMA
-  static constexpr uint32_t kTmemCols = 512;              // S/P 0 [0,128) S/P 1 [128,256) O [256,+d)
+  static constexpr int kParity = 128;                     // softmax threads per key-tile parity
+  // + a warpgroup of K producer, V producer, MMA issuer and one idle warp
+  static constexpr int kThreads = kSoftmax + 4 * 32;
+  // Registers: launched at 168 per thread (384 x 168 = 64512); the producer warpgroup gives
+  // back down to 72 and the two softmax warpgroups take 216: 256 x 216 + 128 x 72 = 64512.
+  static constexpr int kRegsSoftmax = 216;
+  static constexpr int kRegsOther = 72;
+  // TMEM columns: S/P of even tiles [0,128), of odd tiles [128,256), O_even, O_odd from 256.
+  static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 256;
   static constexpr float kRescaleLog2 = 8.f;              // raise the max only past 2^8
 };
@@ -58,10 +66,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[C::kKStages], k_empty[C::kKStages];
   __shared__ __align__(8) uint64_t v_full[C::kVStages], v_empty[C::kVStages];
-  __shared__ __align__(8) uint64_t s_full[2];
-  __shared__ __align__(8) uint64_t q_full, p_full, o_done, drain;
+  __shared__ __align__(8) uint64_t s_full[2], p_full[2];  // per key-tile parity
+  __shared__ __align__(8) uint64_t q_full, drain;
   __shared__ uint32_t tmem_base;
-  __shared__ float red_max[2][2][128];  // [tile parity][column half][row]
+  __shared__ float red_m[2][128];  // [parity][row]: running max and sum for the final merge
   __shared__ float red_l[2][128];
   __shared__ int softmax_stop;  // set by a softmax thread whose wait gave up
   __shared__ int warp_count[PrefillCfg<D>::kThreads / 32];
@@ -158,11 +166,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       mbar_init(smem_addr(&v_full[st]), 1);
       mbar_init(smem_addr(&v_empty[st]), 1);
     }
-    mbar_init(smem_addr(&s_full[0]), 1);
-    mbar_init(smem_addr(&s_full[1]), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&s_full[b]), 1);
+      mbar_init(smem_addr(&p_full[b]), C::kParity);
+    }
     mbar_init(smem_addr(&q_full), C::kSoftmax);
-    mbar_init(smem_addr(&p_full), C::kSoftmax);
-    mbar_init(smem_addr(&o_done), 1);
     mbar_init(smem_addr(&drain), 1);
     mbar_init_fence();
     softmax_stop = 0;
@@ -173,6 +181,12 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   const uint32_t tmem = tmem_base;
 
   constexpr int kKWarp = C::kSoftmax / 32, kVWarp = kKWarp + 1, kMmaWarp = kKWarp + 2;
+  static_assert(C::kRegsSoftmax * C::kSoftmax + C::kRegsOther * (C::kThreads - C::kSoftmax) <=
+                    168 * C::kThreads,
+                "register split exceeds the launch allocation");
+  if (warp >= kKWarp) {
+  // ================================================ producer / MMA warpgroup (warps 8-11)
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsOther));
   if (warp == kKWarp || warp == kVWarp) {
     // ============================================================== producer warps (K, V)
     const bool is_v = warp == kVWarp;
@@ -242,17 +256,16 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     bool ok = wait1(&q_full, 0) && issue_s(0) && (ntiles < 2 || issue_s(1));
     for (int j = 0; ok && j < ntiles; ++j) {
       const int vst = j % C::kVStages;
-      ok = wait1(&p_full, j & 1) && wait1(&v_full[vst], (j / C::kVStages) & 1);
+      ok = wait1(&p_full[j & 1], (j >> 1) & 1) && wait1(&v_full[vst], (j / C::kVStages) & 1);
       if (!ok) break;
       tmem_fence_after_sync();
       if (lane == 0) {
         const uint32_t vb = v_s + vst * C::kKVBytes;
 #pragma unroll
         for (int k = 0; k < C::kKeys / 16; ++k)
-          umma_f16_tmem_a(tmem + C::kOCol, tmem + (j & 1) * 128 + k * 8,
+          umma_f16_tmem_a(tmem + C::kOCol + (j & 1) * D, tmem + (j & 1) * 128 + k * 8,
                           umma_sdesc(vb + k * 16 * 128, C::kKeys * 128, 1024), kIdO,
-                          (j > 0 || k > 0));
-        umma_commit(smem_addr(&o_done));
+                          (j > 1 || k > 0));
         umma_commit(smem_addr(&v_empty[vst]));
       }
       __syncwarp();
@@ -264,28 +277,28 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       mbar_wait(smem_addr(&drain), 0, a.err);
     }
     __syncwarp();
+  }  // warp 11 has no role
   } else {
     // ============================================================== softmax warps 0-7
-    // Warps w and w+4 share TMEM lanes 32(w%4) .. +31 (one row per lane); warp w takes the
-    // row's columns half ch = w / 4 of S and O.  The two halves of a row exchange their maxima
-    // through shared memory, so both take identical rescale decisions.
-    constexpr int kHalfCols = C::kKeys / 2;   // S columns per thread
-    constexpr int kOHalf = D / 2;             // O columns per thread
-    const int ch = warp >> 2;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
+    // Warp w takes key tiles j with j % 2 == par = w / 4 for TMEM lanes 32(w%4) .. +31, one
+    // row per thread, all columns.  Its O accumulator is O_par.
+    constexpr int kOHalf = D / 2;             // output columns per thread in the epilogue
+    const int par = warp >> 2;
     const int r = (warp & 3) * 32 + lane;     // TMEM lane = tile row
     const int qi = r / a.group, hg = r % a.group;
     const bool rv = qi < tile_q && qbase + qi < q_len;
     const int pos = ctx + (rv ? qbase + qi : qbase);  // padding rows mirror the first row
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    auto sync_softmax = [] { asm volatile("bar.sync 1, %0;" ::"n"(C::kSoftmax) : "memory"); };
+    const uint32_t obuf = tmem + lane_addr + C::kOCol + par * D;
 
-    // This thread's half of the Q row -> shared memory, 128B-swizzled K-major.
+    // Half par of the Q row -> shared memory, 128B-swizzled K-major.
     {
       const __half* qrow = a.q + static_cast<int64_t>(row0 + qbase + (rv ? qi : 0)) * a.q_stride +
                            static_cast<int64_t>(g * a.group + hg) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 16; ++cc) {
-        const int c = ch * (D / 16) + cc;
+        const int c = par * (D / 16) + cc;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (rv) v = __ldg(reinterpret_cast<const uint4*>(qrow + c * 8));
         const uint32_t dst = q_s + (c >> 3) * C::kHalfBytes + swz128(r, c & 7);
@@ -297,35 +310,34 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
       mbar_arrive(smem_addr(&q_full));
     }
 
-    // A failed (timed-out) wait sets softmax_stop; every softmax thread still reaches the next
-    // named barrier and all of them leave the loop together after it, so none is left waiting.
-    auto note = [&](bool ok) {
-      if (!ok) softmax_stop = 1;
-    };
+    bool stopped = false;  // a wait of this thread gave up
     float m_run = -INFINITY, l_run = 0.f;
     const int min_pos = ctx + qbase;
     const bool prescale = !(a.scale_log2 > 0.f);
     const float mul = prescale ? 1.f : a.scale_log2;  // exponent = fma(score, mul, -m)
-    for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
-      const uint32_t sbuf = tmem + lane_addr + b * 128;
-      note(mbar_wait(smem_addr(&s_full[b]), (j >> 1) & 1, a.err));
+    for (int j = par; j < ntiles; j += 2) {
+      const uint32_t sbuf = tmem + lane_addr + par * 128;
+      // S_j done; it was issued after P_{j-2} V_{j-2}, so O_par is settled too.
+      if (!mbar_wait(smem_addr(&s_full[par]), (j >> 1) & 1, a.err)) {
+        stopped = true;
+        break;
+      }
       tmem_fence_after_sync();
-      uint32_t sv[kHalfCols / 32][32];
+      uint32_t sv[C::kKeys / 32][32];
 #pragma unroll
-      for (int qq = 0; qq < kHalfCols / 32; ++qq) tmem_ld32(sbuf + ch * kHalfCols + qq * 32, sv[qq]);
+      for (int qq = 0; qq < C::kKeys / 32; ++qq) tmem_ld32(sbuf + qq * 32, sv[qq]);
       tmem_wait_ld();
 #pragma unroll
-      for (int qq = 0; qq < kHalfCols / 32; ++qq) tmem_regs_ready(sv[qq]);
+      for (int qq = 0; qq < C::kKeys / 32; ++qq) tmem_regs_ready(sv[qq]);
 
       // Scores stay raw where scale > 0 (the max commutes with the scale, which is folded into
       // the exponent's FMA below); otherwise they are scaled here.  Masked keys become -inf.
-      const int key0 = j * C::kKeys + ch * kHalfCols;
-      const bool masked = key0 + kHalfCols - 1 > min_pos;
+      const int key0 = j * C::kKeys;
+      const bool masked = key0 + C::kKeys - 1 > min_pos;
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (prescale || masked) {
 #pragma unroll
-        for (int c = 0; c < kHalfCols; ++c) {
+        for (int c = 0; c < C::kKeys; ++c) {
           float v = __uint_as_float(sv[c >> 5][c & 31]);
           if (prescale) v *= a.scale_log2;
           if (masked && key0 + c > pos) v = -INFINITY;
@@ -334,112 +346,111 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kHalfCols; ++c)
+        for (int c = 0; c < C::kKeys; ++c)
           m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c >> 5][c & 31]));
       }
-      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mul;
-      red_max[b][ch][r] = mx;
-      // Both halves' S loads are complete before either half writes P over them.
-      tmem_fence_before_sync();
-      sync_softmax();
-      tmem_fence_after_sync();
-      if (*reinterpret_cast<volatile int*>(&softmax_stop)) break;
-      mx = fmaxf(mx, red_max[b][ch ^ 1][r]);
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mul;
       float alpha = 1.f;
-      if (m_run == -INFINITY || mx > m_run + C::kRescaleLog2) {
-        const float m_new = fmaxf(m_run, mx);
-        alpha = ex2_approx(m_run - m_new);  // 0 on the first tile
-        m_run = m_new;
+      if (mx > m_run + C::kRescaleLog2 || (m_run == -INFINITY && mx > -INFINITY)) {
+        alpha = ex2_approx(m_run - mx);  // 0 when m_run is still -inf
+        m_run = mx;
       }
-
-      // Rescaling O needs P_{j-1} V_{j-1} to be complete (o_done's phase j-1; S_j's completion
-      // already implies P_{j-2} V_{j-2}, so the parity is unambiguous).
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        note(mbar_wait(smem_addr(&o_done), (j - 1) & 1, a.err));
-        tmem_fence_after_sync();
+      if (j >= 2 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int c0 = 0; c0 < kOHalf; c0 += 32) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t t[32];
-          const uint32_t ta = tmem + lane_addr + C::kOCol + ch * kOHalf + c0;
-          tmem_ld32(ta, t);
+          tmem_ld32(obuf + c0, t);
           tmem_wait_ld();
           tmem_regs_ready(t);
 #pragma unroll
           for (int c = 0; c < 32; ++c) t[c] = __float_as_uint(__uint_as_float(t[c]) * alpha);
-          tmem_st32(ta, t);
+          tmem_st32(obuf + c0, t);
         }
       }
 
-      // This half of P_j (fp16, keys ch*64 ..) -> TMEM columns ch*32 .. of buffer b; l keeps
-      // the unrounded p.
+      // P_j (fp16) -> TMEM columns 0..63 of the buffer, two keys per column; l keeps the
+      // unrounded p.  A row with every key so far masked keeps m = -inf and gets p = 0.
+      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
-      const float neg_m = -m_run;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const uint32_t* e = &sv[c >> 4][(2 * c) & 31];
-        const float p0 = ex2_approx(fmaf(__uint_as_float(e[0]), mul, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(e[1]), mul, neg_m));
-        ps[c & 3] += p0 + p1;
-        pk[c] = pack_half2(p0, p1);
+      for (int q4 = 0; q4 < C::kKeys / 32; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c]), mul, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c + 1]), mul, neg_m));
+          ps[c & 3] += p0 + p1;
+          pk[c] = pack_half2(p0, p1);
+        }
+        tmem_st16(sbuf + q4 * 16, pk);
       }
-      const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      tmem_st32(sbuf + ch * 32, pk);
-      l_run = l_run * alpha + psum;
+      l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
 
       const int tile0 = j * C::kKeys;
       if (j == ntiles - 1 && tile0 + C::kKeys > kend) {
         // The last tile: V rows at or past kend may be stale or NaN; zero them once the tile
-        // has landed (the MMA reads V only after p_full below).  Thread (r, ch) clears the
-        // 64-column chunks h with h % 2 == ch of V row r.
+        // has landed (the MMA reads V only after p_full below).  Thread r clears V row r.
         const int vst = j % C::kVStages;
         const bool landed = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err);
-        note(landed);
         if (landed && tile0 + r >= kend) {
           const uint32_t vrow = v_s + vst * C::kKVBytes + r * 128;
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h) {
-            if ((h & 1) != ch) continue;
+          for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
               asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
                                vrow + h * (C::kKeys * 128) + c * 16),
                            "r"(0u), "r"(0u), "r"(0u), "r"(0u)
                            : "memory");
-          }
         }
         fence_proxy_async();
+        if (!landed) {
+          stopped = true;
+          break;
+        }
       }
       tmem_wait_st();
       tmem_fence_before_sync();
-      mbar_arrive(smem_addr(&p_full));
+      mbar_arrive(smem_addr(&p_full[par]));
     }
 
-    // l of the whole row = the two halves' partial sums (same max, same rescales).
-    red_l[ch][r] = l_run;
-    sync_softmax();
-    const float l_row = l_run + red_l[ch ^ 1][r];
+    // Merge the even and odd halves of each row: M = max, weights 2^(m - M).  The odd half
+    // exists only when there are at least two key tiles.
+    red_m[par][r] = m_run;
+    red_l[par][r] = l_run;
+    if (stopped) softmax_stop = 1;
+    asm volatile("bar.sync 1, %0;" ::"n"(C::kSoftmax) : "memory");
+    const bool two = ntiles >= 2;
+    const float m_e = red_m[0][r], m_o = two ? red_m[1][r] : -INFINITY;
+    const float mm = fmaxf(m_e, m_o);
+    const float w_e = ex2_approx(m_e - mm), w_o = two ? ex2_approx(m_o - mm) : 0.f;
+    const float inv = 1.f / (red_l[0][r] * w_e + (two ? red_l[1][r] * w_o : 0.f));
     bool ok = !*reinterpret_cast<volatile int*>(&softmax_stop);
     if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err);
     if (!__any_sync(0xffffffffu, !ok)) {
       tmem_fence_after_sync();
-      const float inv = 1.f / l_row;
       __half* dst = a.out + (static_cast<int64_t>(row0 + qbase + qi) * a.num_q_heads +
-                             g * a.group + hg) * D + ch * kOHalf;
+                             g * a.group + hg) * D + par * kOHalf;
+      const uint32_t oe = tmem + lane_addr + C::kOCol + par * kOHalf;
 #pragma unroll
       for (int c0 = 0; c0 < kOHalf; c0 += 32) {
-        uint32_t t[32];
-        tmem_ld32(tmem + lane_addr + C::kOCol + ch * kOHalf + c0, t);
+        uint32_t te[32], to[32];
+        tmem_ld32(oe + c0, te);
+        if (two) tmem_ld32(oe + D + c0, to);
         tmem_wait_ld();
-        tmem_regs_ready(t);
+        tmem_regs_ready(te);
+        if (two) tmem_regs_ready(to);
+        auto o = [&](int c) {
+          return (__uint_as_float(te[c]) * w_e + (two ? __uint_as_float(to[c]) * w_o : 0.f)) * inv;
+        };
         if (rv) {
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {
             uint4 v;
-            v.x = pack_half2(__uint_as_float(t[c]) * inv, __uint_as_float(t[c + 1]) * inv);
-            v.y = pack_half2(__uint_as_float(t[c + 2]) * inv, __uint_as_float(t[c + 3]) * inv);
-            v.z = pack_half2(__uint_as_float(t[c + 4]) * inv, __uint_as_float(t[c + 5]) * inv);
-            v.w = pack_half2(__uint_as_float(t[c + 6]) * inv, __uint_as_float(t[c + 7]) * inv);
+            v.x = pack_half2(o(c), o(c + 1));
+            v.y = pack_half2(o(c + 2), o(c + 3));
+            v.z = pack_half2(o(c + 4), o(c + 5));
+            v.w = pack_half2(o(c + 6), o(c + 7));
             *reinterpret_cast<uint4*>(dst + c0 + c) = v;
           }
         }
@@ -464,6 +475,13 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const C
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  // setmaxnreg.inc can only take registers the CTA was launched with: never launch a build
+  // whose per-thread allocation is below the split (the increase would wait forever).
+  cudaFuncAttributes attr{};
+  if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
+  if (attr.numRegs * C::kThreads < C::kRegsSoftmax * C::kSoftmax +
+                                       C::kRegsOther * (C::kThreads - C::kSoftmax))
+    return cudaErrorInvalidConfiguration;
   const int tile_q = C::kRows / a.group;
   dim3 grid((a.max_query_len + tile_q - 1) / tile_q, a.num_kv_heads, a.prefill_seqs);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
