@@ -224,59 +224,49 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     if (lane == 0)
       for (int j = max(0, issued - stages); j < issued; ++j)
         mbar_wait(smem_addr(&full[j % stages]), (j / stages) & 1, a.err);
-  } else if (warp == kMmaWarp) {
-    // ============================================================== MMA warp (one thread)
+  } else if (warp == kMmaWarp && lane == 0) {
+    // ============================================================== MMA issuer (one thread)
+    // Issuing a tcgen05.mma waits until the pipe takes it and the pipe queues almost nothing,
+    // so every other instruction of this thread idles the tensor cores for its duration: the
+    // issuer runs alone, with no warp-collective operations.
     constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0);
     constexpr uint32_t kIdO = umma_idesc_f16(C::kRows, D, 0, 1);
-    auto wait1 = [&](uint64_t* bar, int parity) {  // lane 0 waits, the warp learns the outcome
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(smem_addr(bar), parity, a.err);
-      return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    };
-    // S_j = Q K_j^T into TMEM buffer j % 2; frees K stage j % 3 once done.
+    // S_j = Q K_j^T into TMEM buffer j % 2; frees its K stage once done.
     auto issue_s = [&](int j) {
       const int st = j % C::kKStages;
-      if (!wait1(&k_full[st], (j / C::kKStages) & 1)) return false;
+      if (!mbar_wait(smem_addr(&k_full[st]), (j / C::kKStages) & 1, a.err)) return false;
       tmem_fence_after_sync();
-      if (lane == 0) {
-        const uint32_t kst = k_s + st * C::kKVBytes;
+      const uint32_t kst = k_s + st * C::kKVBytes;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::kHalfBytes + (k & 3) * 32;
-          umma_f16(tmem + (j & 1) * 128, umma_sdesc(q_s + off, 16, 1024),
-                   umma_sdesc(kst + (k >> 2) * (C::kKeys * 128) + (k & 3) * 32, 16, 1024), kIdS,
-                   k > 0);
-        }
-        umma_commit(smem_addr(&s_full[j & 1]));
-        umma_commit(smem_addr(&k_empty[st]));
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * C::kHalfBytes + (k & 3) * 32;
+        umma_f16(tmem + (j & 1) * 128, umma_sdesc(q_s + off, 16, 1024),
+                 umma_sdesc(kst + (k >> 2) * (C::kKeys * 128) + (k & 3) * 32, 16, 1024), kIdS,
+                 k > 0);
       }
-      __syncwarp();
+      umma_commit(smem_addr(&s_full[j & 1]));
+      umma_commit(smem_addr(&k_empty[st]));
       return true;
     };
-    bool ok = wait1(&q_full, 0) && issue_s(0) && (ntiles < 2 || issue_s(1));
+    bool ok = mbar_wait(smem_addr(&q_full), 0, a.err) && issue_s(0) && (ntiles < 2 || issue_s(1));
     for (int j = 0; ok && j < ntiles; ++j) {
       const int vst = j % C::kVStages;
-      ok = wait1(&p_full[j & 1], (j >> 1) & 1) && wait1(&v_full[vst], (j / C::kVStages) & 1);
+      ok = mbar_wait(smem_addr(&p_full[j & 1]), (j >> 1) & 1, a.err) &&
+           mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err);
       if (!ok) break;
       tmem_fence_after_sync();
-      if (lane == 0) {
-        const uint32_t vb = v_s + vst * C::kKVBytes;
+      const uint32_t vb = v_s + vst * C::kKVBytes;
 #pragma unroll
-        for (int k = 0; k < C::kKeys / 16; ++k)
-          umma_f16_tmem_a(tmem + C::kOCol + (j & 1) * D, tmem + (j & 1) * 128 + k * 8,
-                          umma_sdesc(vb + k * 16 * 128, C::kKeys * 128, 1024), kIdO,
-                          (j > 1 || k > 0));
-        umma_commit(smem_addr(&v_empty[vst]));
-      }
-      __syncwarp();
+      for (int k = 0; k < C::kKeys / 16; ++k)
+        umma_f16_tmem_a(tmem + C::kOCol + (j & 1) * D, tmem + (j & 1) * 128 + k * 8,
+                        umma_sdesc(vb + k * 16 * 128, C::kKeys * 128, 1024), kIdO,
+                        (j > 1 || k > 0));
+      umma_commit(smem_addr(&v_empty[vst]));
       if (j + 2 < ntiles) ok = issue_s(j + 2);
     }
     // Every MMA this thread issued has finished before O is read or the CTA tears down.
-    if (lane == 0) {
-      umma_commit(smem_addr(&drain));
-      mbar_wait(smem_addr(&drain), 0, a.err);
-    }
-    __syncwarp();
+    umma_commit(smem_addr(&drain));
+    mbar_wait(smem_addr(&drain), 0, a.err);
   }  // warp 11 has no role
   } else {
     // ============================================================== softmax warps 0-7
