@@ -5,38 +5,499 @@
 // ("Local_LLM_03_vLLM_Architecture", chunked-prefill slide: a long prefill is cut into chunks,
 // e.g. 512 tokens, interleaved with decodes; the chunk sees the paged context written before).
 //
-// Work item = one CTA = (q tile, kv head g, prefill sequence).  Its 128 rows are (query token,
-// head of the GQA group) pairs, so one K/V tile serves every head of the group.  Warp roles:
+// Two kernels, chosen per launch by the longest chunk (the hint's max_query_len):
+//   * prefill_pair_kernel when a chunk spans more than one 128-row Q tile, described below;
+//   * prefill_parity_kernel when every chunk fits one Q tile (speculative verify, short chunks):
+//     the same warp roles and TMEM layout, but its two softmax warpgroups take the even and the
+//     odd key tiles of the one Q tile, each with its own online softmax and O accumulator, merged
+//     at the end with the log-sum-exp rule (S_{j+2} reuses S_j's buffer after P_j V_j).
+// Both find their sequence with the same scan and feed K/V with the same producer warps.
+//
+// prefill_pair_kernel: work item = one CTA = (two Q tiles, kv head g, prefill sequence).  A Q tile is 128 rows, each
+// a (query token, head of the GQA group) pair, so one K/V tile serves every head of the group,
+// and every K/V tile the CTA loads serves both Q tiles (256 rows).  Warp roles:
 //   * producers (warps 8 and 9): stream 128-key K and V tiles (8 units of 16 tokens gathered
-//     through the block table, 128-byte-swizzled TMA boxes) into separate rings (3 K stages,
-//     2 V stages); a K stage is released as soon as its S = Q K^T is done, a V stage after P V,
-//   * MMA (warp 10, one thread): S_j = Q K_j^T into TMEM buffer j % 2 (M 128, N 128, K d, both
-//     operands K-major from shared memory), and O_{j%2} += P_j V_j with P_j read from TMEM (it
-//     overwrites the first 64 columns of S_j's buffer, two fp16 per column) and V_j MN-major
-//     from shared memory.  Issue order S_0, S_1, PV_0, S_2, PV_1, S_3, ...: the tensor pipe
-//     works on S_{j+1} and P_{j-1} V_{j-1} while tile j is in softmax, and since tcgen05 MMAs of
-//     one thread run in issue order, S_{j+2} never overwrites P_j before P_j V_j has read it,
-//   * softmax: warps 0-3 take the even key tiles and warps 4-7 the odd ones, one thread per
-//     row (TMEM lane) and all 128 columns.  Each parity runs its own online softmax (base 2,
-//     scale * log2(e) folded into the exponent) into its own accumulator O_even / O_odd, so the
-//     two warps sharing a TMEM lane quarter never wait for each other; the running max is only
-//     raised (and that O rescaled) when it grows by more than 8 in log2 units, which keeps
-//     P <= 256 in fp16.  S_j's completion implies P_{j-2} V_{j-2} (the previous product into
-//     the same O) is done, so no softmax step waits on a P V.  The epilogue merges the two
-//     halves of each row with the log-sum-exp rule.
-// V rows past the last visible key of the chunk are zeroed in shared memory before the last
-// P V product (0 * NaN would poison the sum).  Every wait is bounded.
+//     through the block table, 128-byte-swizzled TMA boxes) into separate 2-stage rings; a K
+//     stage is released once both S = Q K^T products that read it are done, a V stage after
+//     both P V products,
+//   * MMA issuer (lane 0 of warp 10): per Q tile t, S_t = Q_t K_j^T into TMEM buffer t (M 128,
+//     N 128, K d, both operands K-major from shared memory) and O_t += P_t V_j with P_t read
+//     from TMEM (it overwrites the first 64 columns of S_t's buffer, two fp16 per column) and
+//     V_j MN-major from shared memory.  Issue order S_A(0), S_B(0), then per key tile j:
+//     P_A V_j, S_A(j+1), P_B V_j, S_B(j+1): the tensor pipe computes one Q tile's products
+//     while the other tile is in softmax, and since tcgen05 MMAs of one thread run in issue
+//     order, S_t(j+1) never overwrites P_t(j) before P_t V_j has read it.  Issuing an MMA
+//     waits until the pipe takes it, so this thread runs alone and never joins a warp
+//     collective (that would idle the pipe),
+//   * softmax: warpgroup t (warps 4t .. 4t+3) owns Q tile t, one thread per row (TMEM lane), all
+//     128 columns of a key tile: online softmax in base 2 with scale * log2(e) folded into the
+//     exponent.  The running max is only raised (and O_t rescaled in TMEM) when it grows by more
+//     than 8 in log2 units, which keeps P <= 256 in fp16.  S_t(j)'s completion implies
+//     P_t V_{j-1} is done (it was issued after it), so no softmax step waits on a P V.
+// V rows past the last visible key of the chunk are zeroed in shared memory before the first
+// P V product of the last key tile (0 * NaN would poison the sum).  Every wait is bounded.
 #include "pa_common.cuh"
 #include "pa_kernels.h"
 
 namespace pa {
 namespace {
 
+// Grid row z of a prefill launch serves the z-th sequence with more than one query row (a
+// block-wide ballot scan of query_start_loc, all threads of the CTA), so decode rows cost the
+// launch nothing.  Returns that sequence, or -1 past the last one; more such sequences than
+// grid rows (or, when the decode launch was skipped on the hint's word, a one-row sequence) is
+// a hint error.
+template <int kThreads>
+__device__ __forceinline__ int find_prefill_seq(const AttnArgs& a, int* warp_count,
+                                                int* chosen_seq) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) *chosen_seq = -1;
+  int found = 0;  // prefill sequences seen so far
+  for (int s0 = 0; s0 < a.num_seqs; s0 += kThreads) {
+    const int si = s0 + tid;
+    const int ql = si < a.num_seqs ? a.query_start_loc[si + 1] - a.query_start_loc[si] : 0;
+    const bool pf = ql > 1;
+    const unsigned bal = __ballot_sync(0xffffffffu, pf);
+    if (a.decode_skipped && __any_sync(0xffffffffu, ql == 1) && lane == 0 && blockIdx.x == 0 &&
+        blockIdx.y == 0 && blockIdx.z == 0)
+      atomicOr(a.err, kErrHint);
+    if (lane == 0) warp_count[warp] = __popc(bal);
+    __syncthreads();
+    int rank = found + __popc(bal & ((1u << lane) - 1u)), total = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      rank += w < warp ? warp_count[w] : 0;
+      total += warp_count[w];
+    }
+    if (pf && rank == static_cast<int>(blockIdx.z)) *chosen_seq = si;
+    found += total;
+    __syncthreads();
+  }
+  __syncthreads();
+  if (found > static_cast<int>(gridDim.z) && blockIdx.x == 0 && blockIdx.y == 0 &&
+      blockIdx.z == 0 && tid == 0)
+    atomicOr(a.err, kErrHint);
+  return *chosen_seq;
+}
+
+// A producer warp: streams the K (or V) tiles 0 .. ntiles-1 of sequence s, kv head g, keys
+// [0, kend), into a ring of `stages` stages of kKVBytes each.  Each 16-token unit is found
+// through the block table and fetched as 128-byte-swizzled TMA boxes (one per 64 columns).
+// Before returning it waits (bounded) for its last copies, so none lands after the CTA retires.
+template <int D, int BS, int kKeys>
+__device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap* map, int s, int g,
+                                           int kend, int ntiles, int stages, uint64_t* full,
+                                           uint64_t* empty, uint32_t ring) {
+  constexpr int kUnits = kKeys / 16, kHalves = D / 64, kKVBytes = kHalves * kKeys * 128;
+  const int lane = threadIdx.x & 31;
+  int issued = 0;
+  for (int j = 0; j < ntiles; ++j) {
+    const int st = j % stages, round = j / stages;
+    bool ok = true;
+    if (lane == 0 && round > 0) ok = mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err);
+    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    const int key0 = j * kKeys;
+    const int units = min(kUnits, (kend - key0 + 15) >> 4);
+    const int id = lane < units
+                       ? a.block_tables[static_cast<int64_t>(s) * a.bt_stride + (key0 + 16 * lane) / BS]
+                       : 0;
+    const uint32_t bar = smem_addr(&full[st]);
+    if (lane == 0) mbar_arrive_expect_tx(bar, units * kHalves * 2048);
+    const uint32_t dst = ring + st * kKVBytes;
+    for (int u = 0; u < units; ++u) {
+      const int blk = __shfl_sync(0xffffffffu, id, u);
+      if (lane == 0) {
+        const int y = (blk * a.num_kv_heads + g) * BS + ((key0 + 16 * u) % BS);
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h)
+          tma_load_2d(dst + h * (kKeys * 128) + u * 2048, map, h * 64, y, bar);
+      }
+    }
+    issued = j + 1;
+  }
+  if (lane == 0)
+    for (int j = max(0, issued - stages); j < issued; ++j)
+      mbar_wait(smem_addr(&full[j % stages]), (j / stages) & 1, a.err);
+}
+
 template <int D>
-struct PrefillCfg {
+struct PairCfg {
+  static constexpr int kRows = 128;  // MMA M: (query token, head) rows of one Q tile
+  static constexpr int kQTiles = 2;  // Q tiles per CTA, sharing every K/V tile
+  static constexpr int kKeys = 128;  // keys per K/V tile: N of S, K of P V
+  static constexpr int kHalves = D / 64;                  // 128-byte column chunks of a row
+  static constexpr int kHalfBytes = kRows * 128;          // one 64-column chunk of a 128-row tile
+  static constexpr int kQBytes = kHalves * kHalfBytes;    // one Q tile, [half][row][128 B]
+  static constexpr int kKVBytes = kHalves * kKeys * 128;  // K (or V) tile, [half][key][128 B]
+  static constexpr int kKStages = 2;
+  static constexpr int kVStages = 2;
+  static constexpr int kSmemBytes =
+      kQTiles * kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
+  static constexpr int kSoftmax = 256;                    // one warpgroup per Q tile
+  static constexpr int kPerTile = 128;                    // softmax threads of one Q tile
+  // + a warpgroup of K producer, V producer, MMA issuer and one idle warp
+  static constexpr int kThreads = kSoftmax + 4 * 32;
+  // Registers: launched at 168 per thread (384 x 168 = 64512); the producer warpgroup gives
+  // back down to 72 and the two softmax warpgroups take 216: 256 x 216 + 128 x 72 = 64512.
+  static constexpr int kRegsSoftmax = 216;
+  static constexpr int kRegsOther = 72;
+  // TMEM columns: S/P of Q tile A [0,128), of Q tile B [128,256), O_A, O_B from 256.
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kOCol = 256;
+  static_assert(kQTiles * kKeys + kQTiles * D <= 512, "S/P buffers and accumulators fit TMEM");
+  static constexpr float kRescaleLog2 = 8.f;              // raise the max only past 2^8
+};
+
+template <int D, int BS>
+__global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
+  using C = PairCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t k_full[C::kKStages], k_empty[C::kKStages];
+  __shared__ __align__(8) uint64_t v_full[C::kVStages], v_empty[C::kVStages];
+  // Per Q tile: S_t(j + 1) is issued only after P_t V_j, which waits for the softmax's P_t(j),
+  // so each of these runs at most one phase ahead of its waiter (no parity ambiguity).
+  __shared__ __align__(8) uint64_t s_full[C::kQTiles], p_full[C::kQTiles];
+  __shared__ __align__(8) uint64_t q_full, drain;
+  __shared__ uint32_t tmem_base;
+  __shared__ int warp_count[C::kThreads / 32];
+  __shared__ int chosen_seq;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t q_s = smem_addr(smem);                     // Q tiles A, B
+  const uint32_t k_s = q_s + C::kQTiles * C::kQBytes;       // K ring
+  const uint32_t v_s = k_s + C::kKStages * C::kKVBytes;     // V ring
+  // Later q tiles of a chunk see more keys: dispatch them first so the grid's tail is short.
+  const int qt = gridDim.x - 1 - blockIdx.x, g = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq);
+  if (s < 0) return;
+
+  const int row0 = a.query_start_loc[s];
+  const int q_len = a.query_start_loc[s + 1] - row0;
+  if (q_len <= 1) return;  // decode rows and idle sequences are handled elsewhere
+  const int L = a.seq_lens[s];
+  const int tile_q = C::kRows / a.group;  // query tokens per Q tile
+  const int qbase = qt * C::kQTiles * tile_q;
+  if (q_len > L || (L + BS - 1) / BS > a.max_blocks || row0 < 0 ||
+      row0 + q_len > a.num_tokens) {
+    if (qt == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
+    return;
+  }
+  if ((q_len + C::kQTiles * tile_q - 1) / (C::kQTiles * tile_q) > static_cast<int>(gridDim.x)) {
+    if (qt == 0 && tid == 0) atomicOr(a.err, kErrHint);
+    return;
+  }
+  if (qbase >= q_len) return;
+  const int ctx = L - q_len;
+  // Key tiles of each Q tile: keys [0, ctx + last row + 1); Q tile B may hold no row at all.
+  int tiles[C::kQTiles];
+#pragma unroll
+  for (int t = 0; t < C::kQTiles; ++t) {
+    const int first = qbase + t * tile_q;
+    tiles[t] = first < q_len
+                   ? (ctx + min(q_len, first + tile_q) + C::kKeys - 1) / C::kKeys
+                   : 0;
+  }
+  const int kend = ctx + min(q_len, qbase + C::kQTiles * tile_q);  // keys loaded: [0, kend)
+  const int ntiles = (kend + C::kKeys - 1) / C::kKeys;             // == max over Q tiles
+
+  // Every block id the CTA will read is checked before any copy is issued.
+  int bad = 0;
+  const int nblk = (kend + BS - 1) / BS;
+  for (int j = tid; j < nblk; j += C::kThreads) {
+    const int32_t blk = a.block_tables[static_cast<int64_t>(s) * a.bt_stride + j];
+    if (blk < 0 || blk >= a.num_blocks) bad = 1;
+  }
+  if (__syncthreads_or(bad)) {
+    if (tid == 0) atomicOr(a.err, kErrBlockRange);
+    return;
+  }
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_base)),
+                 "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int st = 0; st < C::kKStages; ++st) {
+      mbar_init(smem_addr(&k_full[st]), 1);
+      mbar_init(smem_addr(&k_empty[st]), 1);
+    }
+    for (int st = 0; st < C::kVStages; ++st) {
+      mbar_init(smem_addr(&v_full[st]), 1);
+      mbar_init(smem_addr(&v_empty[st]), 1);
+    }
+    for (int t = 0; t < C::kQTiles; ++t) {
+      mbar_init(smem_addr(&s_full[t]), 1);
+      mbar_init(smem_addr(&p_full[t]), C::kPerTile);
+    }
+    mbar_init(smem_addr(&q_full), C::kSoftmax);
+    mbar_init(smem_addr(&drain), 1);
+    mbar_init_fence();
+  }
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  constexpr int kKWarp = C::kSoftmax / 32, kVWarp = kKWarp + 1, kMmaWarp = kKWarp + 2;
+  static_assert(C::kRegsSoftmax * C::kSoftmax + C::kRegsOther * (C::kThreads - C::kSoftmax) <=
+                    168 * C::kThreads,
+                "register split exceeds the launch allocation");
+  if (warp >= kKWarp) {
+  // ================================================ producer / MMA warpgroup (warps 8-11)
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsOther));
+  if (warp == kKWarp || warp == kVWarp) {
+    // ============================================================== producer warps (K, V)
+    const bool is_v = warp == kVWarp;
+    produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
+                                is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
+                                is_v ? v_empty : k_empty, is_v ? v_s : k_s);
+  } else if (warp == kMmaWarp && lane == 0) {
+    // ============================================================== MMA issuer (one thread)
+    constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0);
+    constexpr uint32_t kIdO = umma_idesc_f16(C::kRows, D, 0, 1);
+    // S_t(j) = Q_t K_j^T into TMEM buffer t (K stage j must have landed).
+    auto issue_s = [&](int t, int j) {
+      const uint32_t kst = k_s + (j % C::kKStages) * C::kKVBytes;
+      const uint32_t qb = q_s + t * C::kQBytes;
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * C::kHalfBytes + (k & 3) * 32;
+        umma_f16(tmem + t * C::kKeys, umma_sdesc(qb + off, 16, 1024),
+                 umma_sdesc(kst + (k >> 2) * (C::kKeys * 128) + (k & 3) * 32, 16, 1024), kIdS,
+                 k > 0);
+      }
+      umma_commit(smem_addr(&s_full[t]));
+    };
+    // O_t += P_t V_j (V stage j must have landed, P_t(j) must be written).
+    auto issue_pv = [&](int t, int j) {
+      const uint32_t vb = v_s + (j % C::kVStages) * C::kKVBytes;
+#pragma unroll
+      for (int k = 0; k < C::kKeys / 16; ++k)
+        umma_f16_tmem_a(tmem + C::kOCol + t * D, tmem + t * C::kKeys + k * 8,
+                        umma_sdesc(vb + k * 16 * 128, C::kKeys * 128, 1024), kIdO,
+                        (j > 0 || k > 0));
+    };
+    auto kwait = [&](int j) {
+      const bool ok = mbar_wait(smem_addr(&k_full[j % C::kKStages]), (j / C::kKStages) & 1, a.err);
+      tmem_fence_after_sync();
+      return ok;
+    };
+    bool ok = mbar_wait(smem_addr(&q_full), 0, a.err) && kwait(0);
+    if (ok) {
+#pragma unroll
+      for (int t = 0; t < C::kQTiles; ++t)
+        if (tiles[t] > 0) issue_s(t, 0);
+      umma_commit(smem_addr(&k_empty[0]));
+    }
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const int vst = j % C::kVStages;
+      const bool more = j + 1 < ntiles;
+      ok = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err) &&
+           (!more || kwait(j + 1));
+#pragma unroll
+      for (int t = 0; ok && t < C::kQTiles; ++t) {
+        if (j >= tiles[t]) continue;
+        ok = mbar_wait(smem_addr(&p_full[t]), j & 1, a.err);
+        if (!ok) break;
+        tmem_fence_after_sync();
+        issue_pv(t, j);
+        if (j + 1 < tiles[t]) issue_s(t, j + 1);
+      }
+      if (!ok) break;
+      umma_commit(smem_addr(&v_empty[vst]));
+      if (more) umma_commit(smem_addr(&k_empty[(j + 1) % C::kKStages]));
+    }
+    // Every MMA this thread issued has finished before O is read or the CTA tears down.
+    umma_commit(smem_addr(&drain));
+    mbar_wait(smem_addr(&drain), 0, a.err);
+  }  // warp 11 and lanes 1-31 of warp 10 have no role
+  } else {
+    // ============================================================== softmax warps 0-7
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
+    const int t = warp >> 2;                  // Q tile of this warpgroup
+    const int r = (warp & 3) * 32 + lane;     // TMEM lane = row of the Q tile
+    const int qi = r / a.group, hg = r % a.group;
+    const int first = qbase + t * tile_q;     // first query token of the Q tile
+    const int tok = first + qi;
+    const bool rv = qi < tile_q && tok < q_len;
+    const int pos = ctx + (rv ? tok : first);  // padding rows mirror the tile's first row
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t sbuf = tmem + lane_addr + t * C::kKeys;
+    const uint32_t obuf = tmem + lane_addr + C::kOCol + t * D;
+    const int my_tiles = tiles[t];
+    // The V rows past kend are zeroed by the Q tile whose P V of the last key tile comes first.
+    const bool zeroes_v = t == 0 ? tiles[0] == ntiles : tiles[0] < ntiles;
+
+    // The Q row -> shared memory, 128B-swizzled K-major.
+    {
+      const __half* qrow = a.q + static_cast<int64_t>(row0 + (rv ? tok : 0)) * a.q_stride +
+                           static_cast<int64_t>(g * a.group + hg) * D;
+      const uint32_t qb = q_s + t * C::kQBytes;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (rv) v = __ldg(reinterpret_cast<const uint4*>(qrow + c * 8));
+        const uint32_t dst = qb + (c >> 3) * C::kHalfBytes + swz128(r, c & 7);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+      }
+      fence_proxy_async();
+      mbar_arrive(smem_addr(&q_full));
+    }
+
+    bool stopped = false;  // a wait of this thread gave up
+    float m_run = -INFINITY, l_run = 0.f;
+    const int min_pos = ctx + first;
+    const bool prescale = !(a.scale_log2 > 0.f);
+    const float mul = prescale ? 1.f : a.scale_log2;  // exponent = fma(score, mul, -m)
+    for (int j = 0; j < my_tiles; ++j) {
+      // S_t(j) done; it was issued after P_t V_{j-1}, so O_t is settled too.
+      if (!mbar_wait(smem_addr(&s_full[t]), j & 1, a.err)) {
+        stopped = true;
+        break;
+      }
+      tmem_fence_after_sync();
+      uint32_t sv[C::kKeys / 32][32];
+#pragma unroll
+      for (int qq = 0; qq < C::kKeys / 32; ++qq) tmem_ld32(sbuf + qq * 32, sv[qq]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int qq = 0; qq < C::kKeys / 32; ++qq) tmem_regs_ready(sv[qq]);
+
+      // Scores stay raw where scale > 0 (the max commutes with the scale, which is folded into
+      // the exponent's FMA below); otherwise they are scaled here.  Masked keys become -inf.
+      const int key0 = j * C::kKeys;
+      const bool masked = key0 + C::kKeys - 1 > min_pos;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (prescale || masked) {
+#pragma unroll
+        for (int c = 0; c < C::kKeys; ++c) {
+          float v = __uint_as_float(sv[c >> 5][c & 31]);
+          if (prescale) v *= a.scale_log2;
+          if (masked && key0 + c > pos) v = -INFINITY;
+          sv[c >> 5][c & 31] = __float_as_uint(v);
+          m4[c & 3] = fmaxf(m4[c & 3], v);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::kKeys; ++c)
+          m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c >> 5][c & 31]));
+      }
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mul;
+      float alpha = 1.f;
+      if (mx > m_run + C::kRescaleLog2 || (m_run == -INFINITY && mx > -INFINITY)) {
+        alpha = ex2_approx(m_run - mx);  // 0 when m_run is still -inf
+        m_run = mx;
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t tt[32];
+          tmem_ld32(obuf + c0, tt);
+          tmem_wait_ld();
+          tmem_regs_ready(tt);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) tt[c] = __float_as_uint(__uint_as_float(tt[c]) * alpha);
+          tmem_st32(obuf + c0, tt);
+        }
+      }
+
+      // P (fp16) -> TMEM columns 0..63 of the buffer, two keys per column; l keeps the
+      // unrounded p.  A row with every key so far masked keeps m = -inf and gets p = 0.
+      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q4 = 0; q4 < C::kKeys / 32; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c]), mul, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c + 1]), mul, neg_m));
+          ps[c & 3] += p0 + p1;
+          pk[c] = pack_half2(p0, p1);
+        }
+        tmem_st16(sbuf + q4 * 16, pk);
+      }
+      l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+
+      const int tile0 = j * C::kKeys;
+      if (zeroes_v && j == ntiles - 1 && tile0 + C::kKeys > kend) {
+        // The last key tile: V rows at or past kend may be stale or NaN; zero them once the
+        // tile has landed (the MMA reads V only after p_full below).  Thread r clears row r.
+        const int vst = j % C::kVStages;
+        const bool landed = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err);
+        if (landed && tile0 + r >= kend) {
+          const uint32_t vrow = v_s + vst * C::kKVBytes + r * 128;
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               vrow + h * (C::kKeys * 128) + c * 16),
+                           "r"(0u), "r"(0u), "r"(0u), "r"(0u)
+                           : "memory");
+        }
+        fence_proxy_async();
+        if (!landed) {
+          stopped = true;
+          break;
+        }
+      }
+      tmem_wait_st();
+      tmem_fence_before_sync();
+      mbar_arrive(smem_addr(&p_full[t]));
+    }
+
+    // Epilogue: O_t / l -> out (fp16, rows of real query tokens only).
+    bool ok = !stopped && my_tiles > 0;
+    if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err);
+    if (!__any_sync(0xffffffffu, !ok)) {
+      tmem_fence_after_sync();
+      const float inv = 1.f / l_run;
+      __half* dst = a.out + (static_cast<int64_t>(row0 + tok) * a.num_q_heads + g * a.group + hg) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t tt[32];
+        tmem_ld32(obuf + c0, tt);
+        tmem_wait_ld();
+        tmem_regs_ready(tt);
+        if (rv) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 v;
+            v.x = pack_half2(__uint_as_float(tt[c]) * inv, __uint_as_float(tt[c + 1]) * inv);
+            v.y = pack_half2(__uint_as_float(tt[c + 2]) * inv, __uint_as_float(tt[c + 3]) * inv);
+            v.z = pack_half2(__uint_as_float(tt[c + 4]) * inv, __uint_as_float(tt[c + 5]) * inv);
+            v.w = pack_half2(__uint_as_float(tt[c + 6]) * inv, __uint_as_float(tt[c + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c0 + c) = v;
+          }
+        }
+      }
+    }
+  }
+
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::kTmemCols)
+                 : "memory");
+}
+
+template <int D>
+struct ParityCfg {
   static constexpr int kRows = 128;  // MMA M: (query token, head) rows of the tile
   static constexpr int kKeys = 128;  // keys per K/V tile: N of S, K of P V
-  static constexpr int kUnits = kKeys / 16;
   static constexpr int kHalves = D / 64;                  // 128-byte column chunks of a row
   static constexpr int kHalfBytes = kRows * 128;          // one 64-column chunk of a 128-row tile
   static constexpr int kQBytes = kHalves * kHalfBytes;    // [half][row][128 B]
@@ -59,10 +520,10 @@ struct PrefillCfg {
 };
 
 template <int D, int BS>
-__global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
-    prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
+    prefill_parity_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
-  using C = PrefillCfg<D>;
+  using C = ParityCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[C::kKStages], k_empty[C::kKStages];
   __shared__ __align__(8) uint64_t v_full[C::kVStages], v_empty[C::kVStages];
@@ -72,7 +533,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   __shared__ float red_m[2][128];  // [parity][row]: running max and sum for the final merge
   __shared__ float red_l[2][128];
   __shared__ int softmax_stop;  // set by a softmax thread whose wait gave up
-  __shared__ int warp_count[PrefillCfg<D>::kThreads / 32];
+  __shared__ int warp_count[ParityCfg<D>::kThreads / 32];
   __shared__ int chosen_seq;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -84,37 +545,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   const int qt = gridDim.x - 1 - blockIdx.x, g = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // Grid row z serves the z-th sequence with more than one query row (a block-wide ballot scan
-  // of query_start_loc), so decode rows cost the launch nothing.  Rows past the last such
-  // sequence have no work; more such sequences than rows is a hint error.
-  if (tid == 0) chosen_seq = -1;
-  int found = 0;  // prefill sequences seen so far
-  for (int s0 = 0; s0 < a.num_seqs; s0 += C::kThreads) {
-    const int si = s0 + tid;
-    const int ql = si < a.num_seqs ? a.query_start_loc[si + 1] - a.query_start_loc[si] : 0;
-    const bool pf = ql > 1;
-    const unsigned bal = __ballot_sync(0xffffffffu, pf);
-    // A one-row sequence when the decode launch was skipped on the hint's word is an error.
-    if (a.decode_skipped && __any_sync(0xffffffffu, ql == 1) && lane == 0 && blockIdx.x == 0 &&
-        blockIdx.y == 0 && blockIdx.z == 0)
-      atomicOr(a.err, kErrHint);
-    if (lane == 0) warp_count[warp] = __popc(bal);
-    __syncthreads();
-    int rank = found + __popc(bal & ((1u << lane) - 1u)), total = 0;
-#pragma unroll
-    for (int w = 0; w < C::kThreads / 32; ++w) {
-      rank += w < warp ? warp_count[w] : 0;
-      total += warp_count[w];
-    }
-    if (pf && rank == static_cast<int>(blockIdx.z)) chosen_seq = si;
-    found += total;
-    __syncthreads();
-  }
-  __syncthreads();
-  if (found > static_cast<int>(gridDim.z) && blockIdx.x == 0 && blockIdx.y == 0 &&
-      blockIdx.z == 0 && tid == 0)
-    atomicOr(a.err, kErrHint);
-  const int s = chosen_seq;
+  const int s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq);
   if (s < 0) return;
 
   const int row0 = a.query_start_loc[s];
@@ -190,40 +621,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
   if (warp == kKWarp || warp == kVWarp) {
     // ============================================================== producer warps (K, V)
     const bool is_v = warp == kVWarp;
-    const int stages = is_v ? C::kVStages : C::kKStages;
-    uint64_t* full = is_v ? v_full : k_full;
-    uint64_t* empty = is_v ? v_empty : k_empty;
-    const uint32_t ring = is_v ? v_s : k_s;
-    const CUtensorMap* map = is_v ? &vmap : &kmap;
-    int issued = 0;
-    for (int j = 0; j < ntiles; ++j) {
-      const int st = j % stages, round = j / stages;
-      bool ok = true;
-      if (lane == 0 && round > 0) ok = mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err);
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      const int key0 = j * C::kKeys;
-      const int units = min(C::kUnits, (kend - key0 + 15) >> 4);
-      const int id = lane < units
-                         ? a.block_tables[static_cast<int64_t>(s) * a.bt_stride + (key0 + 16 * lane) / BS]
-                         : 0;
-      const uint32_t bar = smem_addr(&full[st]);
-      if (lane == 0) mbar_arrive_expect_tx(bar, units * C::kHalves * 2048);
-      const uint32_t dst = ring + st * C::kKVBytes;
-      for (int u = 0; u < units; ++u) {
-        const int blk = __shfl_sync(0xffffffffu, id, u);
-        if (lane == 0) {
-          const int y = (blk * a.num_kv_heads + g) * BS + ((key0 + 16 * u) % BS);
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_2d(dst + h * (C::kKeys * 128) + u * 2048, map, h * 64, y, bar);
-        }
-      }
-      issued = j + 1;
-    }
-    // No copy may land after the CTA retires: wait (bounded) for the last tiles issued.
-    if (lane == 0)
-      for (int j = max(0, issued - stages); j < issued; ++j)
-        mbar_wait(smem_addr(&full[j % stages]), (j / stages) & 1, a.err);
+    produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
+                                is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
+                                is_v ? v_empty : k_empty, is_v ? v_s : k_s);
   } else if (warp == kMmaWarp && lane == 0) {
     // ============================================================== MMA issuer (one thread)
     // Issuing a tcgen05.mma waits until the pipe takes it and the pipe queues almost nothing,
@@ -457,11 +857,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                  : "memory");
 }
 
-template <int D, int BS>
-cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                             cudaStream_t stream) {
-  using C = PrefillCfg<D>;
-  auto kern = prefill_umma_kernel<D, BS>;
+// Both kernels share the launch shape rules: 384 threads, one CTA per SM (TMEM and shared
+// memory), and a register split that must fit the launch allocation.
+template <typename C, typename K>
+cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                       int rows_per_cta, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -472,10 +872,23 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const C
   if (attr.numRegs * C::kThreads < C::kRegsSoftmax * C::kSoftmax +
                                        C::kRegsOther * (C::kThreads - C::kSoftmax))
     return cudaErrorInvalidConfiguration;
-  const int tile_q = C::kRows / a.group;
-  dim3 grid((a.max_query_len + tile_q - 1) / tile_q, a.num_kv_heads, a.prefill_seqs);
+  const int rows_q = rows_per_cta / a.group;  // query tokens per CTA
+  dim3 grid((a.max_query_len + rows_q - 1) / rows_q, a.num_kv_heads, a.prefill_seqs);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
   return cudaGetLastError();
+}
+
+// Chunks that fit one Q tile (speculative verify, short chunks) go to the parity kernel, which
+// splits their key tiles between two softmax warpgroups; longer chunks to the pair kernel,
+// which gives each warpgroup its own Q tile and shares every K/V tile between them.
+template <int D, int BS>
+cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             cudaStream_t stream) {
+  if (a.max_query_len <= ParityCfg<D>::kRows / a.group)
+    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS>, a, kmap, vmap,
+                                    ParityCfg<D>::kRows, stream);
+  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS>, a, kmap, vmap,
+                                PairCfg<D>::kQTiles * PairCfg<D>::kRows, stream);
 }
 
 }  // namespace

@@ -113,6 +113,24 @@ def test_zero_and_negative_scale_match_oracle(sign, d):
     assert_close(out, oracle.attention_batch(b))
 
 
+@pytest.mark.parametrize("d, bs, hq, hkv", [(128, 16, 32, 4), (64, 32, 16, 4), (128, 32, 32, 2)])
+def test_both_prefill_kernels_match_oracle(d, bs, hq, hkv):
+    """Chunks that fit one 128-row Q tile go to the key-parity prefill kernel; a looser hint
+    (an upper bound is allowed) sends the same batch to the two-Q-tile kernel.  Both must agree
+    with the oracle."""
+    b = small_spec(d=d, bs=bs, hq=hq, hkv=hkv, seed=9410 + d + bs)
+    dev = "cuda"
+    ref = oracle.attention_batch(b)
+    args = [x.to(dev) for x in (b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                                b.query_start_loc)]
+    for max_q in (b.max_query_len, 200):
+        out = torch.full_like(args[0], float("nan"))
+        pa.attention(*args, b.scale, out, max_q, b.max_seq_len,
+                     num_prefill_seqs=b.num_prefill_seqs)
+        assert pa.get_device_error() == (0, 0)
+        assert_close(out, ref)
+
+
 @pytest.mark.parametrize("name", ["decode_d128_bs16_g4", "mixed_d128_bs32_g8", "prefix_d128_bs16"])
 def test_block_placement_is_bit_invariant(name):
     b = SMALL[name]()
