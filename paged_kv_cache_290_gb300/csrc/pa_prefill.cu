@@ -861,7 +861,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
 // memory), and a register split that must fit the launch allocation.
 template <typename C, typename K>
 cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                       int rows_per_cta, cudaStream_t stream) {
+                       int q_tiles, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -872,7 +872,8 @@ cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const
   if (attr.numRegs * C::kThreads < C::kRegsSoftmax * C::kSoftmax +
                                        C::kRegsOther * (C::kThreads - C::kSoftmax))
     return cudaErrorInvalidConfiguration;
-  const int rows_q = rows_per_cta / a.group;  // query tokens per CTA
+  // Query tokens per CTA: whole tokens per Q tile (128 / group rounds down), times the tiles.
+  const int rows_q = q_tiles * (C::kRows / a.group);
   dim3 grid((a.max_query_len + rows_q - 1) / rows_q, a.num_kv_heads, a.prefill_seqs);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
   return cudaGetLastError();
@@ -885,10 +886,9 @@ template <int D, int BS>
 cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
   if (a.max_query_len <= ParityCfg<D>::kRows / a.group)
-    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS>, a, kmap, vmap,
-                                    ParityCfg<D>::kRows, stream);
-  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS>, a, kmap, vmap,
-                                PairCfg<D>::kQTiles * PairCfg<D>::kRows, stream);
+    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS>, a, kmap, vmap, 1, stream);
+  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS>, a, kmap, vmap, PairCfg<D>::kQTiles,
+                                stream);
 }
 
 }  // namespace

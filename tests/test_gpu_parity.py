@@ -84,6 +84,13 @@ SMALL = {
     "spec_d128_bs16_g8": lambda: small_spec(),
     "spec_d64_bs32_g4": lambda: small_spec(d=64, bs=32, hq=16, hkv=4, seed=9401),
     "spec_d128_bs32_g16": lambda: small_spec(bs=32, hq=32, hkv=2, seed=9402),
+    # group sizes that do not divide 128: a Q tile holds 128 // G whole tokens
+    "mixed_d64_bs16_g3": lambda: small_mixed(d=64, hq=6, hkv=2, seed=9211),
+    # 84 tokens per CTA (two tiles of 42): a 170-row chunk needs 3 CTAs, not ceil(170 / 85)
+    "chunk170_d64_bs16_g3": lambda: W.build_batch(
+        "chunk170_g3", [W.SeqSpec(200, 170), W.SeqSpec(90, 1), W.SeqSpec(300, 40)],
+        num_q_heads=6, num_kv_heads=2, head_dim=64, block_size=16, seed_base=9213),
+    "mixed_d128_bs32_g6": lambda: small_mixed(bs=32, hq=12, hkv=2, seed=9212),
 }
 
 
@@ -129,6 +136,27 @@ def test_both_prefill_kernels_match_oracle(d, bs, hq, hkv):
                      num_prefill_seqs=b.num_prefill_seqs)
         assert pa.get_device_error() == (0, 0)
         assert_close(out, ref)
+
+
+@pytest.mark.parametrize("case", ["many_sequences", "many_pairs"])
+def test_prefill_many_sequences_and_tiles(case):
+    """A batch of 140 short verify chunks (the scan spans two rounds of the CTA's threads) and
+    one of nine 512-row chunks at 16 rows per CTA (288 CTAs per head): both must give the
+    oracle's result."""
+    g = torch.Generator().manual_seed(9500)
+    if case == "many_sequences":   # 140 short verify chunks
+        ctx = torch.randint(1, 41, (140,), generator=g).tolist()
+        ql = torch.randint(2, 5, (140,), generator=g).tolist()
+        b = W.build_batch("plan_seqs", [W.SeqSpec(c + q, q) for c, q in zip(ctx, ql)],
+                          num_q_heads=8, num_kv_heads=2, head_dim=64, block_size=16,
+                          seed_base=9501)
+    else:                          # 9 chunks of 512 rows, 16 rows per CTA: 288 pairs
+        ctx = torch.randint(0, 101, (9,), generator=g).tolist()
+        b = W.build_batch("plan_pairs", [W.SeqSpec(c + 512, 512) for c in ctx],
+                          num_q_heads=32, num_kv_heads=2, head_dim=64, block_size=16,
+                          seed_base=9502)
+    _, _, out = gpu_step(b, write=False)
+    assert_close(out, oracle.attention_batch(b))
 
 
 @pytest.mark.parametrize("name", ["decode_d128_bs16_g4", "mixed_d128_bs32_g8", "prefix_d128_bs16"])
