@@ -338,8 +338,8 @@ def run_ours(args, world, rank, local):
     peaks = load_peaks()
     peak, peak_src = peaks["hbm_gbs"], peaks["hbm_src"]
     kernels = kernel_rooflines(nbytes, kern_ms, peaks)
-    if "decode" in kernels:
-        kernels["decode"]["traffic"] = load_traffic(args.workload)
+    for k in kernels:
+        kernels[k]["traffic"] = load_traffic(args.workload, k)
     dominant = max(kernels, key=lambda k: kernels[k]["ms_per_launch"])
     value = world * nbytes["step_logical"] / (ms_max * 1e-3) / 1e9
     tok_s = world * nbytes["decode_rows"] / (ms_max * 1e-3)
@@ -394,17 +394,18 @@ def kernel_rooflines(nbytes, kern_ms, peaks) -> dict:
     return out
 
 
-def load_traffic(workload):
-    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if any, and
-    only while the kernel source is the one the counters were taken on (else None)."""
+def load_traffic(workload, kernel="decode"):
+    """DRAM bytes per launch of one kernel ("decode" or "prefill") on one workload, from the
+    committed ncu summaries (profiles/traffic.json), and only while that kernel's source file
+    is the one the counters were taken on (else None)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    entry = json.load(open(path)).get(workload)
+    entry = json.load(open(path)).get(workload if kernel == "decode" else f"{workload}:{kernel}")
     if not entry:
         return None
-    src = os.path.join(ROOT, "paged_kv_cache_290_gb300", "csrc", "pa_decode.cu")
+    src = os.path.join(ROOT, "paged_kv_cache_290_gb300", "csrc", entry.get("source", "pa_decode.cu"))
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     return entry["dram_bytes_per_launch"] if digest == entry.get("source_sha256_16") else None
 

@@ -87,6 +87,26 @@ def test_spec_verify_shapes_and_launches():
     assert {s.query_len for s in sp.seqs if s.query_len > 1} == {2, 3, 4, 5, 6}
 
 
+def test_traffic_is_reported_only_for_the_profiled_source(tmp_path, monkeypatch):
+    """ncu DRAM traffic from profiles/traffic.json is attached to a kernel's roofline only while
+    that kernel's source file hashes to the one the counters were taken on."""
+    import hashlib
+    import json
+    csrc = tmp_path / "paged_kv_cache_290_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "pa_prefill.cu").write_text("kernel v1")
+    h = hashlib.sha256(b"kernel v1").hexdigest()[:16]
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({
+        "w:prefill": {"dram_bytes_per_launch": 123, "source": "pa_prefill.cu",
+                      "source_sha256_16": h}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic("w", "prefill") == 123
+    assert bench.load_traffic("w", "decode") is None   # no entry for that kernel
+    (csrc / "pa_prefill.cu").write_text("kernel v2")  # source changed since the capture
+    assert bench.load_traffic("w", "prefill") is None
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
