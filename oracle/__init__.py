@@ -138,6 +138,89 @@ def copy_blocks(k_cache, v_cache, pairs):
     return kc, vc
 
 
+# ------------------------------------------------------------------ FP8 (E4M3) KV cache
+# E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no infinities; S.1111.111 is NaN,
+# so the largest finite magnitude is 1.75 * 2^8 = 448; exponent field 0 holds the subnormals
+# m * 2^-9.  A stored code c of a cache with scale s stands for s * value(c).
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 value of each E4M3 code (NaN for 0x7F / 0xFF), from the format's definition."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 0xF) & (m == 0x7), np.nan, mag)
+    return sign * mag
+
+
+_E4M3_POS = None
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 code of each float: the nearest finite code (ties to the even code), magnitudes at or
+    beyond 448 (and infinities) saturate to +-448, NaN -> 0x7F; the sign is kept, zero
+    included.  Found by search over the table of the 127 non-negative finite codes."""
+    global _E4M3_POS
+    if _E4M3_POS is None:
+        _E4M3_POS = e4m3_decode(np.arange(0x7F))  # codes 0x00 .. 0x7E, strictly increasing
+    xv = np.asarray(x, dtype=np.float64)
+    mag = np.abs(xv)
+    tab = _E4M3_POS
+    hi = np.clip(np.searchsorted(tab, mag, side="left"), 0, len(tab) - 1)
+    lo = np.clip(hi - 1, 0, len(tab) - 1)
+    d_lo, d_hi = np.abs(mag - tab[lo]), np.abs(tab[hi] - mag)
+    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(mag >= tab[-1], 0x7E, code)
+    code = code | np.where(np.signbit(xv), 0x80, 0)
+    code = np.where(np.isnan(xv), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def reshape_and_cache_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale: float, v_scale: float):
+    """FP8 scatter-write: (k_cache', v_cache') as uint8 arrays, copies of the pools with each new
+    token's rows stored as e4m3_encode(x * (1/scale)), the product taken in float32 (1/scale
+    too), slots < 0 skipped."""
+    kc = _np(k_cache, np.uint8).copy()
+    vc = _np(v_cache, np.uint8).copy()
+    sm = _np(slot_mapping, np.int64)
+    nb, hkv, bs, d = kc.shape
+    for x, pool, scale in ((k, kc, k_scale), (v, vc, v_scale)):
+        inv = np.float32(1.0) / np.float32(scale)
+        vals = half_bits_to_float32(_np(x, np.uint16)) * inv   # float32 * float32
+        codes = e4m3_encode(vals)
+        for t, slot in enumerate(sm.tolist()):
+            if 0 <= slot < nb * bs:
+                pool[slot // bs, :, slot % bs, :] = codes[t]
+    return kc, vc
+
+
+_HALF_LUT = None
+
+
+def half_bits_to_float32(bits) -> np.ndarray:
+    """binary16 bit patterns -> float32 (exact) through the oracle's own decoder."""
+    global _HALF_LUT
+    if _HALF_LUT is None:
+        _HALF_LUT = half_to_double(np.arange(1 << 16, dtype=np.uint16)).astype(np.float32)
+    return _HALF_LUT[np.asarray(bits, dtype=np.uint16)]
+
+
+def attention_fp8(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale,
+                  k_scale: float, v_scale: float, row_mask=None) -> np.ndarray:
+    """fp64 attention over an E4M3 cache: K = k_scale * value(code), V = v_scale * value(code).
+    Every E4M3 value is exact in binary16, so this is the fp16-pool attention of the decoded
+    codes with the score scale multiplied by k_scale (exact in fp64) and the output by
+    v_scale."""
+    kc, vc = _np(k_cache, np.uint8), _np(v_cache, np.uint8)
+    k16 = e4m3_decode(kc).astype(np.float16).view(np.uint16)
+    v16 = e4m3_decode(vc).astype(np.float16).view(np.uint16)
+    out = attention(q, k16, v16, block_tables, seq_lens, query_start_loc,
+                    float(scale) * float(k_scale), row_mask=row_mask)
+    return out * float(v_scale)
+
+
 def _attn_args(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc):
     q16 = _np(q, np.uint16)
     kc, vc = _np(k_cache, np.uint16), _np(v_cache, np.uint16)

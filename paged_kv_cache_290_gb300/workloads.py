@@ -89,6 +89,10 @@ class PagedBatch:
     v_contig: Optional[torch.Tensor] = None
     kv_start: Optional[torch.Tensor] = None   # int64 [N], row of k_contig where seq s starts
     meta: dict = field(default_factory=dict)
+    # "f16", or "e4m3": the pools hold E4M3 codes (uint8) standing for k_scale * value (v_scale)
+    kv_dtype: str = "f16"
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def num_seqs(self) -> int:
@@ -306,6 +310,24 @@ def repermute(b: PagedBatch, seed: int) -> PagedBatch:
     return out
 
 
+def to_fp8(b: PagedBatch, k_scale: float = 1.0 / 32, v_scale: float = 1.0 / 32) -> PagedBatch:
+    """The same batch over an FP8 (E4M3) cache with per-tensor scales: every pool value x becomes
+    the E4M3 code of x * (1 / scale) (float32), by torch's float8_e4m3fn conversion (round to
+    nearest even; the scales keep N(0,1) data far inside +-448).  NaN sentinels stay NaN (0x7F).
+    The new tokens stay fp16: the scatter-write quantises them."""
+    def q8(pool, scale):
+        if pool is None:
+            return None
+        inv = torch.tensor(1.0 / scale, dtype=torch.float32)
+        return (pool.float() * inv).to(torch.float8_e4m3fn).view(torch.uint8)
+    out = PagedBatch(**{**b.__dict__})
+    out.name = b.name + "_fp8"
+    out.k_cache, out.v_cache = q8(b.k_cache, k_scale), q8(b.v_cache, v_scale)
+    out.k_cache_pre, out.v_cache_pre = q8(b.k_cache_pre, k_scale), q8(b.v_cache_pre, v_scale)
+    out.kv_dtype, out.k_scale, out.v_scale = "e4m3", float(k_scale), float(v_scale)
+    return out
+
+
 # ---------------------------------------------------------------------------------------------
 # The five workloads.  Model names only fix head counts and head_dim.
 
@@ -392,4 +414,6 @@ WORKLOADS = {
     "mixed_step_bs32": lambda **kw: mixed_step(32, **kw),
     "mixed_step_bs16_8dec": lambda **kw: mixed_step(16, num_decode=8, **kw),
     "spec_verify": spec_verify,
+    "llama70b_32x8k_decode_fp8": lambda **kw: to_fp8(llama70b_decode(**kw)),
+    "llama70b_8x8k_decode_fp8": lambda **kw: to_fp8(llama70b_decode(8, **kw)),
 }

@@ -331,3 +331,80 @@ def test_descriptor_errors():
     bt[0, 0] = b.num_blocks                       # block id past the pool
     with pytest.raises(oracle.OracleError):
         oracle.attention(b.q, b.k_cache, b.v_cache, bt, b.seq_lens, b.query_start_loc, b.scale)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) KV cache
+
+def test_e4m3_decode_known_values():
+    """Values the E4M3 format fixes: zero, smallest subnormal 2^-9, largest subnormal 7 * 2^-9,
+    smallest normal 2^-6, one, two, the largest finite 448, negative zero and one, and the two
+    NaN codes."""
+    c = [0x00, 0x01, 0x07, 0x08, 0x38, 0x40, 0x7E, 0x80, 0xB8]
+    want = [0.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.0, 2.0, 448.0, -0.0, -1.0]
+    got = oracle.e4m3_decode(c)
+    assert got.tolist() == want and np.signbit(got[7])
+    assert np.isnan(oracle.e4m3_decode([0x7F, 0xFF])).all()
+
+
+def test_e4m3_table_is_monotone_symmetric_and_exact_in_fp16():
+    pos = oracle.e4m3_decode(np.arange(0x7F))
+    assert (np.diff(pos) > 0).all()
+    assert np.array_equal(oracle.e4m3_decode(np.arange(0x7F) | 0x80), -pos)
+    assert np.array_equal(pos.astype(np.float16).astype(np.float64), pos)
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    """Round to nearest, ties to even, against torch's float8_e4m3fn conversion: random values
+    inside +-448 and every exact midpoint between neighbouring codes."""
+    pos = oracle.e4m3_decode(np.arange(0x7F))
+    g = np.random.default_rng(290)
+    mids = (pos[1:] + pos[:-1]) / 2
+    x = np.concatenate([g.normal(0, 30, 20000), g.uniform(-447.9, 447.9, 20000), mids, -mids,
+                        pos, -pos, [2.0 ** -11, -2.0 ** -11]]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), ref)
+    assert np.array_equal(oracle.e4m3_encode(pos), np.arange(0x7F))  # round trip
+
+
+def test_e4m3_encode_saturates_and_keeps_sign_and_nan():
+    x = np.array([448.0, 463.9, 464.0, 500.0, 1e30, np.inf, -500.0, -np.inf, np.nan, -0.0],
+                 dtype=np.float32)
+    assert oracle.e4m3_encode(x).tolist() == [0x7E] * 6 + [0xFE, 0xFE, 0x7F, 0x80]
+
+
+def test_fp8_scatter_writes_codes_of_scaled_tokens():
+    """Each new token lands at its slot as the code of x * (1/scale) (float32 product, torch's
+    conversion as the independent encoder); every other byte of the pool is unchanged."""
+    b = W.to_fp8(small_mixed(d=64, hq=8, hkv=2, seed=9231), k_scale=0.05, v_scale=0.02)
+    kc, vc = oracle.reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
+                                          b.slot_mapping, b.k_scale, b.v_scale)
+    bs = b.block_size
+    for new, pool, pre, scale in ((b.k_new, kc, b.k_cache_pre, b.k_scale),
+                                  (b.v_new, vc, b.v_cache_pre, b.v_scale)):
+        inv = torch.tensor(1.0 / scale, dtype=torch.float32)
+        want = (new.float() * inv).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        touched = np.zeros(pool.shape, dtype=bool)
+        for t, slot in enumerate(b.slot_mapping.tolist()):
+            if slot >= 0:
+                assert np.array_equal(pool[slot // bs, :, slot % bs, :], want[t])
+                touched[slot // bs, :, slot % bs, :] = True
+        assert np.array_equal(pool[~touched], pre.numpy()[~touched])
+
+
+@pytest.mark.parametrize("make", [lambda: small_decode(d=64, hq=8, hkv=2, seed=9105),
+                                  lambda: small_mixed(d=64, bs=32, hq=8, hkv=4, seed=9232)])
+def test_fp8_attention_matches_brute_force_on_dequantised_kv(make):
+    """The FP8 attention equals a NumPy brute force over K = k_scale * value(code) and
+    V = v_scale * value(code), the codes taken from the contiguous K/V by torch's conversion."""
+    b = W.to_fp8(make(), k_scale=0.04, v_scale=0.03)
+    o = oracle.attention_fp8(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                             b.query_start_loc, b.scale, b.k_scale, b.v_scale)
+
+    def deq(x, scale):
+        inv = torch.tensor(1.0 / scale, dtype=torch.float32)
+        codes = (x.float() * inv).to(torch.float8_e4m3fn)
+        return codes.to(torch.float64) * scale
+
+    ref = brute_attention(b.q, deq(b.k_contig, b.k_scale), deq(b.v_contig, b.v_scale),
+                          b.kv_start, b.seq_lens, b.query_start_loc, b.scale)
+    assert np.allclose(o, ref, rtol=0, atol=1e-12, equal_nan=True)
