@@ -46,7 +46,8 @@ def algorithmic_bytes(b) -> dict:
     sequence ("logical"); "unique" counts each physical (block, offset) slot once, which is what
     the roofline of an aliased-prefix batch is measured against."""
     hkv, d, bs = b.num_kv_heads, b.head_dim, b.block_size
-    row_kv = hkv * d * 2 * 2  # K and V of one token, all kv heads, fp16
+    eb = 1 if b.kv_dtype == "e4m3" else 2  # bytes per cached value (E4M3 or fp16)
+    row_kv = hkv * d * eb * 2  # K and V of one token, all kv heads
     lens = np.array([s.seq_len for s in b.seqs], dtype=np.int64)
     qlens = np.array([s.query_len for s in b.seqs], dtype=np.int64)
     active = qlens > 0
@@ -63,7 +64,7 @@ def algorithmic_bytes(b) -> dict:
     table = int(((lens[active] + bs - 1) // bs).sum()) * 4
     desc = b.num_seqs * 4 + (b.num_seqs + 1) * 4
     t_new = int(b.k_new.shape[0])
-    cache = 2 * t_new * hkv * d * 2 * 2 + t_new * 8
+    cache = t_new * hkv * d * 2 * (2 + eb) + t_new * 8  # fp16 K/V read, cache values written
     attn = q_bytes + out_bytes + table + desc
 
     def flops(sel):
@@ -250,10 +251,12 @@ def run_ours(args, world, rank, local):
                                               b.max_seq_len)), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    sc = dict(k_scale=b.k_scale, v_scale=b.v_scale) if b.kv_dtype == "e4m3" else {}
+
     def step(q_, k_, v_, s_, bt_, sl_, qsl_, out_):
-        pa.reshape_and_cache(k_, v_, kc, vc, s_)
+        pa.reshape_and_cache(k_, v_, kc, vc, s_, **sc)
         pa.attention(q_, kc, vc, bt_, sl_, qsl_, b.scale, out_, b.max_query_len, b.max_seq_len,
-                     workspace=ws, num_prefill_seqs=b.num_prefill_seqs)
+                     workspace=ws, num_prefill_seqs=b.num_prefill_seqs, **sc)
 
     for i in range(args.warmup):
         flush.fill_(i & 255)
@@ -352,7 +355,8 @@ def run_ours(args, world, rank, local):
                    "num_tokens": b.num_tokens, "num_q_heads": b.num_q_heads,
                    "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
                    "block_size": b.block_size, "num_blocks": b.num_blocks,
-                   "partition_tokens": 512, "parallelism": f"replicas x{world}",
+                   "kv_cache_dtype": b.kv_dtype, "partition_tokens": 512,
+                   "parallelism": f"replicas x{world}",
                    "l2": "flushed before every timed step (512 MiB write, outside the events)"},
         "decode_tok_s_per_layer": tok_s,
         "hbm_roofline_frac_step": (nbytes["step_logical"] / (ms * 1e-3) / 1e9) / peak,
@@ -427,16 +431,20 @@ def _oracle_sample_seconds(b, seqs):
     import oracle
     q, bt, sl, qsl, rows = _sub_batch(b, seqs)
     t0 = time.perf_counter()
-    oracle.attention(q, b.k_cache, b.v_cache, bt, sl, qsl, b.scale)
+    if b.kv_dtype == "e4m3":
+        oracle.attention_fp8(q, b.k_cache, b.v_cache, bt, sl, qsl, b.scale, b.k_scale, b.v_scale)
+    else:
+        oracle.attention(q, b.k_cache, b.v_cache, bt, sl, qsl, b.scale)
     return time.perf_counter() - t0
 
 
 def _sample_bytes(b, seqs):
     hkv, d, bs = b.num_kv_heads, b.head_dim, b.block_size
+    eb = 1 if b.kv_dtype == "e4m3" else 2
     tot = 0
     for i in seqs:
         s = b.seqs[i]
-        tot += s.seq_len * hkv * d * 4 + 2 * s.query_len * b.num_q_heads * d * 2
+        tot += s.seq_len * hkv * d * eb * 2 + 2 * s.query_len * b.num_q_heads * d * 2
         tot += ((s.seq_len + bs - 1) // bs) * 4 + 8
     return tot
 

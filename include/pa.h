@@ -56,7 +56,12 @@ typedef enum pa_status {
   PA_ERR_NO_BLOCKS = 8    /* host block manager: too few free or evictable blocks */
 } pa_status;
 
-typedef enum pa_dtype { PA_F16 = 0, PA_I32 = 1, PA_I64 = 2 } pa_dtype;
+typedef enum pa_dtype {
+  PA_F16 = 0,
+  PA_I32 = 1,
+  PA_I64 = 2,
+  PA_F8E4M3 = 3 /* one byte: 1 sign, 4 exponent (bias 7), 3 mantissa bits; 0x7F/0xFF NaN, max 448 */
+} pa_dtype;
 
 typedef struct pa_tensor {
   void* data;                 /* device pointer, 16-byte aligned for fp16 tensors */
@@ -144,6 +149,41 @@ int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
                  void* stream);
 
 /*
+ * FP8 KV cache ("Local_LLM_03_vLLM_Architecture", KV-sizing slide: the cache's bytes per token
+ * decide how many sequences fit and how fast decode reads them; the pages quantise weights
+ * only, so storing K/V in 8 bits is this library's extension).  The pools are PA_F8E4M3
+ * [NB, Hkv, bs, d] with one scale per tensor: a stored code c of K stands for
+ * k_scale * value(c), of V for v_scale * value(c).  Both scales must be finite and > 0.
+ */
+typedef struct pa_kv_scales {
+  float k_scale;
+  float v_scale;
+} pa_kv_scales;
+
+/*
+ * pa_reshape_and_cache_fp8 -- pa_reshape_and_cache into an FP8 cache: each new value x (fp16)
+ * is stored as the E4M3 code of x * (1 / scale), the reciprocal and the product in float32,
+ * rounded to nearest even; magnitudes from 448 up (and infinities) saturate to +-448, NaN
+ * stays NaN.  Arguments and errors as pa_reshape_and_cache, with k_cache / v_cache PA_F8E4M3.
+ */
+int pa_reshape_and_cache_fp8(const pa_tensor* k, const pa_tensor* v, const pa_tensor* k_cache,
+                             const pa_tensor* v_cache, const pa_tensor* slot_mapping,
+                             const pa_kv_scales* scales, void* stream);
+
+/*
+ * pa_attention_fp8 -- pa_attention over an FP8 cache (q and out stay fp16).  Every E4M3 value
+ * is exact in fp16, so the kernel converts a K/V unit to fp16 in shared memory and runs the fp16
+ * path with the score scale multiplied by k_scale and the output by v_scale.  Decode rows
+ * only: a batch whose hint has max_query_len > 1 is refused with PA_ERR_UNSUPPORTED (prefill
+ * over an FP8 cache is not built).  Workspace as for pa_attention.
+ */
+int pa_attention_fp8(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                     const pa_tensor* block_tables, const pa_tensor* seq_lens,
+                     const pa_tensor* query_start_loc, float scale, const pa_tensor* out,
+                     const pa_batch_hint* hint, const pa_kv_scales* scales, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
  * pa_attention_static_scratch -- pa_attention without a caller-provided workspace, for callers
  * that cannot allocate device memory (no paper counterpart: the pages describe no such call).
  *
@@ -183,7 +223,7 @@ int pa_get_device_error(void* stream, uint32_t* bits);
  * pairs[i][0] are copied to block pairs[i][1] ("Local_LLM_03_vLLM_Architecture", prefix-caching
  * slide: shared blocks; a sequence that appends into a partial block it shares gets its own
  * copy first, the copy-on-write the host block manager asks for).
- *   k_cache, v_cache  fp16 [NB, Hkv, bs, d], contiguous, as for pa_attention.
+ *   k_cache, v_cache  [NB, Hkv, bs, d], contiguous, fp16 or PA_F8E4M3 (both the same).
  *   pairs             int32 [n, 2] contiguous device array (src, dst).  Destinations must be
  *                     distinct and never a source of the same call.
  * A pair with an id outside the pool is skipped and reported as PA_ERR_OUT_OF_RANGE by

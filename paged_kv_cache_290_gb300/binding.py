@@ -29,16 +29,19 @@ PA_ERR_NO_BLOCKS = 8
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
                 4: "PA_ERR_TIMEOUT", 5: "PA_ERR_OUT_OF_RANGE", 6: "PA_ERR_WORKSPACE",
                 7: "PA_ERR_DESCRIPTOR", 8: "PA_ERR_NO_BLOCKS"}
-PA_F16, PA_I32, PA_I64 = 0, 1, 2
+PA_F16, PA_I32, PA_I64, PA_F8E4M3 = 0, 1, 2, 3
 PARTITION_TOKENS = 512
 EXPORTED = ("pa_reshape_and_cache", "pa_attention_workspace_size", "pa_attention",
             "pa_last_error", "pa_get_device_error", "pa_set_timing_events", "pa_version",
-            "pa_attention_static_scratch", "pa_copy_blocks",
+            "pa_attention_static_scratch", "pa_copy_blocks", "pa_reshape_and_cache_fp8",
+            "pa_attention_fp8",
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_append",
             "pa_bm_truncate", "pa_bm_fork", "pa_bm_free", "pa_bm_stats", "pa_bm_sequence",
             "pa_bm_step_descriptor")
 
-_DTYPES = {torch.float16: PA_F16, torch.int32: PA_I32, torch.int64: PA_I64}
+# Byte tensors are E4M3 codes (the only one-byte type of the ABI).
+_DTYPES = {torch.float16: PA_F16, torch.int32: PA_I32, torch.int64: PA_I64,
+           torch.uint8: PA_F8E4M3, torch.float8_e4m3fn: PA_F8E4M3}
 
 
 class PATensor(ctypes.Structure):
@@ -49,6 +52,10 @@ class PATensor(ctypes.Structure):
 class PABatchHint(ctypes.Structure):
     _fields_ = [("max_query_len", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
                 ("num_prefill_seqs", ctypes.c_int32)]
+
+
+class PAKVScales(ctypes.Structure):
+    _fields_ = [("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class PAError(RuntimeError):
@@ -89,6 +96,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_set_timing_events.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.pa_copy_blocks.restype = ctypes.c_int
         lib.pa_copy_blocks.argtypes = [P, P, P, ctypes.c_void_p]
+        S = ctypes.POINTER(PAKVScales)
+        lib.pa_reshape_and_cache_fp8.restype = ctypes.c_int
+        lib.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, S, ctypes.c_void_p]
+        lib.pa_attention_fp8.restype = ctypes.c_int
+        lib.pa_attention_fp8.argtypes = [P, P, P, P, P, P, ctypes.c_float, P,
+                                         ctypes.POINTER(PABatchHint), S, ctypes.c_void_p,
+                                         ctypes.c_size_t, ctypes.c_void_p]
         I32, I64, VP = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
         PI32, PI64 = ctypes.POINTER(I32), ctypes.POINTER(I64)
         for name, res, args in (
@@ -146,11 +160,21 @@ def version() -> int:
     return load_library().pa_version()
 
 
-def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None) -> None:
-    """``pa_reshape_and_cache``: write new K/V tokens [T, Hkv, d] into pool slots (in place)."""
+def _is_fp8(pool) -> bool:
+    return pool.dtype in (torch.uint8, torch.float8_e4m3fn)
+
+
+def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None, k_scale=None,
+                      v_scale=None) -> None:
+    """``pa_reshape_and_cache``: write new K/V tokens [T, Hkv, d] into pool slots (in place).
+    A byte pool is an FP8 (E4M3) cache: ``pa_reshape_and_cache_fp8`` with the two scales."""
     lib = load_library()
     args = [ctypes.byref(describe(x)) for x in (k, v, k_cache, v_cache, slot_mapping)]
-    _check(lib.pa_reshape_and_cache(*args, _stream_handle(stream)))
+    if _is_fp8(k_cache):
+        sc = PAKVScales(float(k_scale), float(v_scale))
+        _check(lib.pa_reshape_and_cache_fp8(*args, ctypes.byref(sc), _stream_handle(stream)))
+    else:
+        _check(lib.pa_reshape_and_cache(*args, _stream_handle(stream)))
 
 
 def workspace_size(num_tokens: int, num_q_heads: int, head_dim: int, max_seq_len: int) -> int:
@@ -160,8 +184,9 @@ def workspace_size(num_tokens: int, num_q_heads: int, head_dim: int, max_seq_len
 
 def attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale: float, out,
               max_query_len: int, max_seq_len: int, workspace: Optional[torch.Tensor] = None,
-              stream=None, num_prefill_seqs: int = 0) -> torch.Tensor:
-    """``pa_attention`` for one mixed batch; writes ``out`` [T, Hq, d] and returns it.
+              stream=None, num_prefill_seqs: int = 0, k_scale=None, v_scale=None) -> torch.Tensor:
+    """``pa_attention`` for one mixed batch; writes ``out`` [T, Hq, d] and returns it.  A byte
+    pool is an FP8 (E4M3) cache: ``pa_attention_fp8`` with the two scales (decode rows only).
 
     ``workspace`` is a caller-owned uint8 device tensor of at least ``workspace_size(...)``
     bytes (allocated here when omitted).  ``num_prefill_seqs`` is the count of sequences with
@@ -174,9 +199,15 @@ def attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scal
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     hint = PABatchHint(int(max_query_len), int(max_seq_len), int(num_prefill_seqs))
     descs = [describe(x) for x in (q, k_cache, v_cache, block_tables, seq_lens, query_start_loc)]
-    _check(lib.pa_attention(*[ctypes.byref(d) for d in descs], ctypes.c_float(scale),
-                            ctypes.byref(describe(out)), ctypes.byref(hint), wptr, wbytes,
-                            _stream_handle(stream)))
+    if _is_fp8(k_cache):
+        sc = PAKVScales(float(k_scale), float(v_scale))
+        _check(lib.pa_attention_fp8(*[ctypes.byref(d) for d in descs], ctypes.c_float(scale),
+                                    ctypes.byref(describe(out)), ctypes.byref(hint),
+                                    ctypes.byref(sc), wptr, wbytes, _stream_handle(stream)))
+    else:
+        _check(lib.pa_attention(*[ctypes.byref(d) for d in descs], ctypes.c_float(scale),
+                                ctypes.byref(describe(out)), ctypes.byref(hint), wptr, wbytes,
+                                _stream_handle(stream)))
     return out
 
 

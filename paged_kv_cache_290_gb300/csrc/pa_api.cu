@@ -69,15 +69,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 2-D view of a pool [NB, Hkv, bs, d] as rows of d fp16 values; TMA box = 16 rows x 64 values
 // (128 B) with the 128-byte swizzle the kernels' fragment loads expect.
-int make_pool_map(CUtensorMap* m, void* base, int64_t rows, int d) {
+// The pool as a 2-D tensor of NB*Hkv*bs rows x d elements.  fp16: boxes of 16 rows x 64 values
+// (128 bytes), 128-byte swizzle.  FP8: boxes of 16 rows x d bytes, 128-byte swizzle for d = 128
+// and none for d = 64 (a 64-byte row).
+int make_pool_map(CUtensorMap* m, void* base, int64_t rows, int d, bool fp8 = false) {
   auto enc = tensor_map_encoder();
   if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * (fp8 ? 1 : 2)};
+  cuuint32_t box[2] = {fp8 ? static_cast<cuuint32_t>(d) : 64u, 16};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUtensorMapSwizzle swz =
+      !fp8 || d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                   base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
@@ -89,6 +94,7 @@ const char* dtype_name(int dt) {
     case PA_F16: return "float16";
     case PA_I32: return "int32";
     case PA_I64: return "int64";
+    case PA_F8E4M3: return "float8_e4m3";
     default: return "unknown";
   }
 }
@@ -129,10 +135,10 @@ int check_contiguous(const pa_tensor* t, const char* name) {
 }
 
 // Pool [NB, Hkv, bs, d] checks shared by both entry points.
-int check_pool(const pa_tensor* kc, const pa_tensor* vc) {
+int check_pool(const pa_tensor* kc, const pa_tensor* vc, int dtype = PA_F16) {
   int rc;
-  if ((rc = check_tensor(kc, "k_cache", PA_F16, 4))) return rc;
-  if ((rc = check_tensor(vc, "v_cache", PA_F16, 4))) return rc;
+  if ((rc = check_tensor(kc, "k_cache", dtype, 4))) return rc;
+  if ((rc = check_tensor(vc, "v_cache", dtype, 4))) return rc;
   for (int i = 0; i < 4; ++i)
     if (kc->shape[i] != vc->shape[i])
       return fail(PA_ERR_INVALID_ARG, "k_cache and v_cache shapes differ");
@@ -187,11 +193,22 @@ size_t pa_attention_workspace_size(int64_t num_tokens, int64_t num_q_heads, int6
   return workspace_layout(num_tokens, num_q_heads, head_dim, max_seq_len).total;
 }
 
-int pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_tensor* k_cache,
-                         const pa_tensor* v_cache, const pa_tensor* slot_mapping, void* stream) {
+static int check_scales(const pa_kv_scales* sc) {
+  if (!sc) return fail(PA_ERR_INVALID_ARG, "scales is NULL");
+  for (float x : {sc->k_scale, sc->v_scale})
+    if (!(x > 0.f) || !(x < INFINITY))
+      return fail(PA_ERR_INVALID_ARG, "k_scale and v_scale must be finite and > 0");
+  return PA_OK;
+}
+
+// The scatter-write into an fp16 cache (sc == NULL) or an FP8 cache with scales sc.
+static int reshape_impl(const pa_tensor* k, const pa_tensor* v, const pa_tensor* k_cache,
+                        const pa_tensor* v_cache, const pa_tensor* slot_mapping,
+                        const pa_kv_scales* sc, bool fp8, void* stream) {
   g_last_error.clear();
   int rc;
-  if ((rc = check_pool(k_cache, v_cache))) return rc;
+  if (fp8 && (rc = check_scales(sc))) return rc;
+  if ((rc = check_pool(k_cache, v_cache, fp8 ? PA_F8E4M3 : PA_F16))) return rc;
   if ((rc = check_tensor(k, "k", PA_F16, 3))) return rc;
   if ((rc = check_tensor(v, "v", PA_F16, 3))) return rc;
   if ((rc = check_tensor(slot_mapping, "slot_mapping", PA_I64, 1))) return rc;
@@ -214,8 +231,11 @@ int pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_tensor
   a.v = static_cast<const __half*>(v->data);
   a.k_stride = k->stride[0];
   a.v_stride = v->stride[0];
-  a.k_cache = static_cast<__half*>(k_cache->data);
-  a.v_cache = static_cast<__half*>(v_cache->data);
+  a.k_cache = k_cache->data;
+  a.v_cache = v_cache->data;
+  a.fp8 = fp8 ? 1 : 0;
+  a.k_inv = fp8 ? 1.0f / sc->k_scale : 1.f;
+  a.v_inv = fp8 ? 1.0f / sc->v_scale : 1.f;
   a.slot_mapping = static_cast<const int64_t*>(slot_mapping->data);
   a.num_tokens = t;
   a.num_kv_heads = static_cast<int>(hkv);
@@ -229,11 +249,23 @@ int pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_tensor
   return PA_OK;
 }
 
+int pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_tensor* k_cache,
+                         const pa_tensor* v_cache, const pa_tensor* slot_mapping, void* stream) {
+  return reshape_impl(k, v, k_cache, v_cache, slot_mapping, nullptr, false, stream);
+}
+
+int pa_reshape_and_cache_fp8(const pa_tensor* k, const pa_tensor* v, const pa_tensor* k_cache,
+                             const pa_tensor* v_cache, const pa_tensor* slot_mapping,
+                             const pa_kv_scales* scales, void* stream) {
+  return reshape_impl(k, v, k_cache, v_cache, slot_mapping, scales, true, stream);
+}
+
 int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_tensor* pairs,
                    void* stream) {
   g_last_error.clear();
   int rc;
-  if ((rc = check_pool(k_cache, v_cache))) return rc;
+  const bool fp8 = k_cache && k_cache->dtype == PA_F8E4M3;
+  if ((rc = check_pool(k_cache, v_cache, fp8 ? PA_F8E4M3 : PA_F16))) return rc;
   if ((rc = check_tensor(pairs, "pairs", PA_I32, 2))) return rc;
   if (pairs->shape[1] != 2 || (pairs->shape[0] > 1 && pairs->stride[0] != 2))
     return fail(PA_ERR_INVALID_ARG, "pairs must be a contiguous int32 [n, 2] array");
@@ -243,7 +275,7 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_
   a.v_cache = static_cast<uint4*>(v_cache->data);
   a.pairs = static_cast<const int32_t*>(pairs->data);
   a.num_pairs = pairs->shape[0];
-  a.chunks_per_block = k_cache->shape[1] * k_cache->shape[2] * k_cache->shape[3] / 8;
+  a.chunks_per_block = k_cache->shape[1] * k_cache->shape[2] * k_cache->shape[3] / (fp8 ? 16 : 8);
   a.num_blocks = k_cache->shape[0];
   cudaError_t e = device_error_word(&a.err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
@@ -252,14 +284,16 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_
   return PA_OK;
 }
 
-int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
-                 const pa_tensor* block_tables, const pa_tensor* seq_lens,
-                 const pa_tensor* query_start_loc, float scale, const pa_tensor* out,
-                 const pa_batch_hint* hint, void* workspace, size_t workspace_bytes,
-                 void* stream) {
+// Attention over an fp16 cache (fp8 false) or an FP8 cache with scales sc.
+static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                          const pa_tensor* block_tables, const pa_tensor* seq_lens,
+                          const pa_tensor* query_start_loc, float scale, const pa_tensor* out,
+                          const pa_batch_hint* hint, const pa_kv_scales* sc, bool fp8,
+                          void* workspace, size_t workspace_bytes, void* stream) {
   g_last_error.clear();
   int rc;
-  if ((rc = check_pool(k_cache, v_cache))) return rc;
+  if (fp8 && (rc = check_scales(sc))) return rc;
+  if ((rc = check_pool(k_cache, v_cache, fp8 ? PA_F8E4M3 : PA_F16))) return rc;
   if ((rc = check_tensor(q, "q", PA_F16, 3))) return rc;
   if ((rc = check_tensor(out, "out", PA_F16, 3))) return rc;
   if ((rc = check_tensor(block_tables, "block_tables", PA_I32, 2))) return rc;
@@ -296,6 +330,8 @@ int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   if (hint->max_query_len > hint->max_seq_len)
     return fail(PA_ERR_INVALID_ARG, "hint max_query_len exceeds max_seq_len");
   if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN");
+  if (fp8 && hint->max_query_len > 1)
+    return fail(PA_ERR_UNSUPPORTED, "prefill rows over an FP8 cache are not built (decode only)");
   const WorkspaceLayout ws = workspace_layout(t, hq, d, hint->max_seq_len);
   if (ws.total > 0) {
     if (!workspace || workspace_bytes < ws.total)
@@ -333,14 +369,17 @@ int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   // Every sequence has several rows (by the hint): no decode rows, so no decode or merge launch.
   const bool all_prefill = hint->max_query_len > 1 && hint->num_prefill_seqs >= n;
   a.decode_skipped = all_prefill ? 1 : 0;
-  a.scale_log2 = scale * 1.4426950408889634f;
+  // FP8: K = k_scale * code value, so the score scale takes k_scale; V's scale goes on the output.
+  a.scale_log2 = scale * 1.4426950408889634f * (fp8 ? sc->k_scale : 1.f);
+  a.v_scale = fp8 ? sc->v_scale : 1.f;
+  a.kv_fp8 = fp8 ? 1 : 0;
   cudaError_t e = device_error_word(&a.err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
 
   const int64_t rows = k_cache->shape[0] * hkv * k_cache->shape[2];
   CUtensorMap kmap, vmap;
-  if ((rc = make_pool_map(&kmap, k_cache->data, rows, static_cast<int>(d)))) return rc;
-  if ((rc = make_pool_map(&vmap, v_cache->data, rows, static_cast<int>(d)))) return rc;
+  if ((rc = make_pool_map(&kmap, k_cache->data, rows, static_cast<int>(d), fp8))) return rc;
+  if ((rc = make_pool_map(&vmap, v_cache->data, rows, static_cast<int>(d), fp8))) return rc;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   auto mark = [&](int kernel, bool stop) {
@@ -364,6 +403,24 @@ int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
     if ((e = mark(PA_TIMED_PREFILL, true)) != cudaSuccess) return cuda_fail(e, "timing event");
   }
   return PA_OK;
+}
+
+int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                 const pa_tensor* block_tables, const pa_tensor* seq_lens,
+                 const pa_tensor* query_start_loc, float scale, const pa_tensor* out,
+                 const pa_batch_hint* hint, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  return attention_impl(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out,
+                        hint, nullptr, false, workspace, workspace_bytes, stream);
+}
+
+int pa_attention_fp8(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                     const pa_tensor* block_tables, const pa_tensor* seq_lens,
+                     const pa_tensor* query_start_loc, float scale, const pa_tensor* out,
+                     const pa_batch_hint* hint, const pa_kv_scales* scales, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return attention_impl(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out,
+                        hint, scales, true, workspace, workspace_bytes, stream);
 }
 
 int pa_set_timing_events(int kernel, void* start, void* stop) {

@@ -7,7 +7,8 @@
 //
 // One thread moves one 16-byte chunk of K and the matching chunk of V; consecutive threads
 // cover consecutive chunks of a (token, head) row, so both the reads and the writes of a row are
-// full 128-byte-line transactions.  Pure copy: the cache receives the exact bit patterns.
+// full 128-byte-line transactions.  fp16 cache: a pure copy, the cache receives the exact bit
+// patterns.  FP8 cache: a chunk is 16 codes, each the E4M3 code of x * (1/scale) (float32).
 #include "pa_common.cuh"
 #include "pa_kernels.h"
 
@@ -38,8 +39,50 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheArgs 
     const int64_t dst = ((blk * a.num_kv_heads + h) * a.block_size + off) * D + ch * 8;
     const uint4 kv = __ldg(reinterpret_cast<const uint4*>(a.k + t * a.k_stride + h * D + ch * 8));
     const uint4 vv = __ldg(reinterpret_cast<const uint4*>(a.v + t * a.v_stride + h * D + ch * 8));
-    *reinterpret_cast<uint4*>(a.k_cache + dst) = kv;
-    *reinterpret_cast<uint4*>(a.v_cache + dst) = vv;
+    *reinterpret_cast<uint4*>(static_cast<__half*>(a.k_cache) + dst) = kv;
+    *reinterpret_cast<uint4*>(static_cast<__half*>(a.v_cache) + dst) = vv;
+  }
+}
+
+// 16 fp16 values (two 16-byte loads) -> 16 E4M3 codes of x * inv.
+__device__ __forceinline__ uint4 quantize16(const __half* src, float inv) {
+  const uint4 lo = __ldg(reinterpret_cast<const uint4*>(src));
+  const uint4 hi = __ldg(reinterpret_cast<const uint4*>(src + 8));
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  uint32_t c[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    c[i] = e4m3x2_from_f32(f.x * inv, f.y * inv);
+  }
+  return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16),
+                    c[6] | (c[7] << 16));
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(const CacheArgs a) {
+  constexpr int kChunks = D / 16;  // 16-byte chunks (16 codes) per (token, head) row
+  grid_launch_dependents();
+  const int64_t total = a.num_tokens * a.num_kv_heads * kChunks;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int ch = static_cast<int>(idx % kChunks);
+    const int64_t row = idx / kChunks;
+    const int h = static_cast<int>(row % a.num_kv_heads);
+    const int64_t t = row / a.num_kv_heads;
+    const int64_t slot = a.slot_mapping[t];
+    if (slot < 0) continue;  // padding token
+    if (slot >= a.num_blocks * a.block_size) {
+      atomicOr(a.err, kErrSlotRange);
+      continue;
+    }
+    const int64_t blk = slot / a.block_size;
+    const int64_t off = slot % a.block_size;
+    const int64_t dst = ((blk * a.num_kv_heads + h) * a.block_size + off) * D + ch * 16;
+    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.k_cache) + dst) =
+        quantize16(a.k + t * a.k_stride + h * D + ch * 16, a.k_inv);
+    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.v_cache) + dst) =
+        quantize16(a.v + t * a.v_stride + h * D + ch * 16, a.v_inv);
   }
 }
 
@@ -75,15 +118,21 @@ cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_reshape_and_cache(const CacheArgs& a, cudaStream_t stream) {
-  const int64_t total = a.num_tokens * a.num_kv_heads * (a.head_dim / 8);
+  const int64_t total = a.num_tokens * a.num_kv_heads * (a.head_dim / (a.fp8 ? 16 : 8));
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t want = (total + threads - 1) / threads;
   const int blocks = static_cast<int>(want < 152 * 64 ? want : 152 * 64);
-  if (a.head_dim == 128)
+  if (a.fp8) {
+    if (a.head_dim == 128)
+      reshape_and_cache_fp8_kernel<128><<<blocks, threads, 0, stream>>>(a);
+    else
+      reshape_and_cache_fp8_kernel<64><<<blocks, threads, 0, stream>>>(a);
+  } else if (a.head_dim == 128) {
     reshape_and_cache_kernel<128><<<blocks, threads, 0, stream>>>(a);
-  else
+  } else {
     reshape_and_cache_kernel<64><<<blocks, threads, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -279,6 +279,22 @@ __device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
+// Two floats -> two E4M3 codes, lo in the low byte: round to nearest even, magnitudes beyond
+// 448 saturate to +-448, NaN stays NaN (PTX cvt with .satfinite; a goes to the upper byte).
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two E4M3 codes (lo in the low byte) -> an fp16 pair (lo in the low half); exact.
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t codes16) {
+  uint32_t r;
+  const uint16_t c = static_cast<uint16_t>(codes16);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+  return r;
+}
+
 // 2^x by the PTX approximate base-2 exponential (flushes subnormal results to zero; -inf -> +0).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -18,6 +18,10 @@
 //   * the 4 warps' (m, l, O) are combined in shared memory; a single-partition sequence writes
 //     fp16 output directly, otherwise the partition writes fp32 (m, l, O/l) partials that the
 //     merge kernel combines:  M = max m_p,  w_p = 2^(m_p - M) l_p,  out = sum w_p o_p / sum w_p.
+// FP8 (E4M3) cache: a unit is 16 rows of d bytes (one TMA box each for K and V, half the bytes);
+// the warp converts K, then V, into an fp16 staging buffer laid out like an fp16 stage (exact:
+// every E4M3 value is an fp16 value) and runs the same tensor-core path; k_scale is folded into
+// the score scale and v_scale multiplies the outputs.
 // Both kernels are programmatic dependents of what precedes them on the stream: they may be
 // scheduled early but read nothing from global memory before griddepcontrol.wait.
 #include <algorithm>
@@ -28,34 +32,69 @@
 namespace pa {
 namespace {
 
-template <int D, int BS, int NT>
+template <int D, int BS, int NT, bool F8>
 struct DecodeCfg {
   static constexpr int kWarps = 4;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kHalves = D / 64;                // 128-byte boxes per token row
+  static constexpr int kHalves = D / 64;                // 128-byte fp16 boxes per token row
   static constexpr int kBoxBytes = 16 * 128;            // 16 token rows x 128 B
-  static constexpr int kKBytes = kHalves * kBoxBytes;   // K of one 16-token unit
+  static constexpr int kF16Bytes = kHalves * kBoxBytes; // fp16 K (or V) of one 16-token unit
+  static constexpr int kKBytes = F8 ? 16 * D : kF16Bytes;  // K of one unit as stored in a stage
   static constexpr int kStageBytes = 2 * kKBytes;       // K + V
-  static constexpr int kStages = (64 * 1024) / (kWarps * kStageBytes);
+  static constexpr int kStages = (F8 ? 48 * 1024 : 64 * 1024) / (kWarps * kStageBytes);
   static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+  static constexpr int kStagingBytes = F8 ? kF16Bytes : 0;  // per warp: one unit's K or V, fp16
   static constexpr int kUnitsPerPart = kPartitionTokens / 16;
   static constexpr int kDK = D / 16;
   static constexpr int kHeads = NT * 8;
   static constexpr int kMergeBytes = kWarps * kHeads * (D + 2) * 4;
-  static constexpr int kSmemBytes = (kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes) + 1024;
+  static constexpr int kDataBytes = kRingBytes + kWarps * kStagingBytes;
+  static constexpr int kSmemBytes = (kDataBytes > kMergeBytes ? kDataBytes : kMergeBytes) + 1024;
   static_assert(kStages >= 1, "stage ring");
   static_assert(BS % 16 == 0, "block size must be a multiple of the 16-token unit");
 };
+
+// One 16-token unit of E4M3 codes (16 rows x D bytes; 128-byte swizzled rows for D = 128, plain
+// 64-byte rows for D = 64, as the TMA box lands) -> fp16 in the layout of an fp16 stage:
+// [D / 64][16 rows][128 B], 16-byte chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4).
+template <int D>
+__device__ __forceinline__ void e4m3_unit_to_f16(uint32_t src, uint32_t dst, int lane) {
+  constexpr int kRowChunks = D / 16;                 // 16-byte code chunks per row
+  constexpr int kPerLane = 16 * kRowChunks / 32;
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int q = lane + 32 * i;
+    const int r = q / kRowChunks, c8 = q % kRowChunks;
+    const uint32_t sa = D == 128 ? src + r * 128 + ((c8 ^ (r & 7)) << 4) : src + r * 64 + c8 * 16;
+    uint32_t w0, w1, w2, w3;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                 : "r"(sa)
+                 : "memory");
+    const int e = 2 * c8;                            // fp16 chunk of the code chunk's first half
+    const uint32_t half = dst + (e >> 3) * (16 * 128) + r * 128;
+    const uint32_t d0 = half + (((e & 7) ^ (r & 7)) << 4);
+    const uint32_t d1 = half + ((((e & 7) + 1) ^ (r & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d0),
+                 "r"(f16x2_from_e4m3x2(w0)), "r"(f16x2_from_e4m3x2(w0 >> 16)),
+                 "r"(f16x2_from_e4m3x2(w1)), "r"(f16x2_from_e4m3x2(w1 >> 16))
+                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d1),
+                 "r"(f16x2_from_e4m3x2(w2)), "r"(f16x2_from_e4m3x2(w2 >> 16)),
+                 "r"(f16x2_from_e4m3x2(w3)), "r"(f16x2_from_e4m3x2(w3 >> 16))
+                 : "memory");
+  }
+}
 
 __device__ __forceinline__ uint32_t ldg_u32(const __half* p) {
   return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
-template <int D, int BS, int NT>
-__global__ void __launch_bounds__(DecodeCfg<D, BS, NT>::kThreads)
+template <int D, int BS, int NT, bool F8>
+__global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
     decode_partition_kernel(const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
-  using C = DecodeCfg<D, BS, NT>;
+  using C = DecodeCfg<D, BS, NT, F8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[C::kWarps][C::kStages];
   __shared__ int32_t unit_row[C::kUnitsPerPart];
@@ -123,10 +162,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT>::kThreads)
     const uint32_t kdst = ring + st * C::kStageBytes;
     const int y = unit_row[u];
     mbar_arrive_expect_tx(bar, C::kStageBytes);
+    if constexpr (F8) {  // one box of 16 rows x D bytes each
+      tma_load_2d(kdst, &kmap, 0, y, bar);
+      tma_load_2d(kdst + C::kKBytes, &vmap, 0, y, bar);
+    } else {
 #pragma unroll
-    for (int h = 0; h < C::kHalves; ++h) {
-      tma_load_2d(kdst + h * C::kBoxBytes, &kmap, h * 64, y, bar);
-      tma_load_2d(kdst + C::kKBytes + h * C::kBoxBytes, &vmap, h * 64, y, bar);
+      for (int h = 0; h < C::kHalves; ++h) {
+        tma_load_2d(kdst + h * C::kBoxBytes, &kmap, h * 64, y, bar);
+        tma_load_2d(kdst + C::kKBytes + h * C::kBoxBytes, &vmap, h * 64, y, bar);
+      }
     }
   };
   if (lane == 0) {
@@ -171,8 +215,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT>::kThreads)
     }
     const int u = warp + i * C::kWarps;
     const int nvalid = min(16, tok_end - (tok_begin + u * 16));
-    const uint32_t kb = ring + st * C::kStageBytes;
-    const uint32_t vb = kb + C::kKBytes;
+    const uint32_t stage = ring + st * C::kStageBytes;
+    // fp16 K (and later V) of the unit: the stage itself, or the warp's staging buffer.
+    const uint32_t staging = smem_addr(smem + C::kRingBytes + warp * C::kStagingBytes);
+    uint32_t kb = stage, vb = stage + C::kKBytes;
+    if constexpr (F8) {
+      e4m3_unit_to_f16<D>(stage, staging, lane);
+      __syncwarp();
+      kb = vb = staging;
+    }
 
     // ---- S^T[16 tokens][8 heads] = K Q^T
     float sacc[NT][4];
@@ -221,6 +272,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT>::kThreads)
       }
       pb0[nt] = movmatrix_trans(pack_half2(p00, p01));  // P^T[tok 2cq..2cq+1][head gq]
       pb1[nt] = movmatrix_trans(pack_half2(p10, p11));  // P^T[tok 2cq+8..][head gq]
+    }
+
+    if constexpr (F8) {  // every lane's K fragments are loaded: V takes the staging buffer
+      __syncwarp();
+      e4m3_unit_to_f16<D>(stage + C::kKBytes, staging, lane);
+      __syncwarp();
     }
 
     // ---- O^T[d][heads] += V^T[d][16 tokens] P^T
@@ -311,10 +368,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT>::kThreads)
     const int hq = g * a.group + h;
     const int64_t orow = static_cast<int64_t>(row0) * a.num_q_heads + hq;
     if (nparts == 1) {
-      a.out[orow * D + d] = __float2half_rn(osum / wsum);
+      a.out[orow * D + d] = __float2half_rn(osum / wsum * a.v_scale);
     } else {
       const int64_t pidx = orow * a.max_parts + part;
-      a.part_o[pidx * D + d] = osum / wsum;
+      a.part_o[pidx * D + d] = osum / wsum * a.v_scale;
       if (d == 0) {
         a.part_m[pidx] = M;
         a.part_l[pidx] = wsum;
@@ -394,11 +451,11 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a)
   }
 }
 
-template <int D, int BS, int NT>
+template <int D, int BS, int NT, bool F8>
 cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t stream) {
-  using C = DecodeCfg<D, BS, NT>;
-  auto kern = decode_partition_kernel<D, BS, NT>;
+  using C = DecodeCfg<D, BS, NT, F8>;
+  auto kern = decode_partition_kernel<D, BS, NT, F8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -416,10 +473,17 @@ cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CU
   return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
-template <int D, int BS>
+template <int D, int BS, bool F8>
 cudaError_t launch_decode_g(const AttnArgs& a, const CUtensorMap& k, const CUtensorMap& v,
                             cudaStream_t st) {
-  return a.group <= 8 ? launch_decode_t<D, BS, 1>(a, k, v, st) : launch_decode_t<D, BS, 2>(a, k, v, st);
+  return a.group <= 8 ? launch_decode_t<D, BS, 1, F8>(a, k, v, st)
+                      : launch_decode_t<D, BS, 2, F8>(a, k, v, st);
+}
+
+template <int D, int BS>
+cudaError_t launch_decode_f(const AttnArgs& a, const CUtensorMap& k, const CUtensorMap& v,
+                            cudaStream_t st) {
+  return a.kv_fp8 ? launch_decode_g<D, BS, true>(a, k, v, st) : launch_decode_g<D, BS, false>(a, k, v, st);
 }
 
 }  // namespace
@@ -427,10 +491,10 @@ cudaError_t launch_decode_g(const AttnArgs& a, const CUtensorMap& k, const CUten
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream) {
   if (a.head_dim == 128)
-    return a.block_size == 16 ? launch_decode_g<128, 16>(a, kmap, vmap, stream)
-                              : launch_decode_g<128, 32>(a, kmap, vmap, stream);
-  return a.block_size == 16 ? launch_decode_g<64, 16>(a, kmap, vmap, stream)
-                            : launch_decode_g<64, 32>(a, kmap, vmap, stream);
+    return a.block_size == 16 ? launch_decode_f<128, 16>(a, kmap, vmap, stream)
+                              : launch_decode_f<128, 32>(a, kmap, vmap, stream);
+  return a.block_size == 16 ? launch_decode_f<64, 16>(a, kmap, vmap, stream)
+                            : launch_decode_f<64, 32>(a, kmap, vmap, stream);
 }
 
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream) {

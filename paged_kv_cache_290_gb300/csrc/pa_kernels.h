@@ -15,8 +15,11 @@ struct CacheArgs {
   const __half* v;
   int64_t k_stride;  // elements between consecutive tokens of k
   int64_t v_stride;
-  __half* k_cache;
-  __half* v_cache;
+  void* k_cache;  // fp16, or E4M3 bytes when fp8
+  void* v_cache;
+  int fp8;        // 1: store E4M3 codes of x * k_inv (v_inv)
+  float k_inv;    // 1 / k_scale in float32
+  float v_inv;
   const int64_t* slot_mapping;
   int64_t num_tokens;
   int num_kv_heads;
@@ -50,7 +53,9 @@ struct AttnArgs {
   int max_query_len;
   int prefill_seqs;  // sequences the prefill launch covers (<= num_seqs)
   int decode_skipped;  // 1: the hint promised no one-row sequence, so no decode launch was made
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // scale * log2(e) (times k_scale for an FP8 cache)
+  float v_scale;     // FP8 cache: multiplies the output; 1 for fp16
+  int kv_fp8;        // 1: the pools hold E4M3 codes
   unsigned* err;
 };
 

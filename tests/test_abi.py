@@ -24,7 +24,7 @@ def declared_functions():
     names = set()
     for h in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names.update(re.findall(r"\b(pa_[a-z_]+)\s*\(", text))
+        names.update(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text))
     return sorted(names)
 
 
@@ -176,3 +176,56 @@ def test_batch_descriptor_from_host():
     assert d.query_start_loc.tolist() == [0, 5, 6, 8]
     assert d.slot_mapping.tolist() == [48, 49, 50, 51, 52, 4 * 16 + 7, 7 * 16 + 15, 6 * 16 + 0]
     assert d.max_query_len == 5 and d.max_seq_len == 40 and d.num_prefill_seqs == 2
+
+
+# --------------------------------------------------------------- FP8 cache entry points
+
+def call_attention_fp8(lib, k_scale=0.05, v_scale=0.02, hint=(1, 100), pool_dtype=B.PA_F8E4M3,
+                       null_scales=False):
+    n, hq, hkv, d, bs, nb, mb = 3, 8, 2, 128, 16, 40, 8
+    q = T(B.PA_F16, [n, hq, d])
+    kc = T(pool_dtype, [nb, hkv, bs, d])
+    vc = T(pool_dtype, [nb, hkv, bs, d])
+    out = T(B.PA_F16, [n, hq, d])
+    sc = None if null_scales else ctypes.byref(B.PAKVScales(k_scale, v_scale))
+    return lib.pa_attention_fp8(ctypes.byref(q), ctypes.byref(kc), ctypes.byref(vc),
+                                ctypes.byref(T(B.PA_I32, [n, mb])), ctypes.byref(T(B.PA_I32, [n])),
+                                ctypes.byref(T(B.PA_I32, [n + 1])), ctypes.c_float(0.1),
+                                ctypes.byref(out), ctypes.byref(B.PABatchHint(*hint)), sc, None,
+                                0, None)
+
+
+@pytest.mark.parametrize("kw, status, text", [
+    (dict(pool_dtype=B.PA_F16), B.PA_ERR_INVALID_ARG, "float8_e4m3"),
+    (dict(k_scale=0.0), B.PA_ERR_INVALID_ARG, "finite and > 0"),
+    (dict(v_scale=-1.0), B.PA_ERR_INVALID_ARG, "finite and > 0"),
+    (dict(k_scale=float("nan")), B.PA_ERR_INVALID_ARG, "finite and > 0"),
+    (dict(v_scale=float("inf")), B.PA_ERR_INVALID_ARG, "finite and > 0"),
+    (dict(null_scales=True), B.PA_ERR_INVALID_ARG, "scales is NULL"),
+    (dict(hint=(4, 100)), B.PA_ERR_UNSUPPORTED, "FP8"),
+])
+def test_attention_fp8_rejects_bad_arguments(lib, kw, status, text):
+    assert call_attention_fp8(lib, **kw) == status
+    assert text in msg(lib), msg(lib)
+
+
+def test_fp16_entry_rejects_an_fp8_pool(lib):
+    kc = T(B.PA_F8E4M3, [40, 2, 16, 64])
+    assert call_attention(lib, kc=kc, vc=T(B.PA_F8E4M3, [40, 2, 16, 64])) == B.PA_ERR_INVALID_ARG
+    assert "float16" in msg(lib)
+
+
+def test_reshape_fp8_checks_scales_and_dtype(lib):
+    t, hkv, d, bs, nb = 5, 2, 128, 16, 10
+    args = [ctypes.byref(x) for x in (T(B.PA_F16, [t, hkv, d]), T(B.PA_F16, [t, hkv, d]),
+                                       T(B.PA_F8E4M3, [nb, hkv, bs, d]),
+                                       T(B.PA_F8E4M3, [nb, hkv, bs, d]), T(B.PA_I64, [t]))]
+    assert lib.pa_reshape_and_cache_fp8(*args, None, None) == B.PA_ERR_INVALID_ARG
+    assert "scales" in msg(lib)
+    bad = ctypes.byref(B.PAKVScales(1.0, 0.0))
+    assert lib.pa_reshape_and_cache_fp8(*args, bad, None) == B.PA_ERR_INVALID_ARG
+    empty = [ctypes.byref(x) for x in (T(B.PA_F16, [0, hkv, d]), T(B.PA_F16, [0, hkv, d]),
+                                        T(B.PA_F8E4M3, [nb, hkv, bs, d]),
+                                        T(B.PA_F8E4M3, [nb, hkv, bs, d]), T(B.PA_I64, [0]))]
+    ok = ctypes.byref(B.PAKVScales(0.5, 0.25))
+    assert lib.pa_reshape_and_cache_fp8(*empty, ok, None) == B.PA_OK

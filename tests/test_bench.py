@@ -27,6 +27,16 @@ def test_70b_step_bytes_match_the_hand_count():
     assert bench.launches_per_step(b) == 3  # scatter-write, decode partitions, merge
 
 
+def test_fp8_cache_halves_the_kv_bytes():
+    b16 = W.llama70b_decode(8, keep_contiguous=False, keep_pre=False)
+    b8 = W.to_fp8(b16)
+    n16, n8 = bench.algorithmic_bytes(b16), bench.algorithmic_bytes(b8)
+    assert n8["kv_logical"] * 2 == n16["kv_logical"] == 8 * 8192 * 8 * 128 * 2 * 2
+    assert n16["attention_logical"] - n8["attention_logical"] == n8["kv_logical"]
+    t = int(b8.k_new.shape[0])
+    assert n8["reshape_and_cache"] == t * 8 * 128 * 2 * 3 + t * 8
+
+
 def test_aliased_prefix_counts_unique_blocks_once():
     b = small_prefix()
     n = bench.algorithmic_bytes(b)
