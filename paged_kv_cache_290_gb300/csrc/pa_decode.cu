@@ -18,10 +18,14 @@
 //   * the 4 warps' (m, l, O) are combined in shared memory; a single-partition sequence writes
 //     fp16 output directly, otherwise the partition writes fp32 (m, l, O/l) partials that the
 //     merge kernel combines:  M = max m_p,  w_p = 2^(m_p - M) l_p,  out = sum w_p o_p / sum w_p.
-// FP8 (E4M3) cache: a unit is 16 rows of d bytes (one TMA box each for K and V, half the bytes);
-// the warp converts K, then V, into an fp16 staging buffer laid out like an fp16 stage (exact:
-// every E4M3 value is an fp16 value) and runs the same tensor-core path; k_scale is folded into
-// the score scale and v_scale multiplies the outputs.
+// FP8 (E4M3) cache: a unit is 16 rows of d bytes (one TMA box each for K and V, half the bytes).
+// The MMA fragments are built from the codes directly (ldmatrix on the byte rows, then an exact
+// E4M3 -> fp16 conversion in registers): a non-transposing ldmatrix gives a lane 4 consecutive
+// codes of one token, which fill the A fragment of S^T = K Q^T under a permutation of the head
+// dimension inside each 16-wide step (Q's B fragment uses the same one, so q.k is unchanged); a
+// transposing ldmatrix gives 2 tokens x 2 dims, which fill the A fragment of V^T under a
+// permutation of its rows (m-row i <-> dim 2i, m-row i + 8 <-> dim 2i + 1), undone when O is
+// written out.  k_scale is folded into the score scale and v_scale multiplies the outputs.
 // Both kernels are programmatic dependents of what precedes them on the stream: they may be
 // scheduled early but read nothing from global memory before griddepcontrol.wait.
 #include <algorithm>
@@ -41,49 +45,22 @@ struct DecodeCfg {
   static constexpr int kF16Bytes = kHalves * kBoxBytes; // fp16 K (or V) of one 16-token unit
   static constexpr int kKBytes = F8 ? 16 * D : kF16Bytes;  // K of one unit as stored in a stage
   static constexpr int kStageBytes = 2 * kKBytes;       // K + V
-  static constexpr int kStages = (F8 ? 48 * 1024 : 64 * 1024) / (kWarps * kStageBytes);
+  static constexpr int kStages = (64 * 1024) / (kWarps * kStageBytes);
   static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
-  static constexpr int kStagingBytes = F8 ? kF16Bytes : 0;  // per warp: one unit's K or V, fp16
   static constexpr int kUnitsPerPart = kPartitionTokens / 16;
   static constexpr int kDK = D / 16;
   static constexpr int kHeads = NT * 8;
   static constexpr int kMergeBytes = kWarps * kHeads * (D + 2) * 4;
-  static constexpr int kDataBytes = kRingBytes + kWarps * kStagingBytes;
-  static constexpr int kSmemBytes = (kDataBytes > kMergeBytes ? kDataBytes : kMergeBytes) + 1024;
+  static constexpr int kSmemBytes = (kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes) + 1024;
   static_assert(kStages >= 1, "stage ring");
   static_assert(BS % 16 == 0, "block size must be a multiple of the 16-token unit");
 };
 
-// One 16-token unit of E4M3 codes (16 rows x D bytes; 128-byte swizzled rows for D = 128, plain
-// 64-byte rows for D = 64, as the TMA box lands) -> fp16 in the layout of an fp16 stage:
-// [D / 64][16 rows][128 B], 16-byte chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4).
+// Shared-memory address of 16-byte chunk `chunk` of token row `tok` of an E4M3 unit as the TMA box
+// lands: 128-byte swizzled rows for D = 128, plain 64-byte rows for D = 64.
 template <int D>
-__device__ __forceinline__ void e4m3_unit_to_f16(uint32_t src, uint32_t dst, int lane) {
-  constexpr int kRowChunks = D / 16;                 // 16-byte code chunks per row
-  constexpr int kPerLane = 16 * kRowChunks / 32;
-#pragma unroll
-  for (int i = 0; i < kPerLane; ++i) {
-    const int q = lane + 32 * i;
-    const int r = q / kRowChunks, c8 = q % kRowChunks;
-    const uint32_t sa = D == 128 ? src + r * 128 + ((c8 ^ (r & 7)) << 4) : src + r * 64 + c8 * 16;
-    uint32_t w0, w1, w2, w3;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                 : "r"(sa)
-                 : "memory");
-    const int e = 2 * c8;                            // fp16 chunk of the code chunk's first half
-    const uint32_t half = dst + (e >> 3) * (16 * 128) + r * 128;
-    const uint32_t d0 = half + (((e & 7) ^ (r & 7)) << 4);
-    const uint32_t d1 = half + ((((e & 7) + 1) ^ (r & 7)) << 4);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d0),
-                 "r"(f16x2_from_e4m3x2(w0)), "r"(f16x2_from_e4m3x2(w0 >> 16)),
-                 "r"(f16x2_from_e4m3x2(w1)), "r"(f16x2_from_e4m3x2(w1 >> 16))
-                 : "memory");
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d1),
-                 "r"(f16x2_from_e4m3x2(w2)), "r"(f16x2_from_e4m3x2(w2 >> 16)),
-                 "r"(f16x2_from_e4m3x2(w3)), "r"(f16x2_from_e4m3x2(w3 >> 16))
-                 : "memory");
-  }
+__device__ __forceinline__ uint32_t f8_row_chunk(uint32_t base, int tok, int chunk) {
+  return D == 128 ? base + tok * 128 + ((chunk ^ (tok & 7)) << 4) : base + tok * 64 + chunk * 16;
 }
 
 __device__ __forceinline__ uint32_t ldg_u32(const __half* p) {
@@ -189,8 +166,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
                          static_cast<int64_t>(g * a.group + (hv ? hg : 0)) * D;
 #pragma unroll
     for (int j = 0; j < C::kDK; ++j) {
-      qf[nt][j][0] = hv ? ldg_u32(qrow + j * 16 + 2 * cq) : 0u;
-      qf[nt][j][1] = hv ? ldg_u32(qrow + j * 16 + 8 + 2 * cq) : 0u;
+      // FP8: k positions (2cq, 2cq+1 | 2cq+8, 2cq+9) hold dims (4cq, 4cq+1 | 4cq+2, 4cq+3)
+      qf[nt][j][0] = hv ? ldg_u32(qrow + j * 16 + (F8 ? 4 * cq : 2 * cq)) : 0u;
+      qf[nt][j][1] = hv ? ldg_u32(qrow + j * 16 + (F8 ? 4 * cq + 2 : 8 + 2 * cq)) : 0u;
     }
   }
 
@@ -215,28 +193,39 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
     }
     const int u = warp + i * C::kWarps;
     const int nvalid = min(16, tok_end - (tok_begin + u * 16));
-    const uint32_t stage = ring + st * C::kStageBytes;
-    // fp16 K (and later V) of the unit: the stage itself, or the warp's staging buffer.
-    const uint32_t staging = smem_addr(smem + C::kRingBytes + warp * C::kStagingBytes);
-    uint32_t kb = stage, vb = stage + C::kKBytes;
-    if constexpr (F8) {
-      e4m3_unit_to_f16<D>(stage, staging, lane);
-      __syncwarp();
-      kb = vb = staging;
-    }
+    const uint32_t kb = ring + st * C::kStageBytes;
+    const uint32_t vb = kb + C::kKBytes;
 
     // ---- S^T[16 tokens][8 heads] = K Q^T
     float sacc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    if constexpr (F8) {
+      // one ldmatrix.x4 = two 16-dim steps x two 8-token halves of E4M3 codes
 #pragma unroll
-    for (int j = 0; j < C::kDK; ++j) {
-      const int tok = mr + ((mi & 1) << 3);
-      const int chunk = 2 * j + (mi >> 1);
-      uint32_t af[4];
-      ldsm_x4(kb + (chunk >> 3) * C::kBoxBytes + swz128(tok, chunk & 7), af);
+      for (int jj = 0; jj < C::kDK / 2; ++jj) {
+        uint32_t r[4];
+        ldsm_x4(f8_row_chunk<D>(kb, mr + ((mi & 1) << 3), 2 * jj + (mi >> 1)), r);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[nt], af, qf[nt][j][0], qf[nt][j][1]);
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t af[4] = {f16x2_from_e4m3x2(r[2 * h]), f16x2_from_e4m3x2(r[2 * h + 1]),
+                                  f16x2_from_e4m3x2(r[2 * h] >> 16),
+                                  f16x2_from_e4m3x2(r[2 * h + 1] >> 16)};
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_f16_16816(sacc[nt], af, qf[nt][2 * jj + h][0], qf[nt][2 * jj + h][1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < C::kDK; ++j) {
+        const int tok = mr + ((mi & 1) << 3);
+        const int chunk = 2 * j + (mi >> 1);
+        uint32_t af[4];
+        ldsm_x4(kb + (chunk >> 3) * C::kBoxBytes + swz128(tok, chunk & 7), af);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[nt], af, qf[nt][j][0], qf[nt][j][1]);
+      }
     }
 
     // ---- online softmax over the unit (per head; this lane holds heads 2cq, 2cq+1)
@@ -274,30 +263,48 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
       pb1[nt] = movmatrix_trans(pack_half2(p10, p11));  // P^T[tok 2cq+8..][head gq]
     }
 
-    if constexpr (F8) {  // every lane's K fragments are loaded: V takes the staging buffer
-      __syncwarp();
-      e4m3_unit_to_f16<D>(stage + C::kKBytes, staging, lane);
-      __syncwarp();
-    }
-
     // ---- O^T[d][heads] += V^T[d][16 tokens] P^T
     uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
     if (nvalid < 16) {
       vm0 = (2 * cq < nvalid ? 0x0000ffffu : 0u) | (2 * cq + 1 < nvalid ? 0xffff0000u : 0u);
       vm1 = (2 * cq + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * cq + 9 < nvalid ? 0xffff0000u : 0u);
     }
+    if constexpr (F8) {
+      // one ldmatrix.x4.trans = two 16-dim blocks x two 8-token halves; a lane holds, per
+      // matrix, tokens (2cq, 2cq+1) x dims (2gq, 2gq+1) of the block: bytes 0, 2 are dim 2gq
+      // (m-row gq), bytes 1, 3 dim 2gq + 1 (m-row gq + 8)
 #pragma unroll
-    for (int dt = 0; dt < C::kDK; ++dt) {
-      const int tok = mr + ((mi >> 1) << 3);
-      const int chunk = 2 * dt + (mi & 1);
-      uint32_t af[4];
-      ldsm_x4_trans(vb + (chunk >> 3) * C::kBoxBytes + swz128(tok, chunk & 7), af);
-      af[0] &= vm0;
-      af[1] &= vm0;
-      af[2] &= vm1;
-      af[3] &= vm1;
+      for (int dd = 0; dd < C::kDK / 2; ++dd) {
+        uint32_t r[4];
+        ldsm_x4_trans(f8_row_chunk<D>(vb, mr + ((mi & 1) << 3), 2 * dd + (mi >> 1)), r);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][dt], af, pb0[nt], pb1[nt]);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t af[4] = {f16x2_from_e4m3x2(__byte_perm(r[2 * h], 0, 0x3320)),
+                            f16x2_from_e4m3x2(__byte_perm(r[2 * h], 0, 0x3331)),
+                            f16x2_from_e4m3x2(__byte_perm(r[2 * h + 1], 0, 0x3320)),
+                            f16x2_from_e4m3x2(__byte_perm(r[2 * h + 1], 0, 0x3331))};
+          af[0] &= vm0;
+          af[1] &= vm0;
+          af[2] &= vm1;
+          af[3] &= vm1;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][2 * dd + h], af, pb0[nt], pb1[nt]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int dt = 0; dt < C::kDK; ++dt) {
+        const int tok = mr + ((mi >> 1) << 3);
+        const int chunk = 2 * dt + (mi & 1);
+        uint32_t af[4];
+        ldsm_x4_trans(vb + (chunk >> 3) * C::kBoxBytes + swz128(tok, chunk & 7), af);
+        af[0] &= vm0;
+        af[1] &= vm0;
+        af[2] &= vm1;
+        af[3] &= vm1;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][dt], af, pb0[nt], pb1[nt]);
+      }
     }
 
     __syncwarp();
@@ -345,8 +352,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
       float* dst = sm_o + (warp * H + h) * D;
 #pragma unroll
       for (int dt = 0; dt < C::kDK; ++dt) {
-        dst[dt * 16 + gq] = o[nt][dt][e];
-        dst[dt * 16 + gq + 8] = o[nt][dt][2 + e];
+        // m-rows gq, gq + 8 of O^T: dims gq, gq + 8 (fp16) or 2gq, 2gq + 1 (FP8 permutation)
+        dst[dt * 16 + (F8 ? 2 * gq : gq)] = o[nt][dt][e];
+        dst[dt * 16 + (F8 ? 2 * gq + 1 : gq + 8)] = o[nt][dt][2 + e];
       }
     }
   }
