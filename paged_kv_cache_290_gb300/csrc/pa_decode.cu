@@ -45,7 +45,8 @@ struct DecodeCfg {
   static constexpr int kF16Bytes = kHalves * kBoxBytes; // fp16 K (or V) of one 16-token unit
   static constexpr int kKBytes = F8 ? 16 * D : kF16Bytes;  // K of one unit as stored in a stage
   static constexpr int kStageBytes = 2 * kKBytes;       // K + V
-  static constexpr int kStages = (64 * 1024) / (kWarps * kStageBytes);
+  // FP8: 3 stages of 4 KB per warp keep the bytes in flight per SM and fit 4 CTAs per SM.
+  static constexpr int kStages = (F8 ? 48 * 1024 : 64 * 1024) / (kWarps * kStageBytes);
   static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
   static constexpr int kUnitsPerPart = kPartitionTokens / 16;
   static constexpr int kDK = D / 16;
