@@ -41,10 +41,20 @@ FLUSH_BYTES = 512 << 20
 
 # ------------------------------------------------------------------------------ bookkeeping
 
-def algorithmic_bytes(b) -> dict:
+def shared_prefix_tokens(b) -> int:
+    """Keys of the prefix every sequence shares, rounded down to whole 512-key partitions, when
+    the batch qualifies for the shared-prefix pass (fp16 cache, decode rows only); else 0."""
+    sp = (int(b.meta.get("shared_prefix_len", 0)) // 512) * 512
+    ok = b.kv_dtype != "e4m3" and b.max_query_len == 1 and sp < b.max_seq_len
+    return sp if ok else 0
+
+
+def algorithmic_bytes(b, sp: int = 0) -> dict:
     """Bytes the step must move at minimum.  K/V are counted per attended token of every
     sequence ("logical"); "unique" counts each physical (block, offset) slot once, which is what
-    the roofline of an aliased-prefix batch is measured against."""
+    the roofline of an aliased-prefix batch is measured against.  With a shared-prefix pass over
+    the first ``sp`` keys, the decode kernel's share is the keys past them and the pass's share
+    the prefix's K/V once plus every row's query."""
     hkv, d, bs = b.num_kv_heads, b.head_dim, b.block_size
     eb = 1 if b.kv_dtype == "e4m3" else 2  # bytes per cached value (E4M3 or fp16)
     row_kv = hkv * d * eb * 2  # K and V of one token, all kv heads
@@ -72,12 +82,13 @@ def algorithmic_bytes(b) -> dict:
                                                  s.query_len * (s.query_len - 1) // 2)
                        for s, keep in zip(b.seqs, sel) if keep))
 
-    def kernel_bytes(sel):
-        """Unique K/V slots of the selected sequences, their Q/out rows and table entries."""
+    def kernel_bytes(sel, first=0):
+        """Unique K/V slots (positions >= first) of the selected sequences, their Q/out rows and
+        table entries."""
         idx = np.nonzero(sel)[0]
         if idx.size == 0:
             return 0
-        uniq = np.unique(np.concatenate([slots[int(np.nonzero(np.nonzero(active)[0] == s)[0][0])]
+        uniq = np.unique(np.concatenate([slots[int(np.nonzero(np.nonzero(active)[0] == s)[0][0])][first:]
                                          for s in idx])).size * row_kv
         rows = int(qlens[idx].sum())
         return (uniq + 2 * rows * b.num_q_heads * d * 2 +
@@ -93,9 +104,15 @@ def algorithmic_bytes(b) -> dict:
         "flops": flops(active),
         # what each attention kernel must move / compute: the decode-partition kernel serves the
         # one-row sequences, the chunked-prefill kernel the sequences with several rows
-        "decode_kernel_bytes": kernel_bytes(dec),
+        "decode_kernel_bytes": kernel_bytes(dec, sp),
         "prefill_kernel_bytes": kernel_bytes(pre),
         "prefill_kernel_flops": flops(pre),
+        "prefill_kernel": ("prefill_parity_kernel" if b.max_query_len <= 128 // (b.num_q_heads //
+                                                                               hkv)
+                           else "prefill_pair_kernel"),
+        "shared_prefix_tokens": sp,
+        "shared_prefix_kernel_bytes": sp * row_kv + q_bytes if sp else 0,
+        "shared_prefix_kernel_flops": 4 * b.num_q_heads * d * sp * t if sp else 0,
     }
 
 
@@ -104,13 +121,14 @@ def all_prefill(b) -> bool:
     return b.max_query_len > 1 and b.num_prefill_seqs == b.num_seqs
 
 
-def launches_per_step(b) -> int:
+def launches_per_step(b, sp: int = 0) -> int:
     parts = max(1, math.ceil(b.max_seq_len / 512))
     decode = not all_prefill(b)
     n = 1 if b.k_new.shape[0] > 0 else 0        # reshape_and_cache
     n += 1 if decode else 0                       # decode partitions
     n += 1 if b.max_query_len > 1 else 0          # chunked-prefill tiles
     n += 1 if parts > 1 and decode else 0         # log-sum-exp merge
+    n += 1 if sp else 0                           # shared-prefix pass
     return n
 
 
@@ -237,7 +255,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
 
     b = W.WORKLOADS[args.workload](keep_contiguous=False, keep_pre=False)
-    nbytes = algorithmic_bytes(b)
+    sp = 0 if args.no_shared_prefix else shared_prefix_tokens(b)
+    nbytes = algorithmic_bytes(b, sp)
     stream = torch.cuda.current_stream()
 
     # device-resident inputs (the pool already holds every token; the scatter rewrites the new
@@ -256,7 +275,8 @@ def run_ours(args, world, rank, local):
     def step(q_, k_, v_, s_, bt_, sl_, qsl_, out_):
         pa.reshape_and_cache(k_, v_, kc, vc, s_, **sc)
         pa.attention(q_, kc, vc, bt_, sl_, qsl_, b.scale, out_, b.max_query_len, b.max_seq_len,
-                     workspace=ws, num_prefill_seqs=b.num_prefill_seqs, **sc)
+                     workspace=ws, num_prefill_seqs=b.num_prefill_seqs,
+                     shared_prefix_tokens=sp, **sc)
 
     for i in range(args.warmup):
         flush.fill_(i & 255)
@@ -267,7 +287,8 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device error after warm-up: status {st} bits {bits}")
 
     # -------- device-resident timed region
-    timed = ([] if all_prefill(b) else ["decode"]) + (["prefill"] if b.max_query_len > 1 else [])
+    timed = (([] if all_prefill(b) else ["decode"]) + (["prefill"] if b.max_query_len > 1 else [])
+             + (["shared_prefix"] if sp else []))
     mk = lambda: torch.cuda.Event(enable_timing=True)
     ev = [(mk(), mk(), {k: (mk(), mk()) for k in timed}) for _ in range(args.steps)]
     for _, _, kev in ev:      # torch creates an event on its first record(); the library then
@@ -356,6 +377,7 @@ def run_ours(args, world, rank, local):
                    "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
                    "block_size": b.block_size, "num_blocks": b.num_blocks,
                    "kv_cache_dtype": b.kv_dtype, "partition_tokens": 512,
+                   "shared_prefix_tokens": sp,
                    "parallelism": f"replicas x{world}",
                    "l2": "flushed before every timed step (512 MiB write, outside the events)"},
         "decode_tok_s_per_layer": tok_s,
@@ -363,7 +385,7 @@ def run_ours(args, world, rank, local):
         "bytes": nbytes,
         "roofline": kernels[dominant],
         "roofline_kernels": kernels,
-        "gpu_launches": launches_per_step(b) * args.steps,
+        "gpu_launches": launches_per_step(b, sp) * args.steps,
         "wall_ms_per_step": wall * 1e3 / args.steps,
         "clocks": clk,
         "impl": "ours",
@@ -381,8 +403,11 @@ def kernel_rooflines(nbytes, kern_ms, peaks) -> dict:
     (HBM copy bandwidth vs fp16 dense tensor throughput, both measured)."""
     out = {}
     specs = {"decode": ("decode_partition_kernel", nbytes["decode_kernel_bytes"], 0),
-             "prefill": ("prefill_umma_kernel", nbytes["prefill_kernel_bytes"],
-                         nbytes["prefill_kernel_flops"])}
+             "prefill": (nbytes.get("prefill_kernel", "prefill"), nbytes["prefill_kernel_bytes"],
+                         nbytes["prefill_kernel_flops"]),
+             "shared_prefix": ("prefill_pair_kernel (shared-prefix pass)",
+                               nbytes.get("shared_prefix_kernel_bytes", 0),
+                               nbytes.get("shared_prefix_kernel_flops", 0))}
     for k, ms in kern_ms.items():
         name, nb, fl = specs[k]
         t = ms * 1e-3
@@ -521,6 +546,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-shared-prefix", action="store_true",
+                    help="attend an aliased prefix per sequence instead of once for all rows")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:

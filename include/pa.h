@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define PA_VERSION 2
+#define PA_VERSION 3
 #define PA_PARTITION_TOKENS 512 /* keys per split-context partition */
 #define PA_MAX_DIMS 5
 
@@ -82,6 +82,15 @@ typedef struct pa_batch_hint {
                                PA_ERR_DESCRIPTOR.  When it equals the number of sequences (and
                                max_query_len > 1) the decode launches are skipped; a one-row
                                sequence in such a batch is then reported the same way. */
+  int32_t shared_prefix_tokens; /* 0, or a multiple of 512 (and of the block size) smaller than
+                               every sequence's seq_len: the first shared_prefix_tokens keys of
+                               every sequence are the same physical blocks (the block tables
+                               agree there), so they are attended once for all query rows (p1:
+                               requests that start alike share pages; p2 prefix-caching slide)
+                               and merged with each sequence's own keys by the log-sum-exp rule.
+                               Decode rows and fp16 caches only (else PA_ERR_UNSUPPORTED); a
+                               sequence whose table differs there, or with no key past the
+                               prefix, is reported as PA_ERR_DESCRIPTOR. */
 } pa_batch_hint;
 
 /*
@@ -237,12 +246,14 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_
  * every later pa_attention call on this host thread records `start` on its stream just before
  * launching the selected kernel and `stop` just after it, so a caller can time that kernel with
  * CUDA events inside a longer step: `kernel` is PA_TIMED_DECODE (the decode-partition kernel,
- * launched by every call with rows) or PA_TIMED_PREFILL (the chunked-prefill kernel, launched
- * when hint->max_query_len > 1).  No work is skipped or reordered.  Pass NULL, NULL to turn
+ * launched by every call with rows), PA_TIMED_PREFILL (the chunked-prefill kernel, launched
+ * when hint->max_query_len > 1) or PA_TIMED_SHARED_PREFIX (the shared-prefix pass, launched
+ * when hint->shared_prefix_tokens > 0).  No work is skipped or reordered.  Pass NULL, NULL to turn
  * the selected hook off.  Returns PA_OK, or PA_ERR_INVALID_ARG for an unknown `kernel`.
  */
 #define PA_TIMED_DECODE 0
 #define PA_TIMED_PREFILL 1
+#define PA_TIMED_SHARED_PREFIX 2
 int pa_set_timing_events(int kernel, void* start, void* stop);
 
 /* PA_VERSION of the built library. */

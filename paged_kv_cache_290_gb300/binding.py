@@ -51,7 +51,7 @@ class PATensor(ctypes.Structure):
 
 class PABatchHint(ctypes.Structure):
     _fields_ = [("max_query_len", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
-                ("num_prefill_seqs", ctypes.c_int32)]
+                ("num_prefill_seqs", ctypes.c_int32), ("shared_prefix_tokens", ctypes.c_int32)]
 
 
 class PAKVScales(ctypes.Structure):
@@ -184,20 +184,24 @@ def workspace_size(num_tokens: int, num_q_heads: int, head_dim: int, max_seq_len
 
 def attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale: float, out,
               max_query_len: int, max_seq_len: int, workspace: Optional[torch.Tensor] = None,
-              stream=None, num_prefill_seqs: int = 0, k_scale=None, v_scale=None) -> torch.Tensor:
+              stream=None, num_prefill_seqs: int = 0, k_scale=None, v_scale=None,
+              shared_prefix_tokens: int = 0) -> torch.Tensor:
     """``pa_attention`` for one mixed batch; writes ``out`` [T, Hq, d] and returns it.  A byte
     pool is an FP8 (E4M3) cache: ``pa_attention_fp8`` with the two scales (decode rows only).
 
     ``workspace`` is a caller-owned uint8 device tensor of at least ``workspace_size(...)``
     bytes (allocated here when omitted).  ``num_prefill_seqs`` is the count of sequences with
-    more than one query row (0 = not known)."""
+    more than one query row (0 = not known).  ``shared_prefix_tokens`` (a multiple of 512 and
+    of the block size, decode rows only) says that every sequence's first keys are the same
+    blocks: they are attended once for all rows and merged with each sequence's own keys."""
     lib = load_library()
     need = workspace_size(q.shape[0], q.shape[1], q.shape[2], max_seq_len)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wptr = workspace.data_ptr() if workspace is not None and workspace.numel() else None
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    hint = PABatchHint(int(max_query_len), int(max_seq_len), int(num_prefill_seqs))
+    hint = PABatchHint(int(max_query_len), int(max_seq_len), int(num_prefill_seqs),
+                       int(shared_prefix_tokens))
     descs = [describe(x) for x in (q, k_cache, v_cache, block_tables, seq_lens, query_start_loc)]
     if _is_fp8(k_cache):
         sc = PAKVScales(float(k_scale), float(v_scale))
@@ -211,7 +215,7 @@ def attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scal
     return out
 
 
-TIMED_KERNELS = {"decode": 0, "prefill": 1}
+TIMED_KERNELS = {"decode": 0, "prefill": 1, "shared_prefix": 2}
 
 
 def copy_blocks(k_cache, v_cache, pairs, stream=None):
@@ -225,7 +229,8 @@ def copy_blocks(k_cache, v_cache, pairs, stream=None):
 def set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event],
                       kernel: str = "decode"):
     """Record ``start``/``stop`` around every later launch of ``kernel`` ("decode": the
-    decode-partition kernel, "prefill": the chunked-prefill kernel) on this thread
+    decode-partition kernel, "prefill": the chunked-prefill kernel, "shared_prefix": the
+    shared-prefix pass) on this thread
     (``None, None`` turns that hook off).  Measurement only; no work changes."""
     lib = load_library()
     if start is None or stop is None:

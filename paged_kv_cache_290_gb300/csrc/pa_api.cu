@@ -17,8 +17,8 @@
 namespace {
 
 thread_local std::string g_last_error;
-thread_local cudaEvent_t g_time_start[2] = {nullptr, nullptr};  // [PA_TIMED_DECODE / _PREFILL]
-thread_local cudaEvent_t g_time_stop[2] = {nullptr, nullptr};
+thread_local cudaEvent_t g_time_start[3] = {};  // indexed by PA_TIMED_*
+thread_local cudaEvent_t g_time_stop[3] = {};
 
 int fail(int code, const std::string& msg) {
   g_last_error = msg;
@@ -35,6 +35,7 @@ __device__ unsigned g_device_error_word;
 constexpr int kMaxDevices = 256;
 std::mutex g_err_mu;
 unsigned* g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
 
 // Address of the error word on the current device (looked up once per device).
 cudaError_t device_error_word(unsigned** out) {
@@ -50,6 +51,21 @@ cudaError_t device_error_word(unsigned** out) {
     g_err_ptr[dev] = static_cast<unsigned*>(p);
   }
   *out = g_err_ptr[dev];
+  return cudaSuccess;
+}
+
+// SM count of the current device (looked up once per device).
+cudaError_t device_sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_sm_count[dev]) {
+    e = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  *out = g_sm_count[dev];
   return cudaSuccess;
 }
 
@@ -325,8 +341,22 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
     return fail(PA_ERR_INVALID_ARG, "block_tables needs at least one column");
   if (block_tables->shape[1] > INT32_MAX || block_tables->stride[0] < block_tables->shape[1])
     return fail(PA_ERR_INVALID_ARG, "block_tables row stride must cover its columns");
-  if (hint->max_query_len < 0 || hint->max_seq_len < 0 || hint->num_prefill_seqs < 0)
+  if (hint->max_query_len < 0 || hint->max_seq_len < 0 || hint->num_prefill_seqs < 0 ||
+      hint->shared_prefix_tokens < 0)
     return fail(PA_ERR_INVALID_ARG, "hint values must be non-negative");
+  const int64_t bs = k_cache->shape[2];
+  const int sp = hint->shared_prefix_tokens;
+  if (sp > 0) {
+    if (sp % PA_PARTITION_TOKENS != 0 || sp % bs != 0)
+      return fail(PA_ERR_INVALID_ARG, "shared_prefix_tokens must be a multiple of 512 and of the "
+                                      "block size");
+    if (sp >= hint->max_seq_len || sp / bs > block_tables->shape[1])
+      return fail(PA_ERR_INVALID_ARG, "shared_prefix_tokens must be below max_seq_len and within "
+                                      "the block tables");
+    if (fp8 || hint->max_query_len > 1)
+      return fail(PA_ERR_UNSUPPORTED, "the shared-prefix pass is built for decode rows over an "
+                                      "fp16 cache");
+  }
   if (hint->max_query_len > hint->max_seq_len)
     return fail(PA_ERR_INVALID_ARG, "hint max_query_len exceeds max_seq_len");
   if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN");
@@ -373,8 +403,11 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
   a.scale_log2 = scale * 1.4426950408889634f * (fp8 ? sc->k_scale : 1.f);
   a.v_scale = fp8 ? sc->v_scale : 1.f;
   a.kv_fp8 = fp8 ? 1 : 0;
+  a.cascade_parts = sp / PA_PARTITION_TOKENS;
   cudaError_t e = device_error_word(&a.err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
+  if (a.cascade_parts > 0 && (e = device_sm_count(&a.num_sms)) != cudaSuccess)
+    return cuda_fail(e, "device attribute");
 
   const int64_t rows = k_cache->shape[0] * hkv * k_cache->shape[2];
   CUtensorMap kmap, vmap;
@@ -391,6 +424,12 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
     e = pa::launch_decode(a, kmap, vmap, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     if ((e = mark(PA_TIMED_DECODE, true)) != cudaSuccess) return cuda_fail(e, "timing event");
+  }
+  if (a.cascade_parts > 0) {
+    if ((e = mark(PA_TIMED_SHARED_PREFIX, false)) != cudaSuccess) return cuda_fail(e, "timing event");
+    e = pa::launch_shared_prefix(a, kmap, vmap, st);
+    if (e != cudaSuccess) return cuda_fail(e, "shared-prefix launch");
+    if ((e = mark(PA_TIMED_SHARED_PREFIX, true)) != cudaSuccess) return cuda_fail(e, "timing event");
   }
   if (a.max_parts > 1 && !all_prefill) {
     e = pa::launch_merge(a, st);
@@ -425,8 +464,9 @@ int pa_attention_fp8(const pa_tensor* q, const pa_tensor* k_cache, const pa_tens
 
 int pa_set_timing_events(int kernel, void* start, void* stop) {
   g_last_error.clear();
-  if (kernel != PA_TIMED_DECODE && kernel != PA_TIMED_PREFILL)
-    return fail(PA_ERR_INVALID_ARG, "timed kernel must be PA_TIMED_DECODE or PA_TIMED_PREFILL");
+  if (kernel != PA_TIMED_DECODE && kernel != PA_TIMED_PREFILL && kernel != PA_TIMED_SHARED_PREFIX)
+    return fail(PA_ERR_INVALID_ARG,
+                "timed kernel must be PA_TIMED_DECODE, PA_TIMED_PREFILL or PA_TIMED_SHARED_PREFIX");
   const bool on = start && stop;
   g_time_start[kernel] = on ? static_cast<cudaEvent_t>(start) : nullptr;
   g_time_stop[kernel] = on ? static_cast<cudaEvent_t>(stop) : nullptr;

@@ -79,7 +79,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int part = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  // Partitions inside a shared prefix belong to the shared-prefix pass and get no CTA here.
+  const int part = blockIdx.x + a.cascade_parts, g = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   grid_dependency_wait();  // everything the previous kernels wrote is visible from here on
   grid_launch_dependents();
@@ -88,18 +89,27 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
   const int q_len = a.query_start_loc[s + 1] - row0;
   if (q_len != 1) return;  // prefill chunks and idle sequences are not decode work
   if (row0 < 0 || row0 + q_len > a.num_tokens) {
-    if (part == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
+    if (blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
     return;
   }
   const int L = a.seq_lens[s];
   const int nparts = (L + kPartitionTokens - 1) / kPartitionTokens;
   if (L < 1 || (L + BS - 1) / BS > a.max_blocks) {
-    if (part == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
+    if (blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
     return;
   }
-  if (nparts > static_cast<int>(gridDim.x)) {
-    if (part == 0 && tid == 0) atomicOr(a.err, kErrHint);
+  if (nparts > static_cast<int>(gridDim.x) + a.cascade_parts) {
+    if (blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrHint);
     return;
+  }
+  if (a.cascade_parts > 0 && blockIdx.x == 0 && g == 0) {
+    // With a shared prefix, the row must have keys past it, and its table must hold sequence
+    // 0's blocks inside it (the blocks the shared-prefix pass reads for every row).
+    int differs = L <= a.cascade_parts * kPartitionTokens;
+    const int nb = a.cascade_parts * (kPartitionTokens / BS);
+    for (int j = tid; j < nb; j += C::kThreads)
+      differs |= a.block_tables[static_cast<int64_t>(s) * a.bt_stride + j] != a.block_tables[j];
+    if (__syncthreads_or(differs) && tid == 0) atomicOr(a.err, kErrDescriptor);
   }
   if (part >= nparts) return;
 
@@ -468,7 +478,7 @@ cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CU
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.max_parts, a.num_kv_heads, a.num_seqs);
+  dim3 grid(a.max_parts - a.cascade_parts, a.num_kv_heads, a.num_seqs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(C::kThreads);

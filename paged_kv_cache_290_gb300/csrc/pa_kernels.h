@@ -56,6 +56,8 @@ struct AttnArgs {
   float scale_log2;  // scale * log2(e) (times k_scale for an FP8 cache)
   float v_scale;     // FP8 cache: multiplies the output; 1 for fp16
   int kv_fp8;        // 1: the pools hold E4M3 codes
+  int cascade_parts; // leading 512-key partitions every sequence shares (attended once for all)
+  int num_sms;       // SMs of the device (launch-shape choices)
   unsigned* err;
 };
 
@@ -80,5 +82,7 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            cudaStream_t stream);
+cudaError_t launch_shared_prefix(const AttnArgs& a, const CUtensorMap& kmap,
+                                 const CUtensorMap& vmap, cudaStream_t stream);
 
 }  // namespace pa

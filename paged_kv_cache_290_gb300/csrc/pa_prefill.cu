@@ -81,13 +81,13 @@ __device__ __forceinline__ int find_prefill_seq(const AttnArgs& a, int* warp_cou
 }
 
 // A producer warp: streams the K (or V) tiles 0 .. ntiles-1 of sequence s, kv head g, keys
-// [0, kend), into a ring of `stages` stages of kKVBytes each.  Each 16-token unit is found
+// [key_base, kend), into a ring of `stages` stages of kKVBytes each.  Each 16-token unit is found
 // through the block table and fetched as 128-byte-swizzled TMA boxes (one per 64 columns).
 // Before returning it waits (bounded) for its last copies, so none lands after the CTA retires.
 template <int D, int BS, int kKeys>
 __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap* map, int s, int g,
                                            int kend, int ntiles, int stages, uint64_t* full,
-                                           uint64_t* empty, uint32_t ring) {
+                                           uint64_t* empty, uint32_t ring, int key_base = 0) {
   constexpr int kUnits = kKeys / 16, kHalves = D / 64, kKVBytes = kHalves * kKeys * 128;
   const int lane = threadIdx.x & 31;
   int issued = 0;
@@ -96,7 +96,7 @@ __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap*
     bool ok = true;
     if (lane == 0 && round > 0) ok = mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err);
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-    const int key0 = j * kKeys;
+    const int key0 = key_base + j * kKeys;
     const int units = min(kUnits, (kend - key0 + 15) >> 4);
     const int id = lane < units
                        ? a.block_tables[static_cast<int64_t>(s) * a.bt_stride + (key0 + 16 * lane) / BS]
@@ -148,7 +148,11 @@ struct PairCfg {
   static constexpr float kRescaleLog2 = 8.f;              // raise the max only past 2^8
 };
 
-template <int D, int BS>
+// CASCADE: the shared-prefix pass.  Rows are every query row of the batch (all decode rows,
+// row i of q), keys are the 512-key partition blockIdx.z of the prefix that every sequence
+// shares (read through sequence 0's table), no causal mask; the epilogue writes the rows'
+// partition partials (m, l, O / l) for the log-sum-exp merge instead of the output.
+template <int D, int BS, bool CASCADE>
 __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
@@ -169,51 +173,71 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   const uint32_t q_s = smem_addr(smem);                     // Q tiles A, B
   const uint32_t k_s = q_s + C::kQTiles * C::kQBytes;       // K ring
   const uint32_t v_s = k_s + C::kKStages * C::kKVBytes;     // V ring
-  // Later q tiles of a chunk see more keys: dispatch them first so the grid's tail is short.
-  const int qt = gridDim.x - 1 - blockIdx.x, g = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  const int s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq);
-  if (s < 0) return;
-
-  const int row0 = a.query_start_loc[s];
-  const int q_len = a.query_start_loc[s + 1] - row0;
-  if (q_len <= 1) return;  // decode rows and idle sequences are handled elsewhere
-  const int L = a.seq_lens[s];
+  const int g = blockIdx.y;
   const int tile_q = C::kRows / a.group;  // query tokens per Q tile
-  const int qbase = qt * C::kQTiles * tile_q;
-  if (q_len > L || (L + BS - 1) / BS > a.max_blocks || row0 < 0 ||
-      row0 + q_len > a.num_tokens) {
-    if (qt == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
-    return;
-  }
-  if ((q_len + C::kQTiles * tile_q - 1) / (C::kQTiles * tile_q) > static_cast<int>(gridDim.x)) {
-    if (qt == 0 && tid == 0) atomicOr(a.err, kErrHint);
-    return;
-  }
-  if (qbase >= q_len) return;
-  const int ctx = L - q_len;
-  // Key tiles of each Q tile: keys [0, ctx + last row + 1); Q tile B may hold no row at all.
+  int s, qt, row0, q_len, ctx, key_base = 0;
   int tiles[C::kQTiles];
+  int kend, ntiles;  // keys loaded: [key_base, kend), in ntiles 128-key tiles
+  if constexpr (CASCADE) {
+    s = 0;
+    qt = blockIdx.x;
+    row0 = 0;
+    q_len = static_cast<int>(a.num_tokens);
+    key_base = blockIdx.z * kPartitionTokens;
+    ctx = 0;  // unused: no causal mask inside the shared prefix
+    kend = key_base + kPartitionTokens;
+    ntiles = kPartitionTokens / C::kKeys;
+    if (qt * C::kQTiles * tile_q >= q_len) {
+      grid_dependency_wait();
+      return;
+    }
 #pragma unroll
-  for (int t = 0; t < C::kQTiles; ++t) {
-    const int first = qbase + t * tile_q;
-    tiles[t] = first < q_len
-                   ? (ctx + min(q_len, first + tile_q) + C::kKeys - 1) / C::kKeys
-                   : 0;
+    for (int t = 0; t < C::kQTiles; ++t)
+      tiles[t] = qt * C::kQTiles * tile_q + t * tile_q < q_len ? ntiles : 0;
+  } else {
+    // Later q tiles of a chunk see more keys: dispatch them first so the grid's tail is short.
+    qt = gridDim.x - 1 - blockIdx.x;
+    s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq);
+    if (s < 0) return;
+    row0 = a.query_start_loc[s];
+    q_len = a.query_start_loc[s + 1] - row0;
+    if (q_len <= 1) return;  // decode rows and idle sequences are handled elsewhere
+    const int L = a.seq_lens[s];
+    if (q_len > L || (L + BS - 1) / BS > a.max_blocks || row0 < 0 ||
+        row0 + q_len > a.num_tokens) {
+      if (qt == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
+      return;
+    }
+    if ((q_len + C::kQTiles * tile_q - 1) / (C::kQTiles * tile_q) > static_cast<int>(gridDim.x)) {
+      if (qt == 0 && tid == 0) atomicOr(a.err, kErrHint);
+      return;
+    }
+    if (qt * C::kQTiles * tile_q >= q_len) return;
+    ctx = L - q_len;
+    // Key tiles of each Q tile: keys [0, ctx + last row + 1); Q tile B may hold no row at all.
+#pragma unroll
+    for (int t = 0; t < C::kQTiles; ++t) {
+      const int first = qt * C::kQTiles * tile_q + t * tile_q;
+      tiles[t] = first < q_len
+                     ? (ctx + min(q_len, first + tile_q) + C::kKeys - 1) / C::kKeys
+                     : 0;
+    }
+    kend = ctx + min(q_len, qt * C::kQTiles * tile_q + C::kQTiles * tile_q);
+    ntiles = (kend + C::kKeys - 1) / C::kKeys;  // == max over Q tiles
   }
-  const int kend = ctx + min(q_len, qbase + C::kQTiles * tile_q);  // keys loaded: [0, kend)
-  const int ntiles = (kend + C::kKeys - 1) / C::kKeys;             // == max over Q tiles
+  const int qbase = qt * C::kQTiles * tile_q;
 
   // Every block id the CTA will read is checked before any copy is issued.
   int bad = 0;
   const int nblk = (kend + BS - 1) / BS;
-  for (int j = tid; j < nblk; j += C::kThreads) {
+  for (int j = key_base / BS + tid; j < nblk; j += C::kThreads) {
     const int32_t blk = a.block_tables[static_cast<int64_t>(s) * a.bt_stride + j];
     if (blk < 0 || blk >= a.num_blocks) bad = 1;
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0) atomicOr(a.err, kErrBlockRange);
+    if constexpr (CASCADE) grid_dependency_wait();
     return;
   }
 
@@ -258,7 +282,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     const bool is_v = warp == kVWarp;
     produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
                                 is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
-                                is_v ? v_empty : k_empty, is_v ? v_s : k_s);
+                                is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base);
   } else if (warp == kMmaWarp && lane == 0) {
     // ============================================================== MMA issuer (one thread)
     constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0);
@@ -334,7 +358,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     const uint32_t obuf = tmem + lane_addr + C::kOCol + t * D;
     const int my_tiles = tiles[t];
     // The V rows past kend are zeroed by the Q tile whose P V of the last key tile comes first.
-    const bool zeroes_v = t == 0 ? tiles[0] == ntiles : tiles[0] < ntiles;
+    const bool zeroes_v = !CASCADE && (t == 0 ? tiles[0] == ntiles : tiles[0] < ntiles);
 
     // The Q row -> shared memory, 128B-swizzled K-major.
     {
@@ -376,7 +400,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       // Scores stay raw where scale > 0 (the max commutes with the scale, which is folded into
       // the exponent's FMA below); otherwise they are scaled here.  Masked keys become -inf.
       const int key0 = j * C::kKeys;
-      const bool masked = key0 + C::kKeys - 1 > min_pos;
+      const bool masked = !CASCADE && key0 + C::kKeys - 1 > min_pos;
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (prescale || masked) {
 #pragma unroll
@@ -457,10 +481,34 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       mbar_arrive(smem_addr(&p_full[t]));
     }
 
-    // Epilogue: O_t / l -> out (fp16, rows of real query tokens only).
+    // Epilogue: O_t / l -> out (fp16, rows of real query tokens only); the shared-prefix pass
+    // writes the rows' partials of partition blockIdx.z instead: m (log2 units), l and O / l.
     bool ok = !stopped && my_tiles > 0;
     if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err);
-    if (!__any_sync(0xffffffffu, !ok)) {
+    if (CASCADE && !__any_sync(0xffffffffu, !ok)) {
+      tmem_fence_after_sync();
+      const float inv = 1.f / l_run;
+      const int64_t pidx = (static_cast<int64_t>(row0 + tok) * a.num_q_heads + g * a.group + hg) *
+                               a.max_parts + blockIdx.z;
+      if (rv) {
+        a.part_m[pidx] = m_run;
+        a.part_l[pidx] = l_run;
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t tt[32];
+        tmem_ld32(obuf + c0, tt);
+        tmem_wait_ld();
+        tmem_regs_ready(tt);
+        if (rv) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4*>(a.part_o + pidx * D + c0 + c) =
+                make_float4(__uint_as_float(tt[c]) * inv, __uint_as_float(tt[c + 1]) * inv,
+                            __uint_as_float(tt[c + 2]) * inv, __uint_as_float(tt[c + 3]) * inv);
+        }
+      }
+    } else if (!CASCADE && !__any_sync(0xffffffffu, !ok)) {
       tmem_fence_after_sync();
       const float inv = 1.f / l_run;
       __half* dst = a.out + (static_cast<int64_t>(row0 + tok) * a.num_q_heads + g * a.group + hg) * D;
@@ -492,6 +540,10 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(C::kTmemCols)
                  : "memory");
+  // The shared-prefix pass may start while the decode kernel before it is still running (it
+  // reads nothing that kernel writes); it must not finish first, since the merge after it waits
+  // only on this grid and reads the decode kernel's partials too.
+  if constexpr (CASCADE) grid_dependency_wait();
 }
 
 template <int D>
@@ -519,7 +571,9 @@ struct ParityCfg {
   static constexpr float kRescaleLog2 = 8.f;              // raise the max only past 2^8
 };
 
-template <int D, int BS>
+// CASCADE: the shared-prefix pass, as in the pair kernel (rows: every query row of the batch;
+// keys: prefix partition blockIdx.z through sequence 0's table; partials out).
+template <int D, int BS, bool CASCADE>
 __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     prefill_parity_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
@@ -541,43 +595,58 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
   const uint32_t q_s = smem_addr(smem);
   const uint32_t k_s = q_s + C::kQBytes;                  // K ring
   const uint32_t v_s = k_s + C::kKStages * C::kKVBytes;   // V ring
-  // Later q tiles of a chunk see more keys: dispatch them first so the grid's tail is short.
-  const int qt = gridDim.x - 1 - blockIdx.x, g = blockIdx.y;
+  const int g = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  const int s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq);
-  if (s < 0) return;
-
-  const int row0 = a.query_start_loc[s];
-  const int q_len = a.query_start_loc[s + 1] - row0;
-  if (q_len <= 1) return;  // decode rows and idle sequences are handled elsewhere
-  const int L = a.seq_lens[s];
   const int tile_q = C::kRows / a.group;  // query tokens per CTA
+  int s, qt, row0, q_len, ctx, kend, ntiles, key_base = 0;  // keys [key_base, kend)
+  if constexpr (CASCADE) {
+    s = 0;
+    qt = blockIdx.x;
+    row0 = 0;
+    q_len = static_cast<int>(a.num_tokens);
+    ctx = 0;  // unused: no causal mask inside the shared prefix
+    key_base = blockIdx.z * kPartitionTokens;
+    kend = key_base + kPartitionTokens;
+    ntiles = kPartitionTokens / C::kKeys;
+    if (qt * tile_q >= q_len) {
+      grid_dependency_wait();
+      return;
+    }
+  } else {
+    // Later q tiles of a chunk see more keys: dispatch them first so the grid's tail is short.
+    qt = gridDim.x - 1 - blockIdx.x;
+    s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq);
+    if (s < 0) return;
+    row0 = a.query_start_loc[s];
+    q_len = a.query_start_loc[s + 1] - row0;
+    if (q_len <= 1) return;  // decode rows and idle sequences are handled elsewhere
+    const int L = a.seq_lens[s];
+    if (q_len > L || (L + BS - 1) / BS > a.max_blocks || row0 < 0 ||
+        row0 + q_len > a.num_tokens) {
+      if (qt == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
+      return;
+    }
+    if ((q_len + tile_q - 1) / tile_q > static_cast<int>(gridDim.x)) {
+      if (qt == 0 && tid == 0) atomicOr(a.err, kErrHint);
+      return;
+    }
+    if (qt * tile_q >= q_len) return;
+    ctx = L - q_len;
+    kend = ctx + min(q_len, qt * tile_q + tile_q);  // keys [0, kend) are visible to some row
+    ntiles = (kend + C::kKeys - 1) / C::kKeys;
+  }
   const int qbase = qt * tile_q;
-  if (q_len > L || (L + BS - 1) / BS > a.max_blocks || row0 < 0 ||
-      row0 + q_len > a.num_tokens) {
-    if (qt == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
-    return;
-  }
-  if ((q_len + tile_q - 1) / tile_q > static_cast<int>(gridDim.x)) {
-    if (qt == 0 && tid == 0) atomicOr(a.err, kErrHint);
-    return;
-  }
-  if (qbase >= q_len) return;
-  const int ctx = L - q_len;
-  const int q_hi = min(q_len, qbase + tile_q);
-  const int kend = ctx + q_hi;  // keys [0, kend) are visible to some row of the tile
-  const int ntiles = (kend + C::kKeys - 1) / C::kKeys;
 
   // Every block id the CTA will read is checked before any copy is issued.
   int bad = 0;
   const int nblk = (kend + BS - 1) / BS;
-  for (int j = tid; j < nblk; j += C::kThreads) {
+  for (int j = key_base / BS + tid; j < nblk; j += C::kThreads) {
     const int32_t blk = a.block_tables[static_cast<int64_t>(s) * a.bt_stride + j];
     if (blk < 0 || blk >= a.num_blocks) bad = 1;
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0) atomicOr(a.err, kErrBlockRange);
+    if constexpr (CASCADE) grid_dependency_wait();
     return;
   }
 
@@ -623,7 +692,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     const bool is_v = warp == kVWarp;
     produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
                                 is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
-                                is_v ? v_empty : k_empty, is_v ? v_s : k_s);
+                                is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base);
   } else if (warp == kMmaWarp && lane == 0) {
     // ============================================================== MMA issuer (one thread)
     // Issuing a tcgen05.mma waits until the pipe takes it and the pipe queues almost nothing,
@@ -723,7 +792,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
       // Scores stay raw where scale > 0 (the max commutes with the scale, which is folded into
       // the exponent's FMA below); otherwise they are scaled here.  Masked keys become -inf.
       const int key0 = j * C::kKeys;
-      const bool masked = key0 + C::kKeys - 1 > min_pos;
+      const bool masked = !CASCADE && key0 + C::kKeys - 1 > min_pos;
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (prescale || masked) {
 #pragma unroll
@@ -777,7 +846,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
       l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
 
       const int tile0 = j * C::kKeys;
-      if (j == ntiles - 1 && tile0 + C::kKeys > kend) {
+      if (!CASCADE && j == ntiles - 1 && tile0 + C::kKeys > kend) {
         // The last tile: V rows at or past kend may be stale or NaN; zero them once the tile
         // has landed (the MMA reads V only after p_full below).  Thread r clears V row r.
         const int vst = j % C::kVStages;
@@ -814,10 +883,41 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     const float m_e = red_m[0][r], m_o = two ? red_m[1][r] : -INFINITY;
     const float mm = fmaxf(m_e, m_o);
     const float w_e = ex2_approx(m_e - mm), w_o = two ? ex2_approx(m_o - mm) : 0.f;
-    const float inv = 1.f / (red_l[0][r] * w_e + (two ? red_l[1][r] * w_o : 0.f));
+    const float l_all = red_l[0][r] * w_e + (two ? red_l[1][r] * w_o : 0.f);
+    const float inv = 1.f / l_all;
     bool ok = !*reinterpret_cast<volatile int*>(&softmax_stop);
     if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err);
-    if (!__any_sync(0xffffffffu, !ok)) {
+    if (CASCADE && !__any_sync(0xffffffffu, !ok)) {
+      // The rows' partials of partition blockIdx.z: m (log2 units), l, and this thread's half
+      // of O / l.
+      tmem_fence_after_sync();
+      const int64_t pidx = (static_cast<int64_t>(qbase + qi) * a.num_q_heads + g * a.group + hg) *
+                               a.max_parts + blockIdx.z;
+      if (rv && par == 0) {
+        a.part_m[pidx] = mm;
+        a.part_l[pidx] = l_all;
+      }
+      const uint32_t oe = tmem + lane_addr + C::kOCol + par * kOHalf;
+      float* dst = a.part_o + pidx * D + par * kOHalf;
+#pragma unroll
+      for (int c0 = 0; c0 < kOHalf; c0 += 32) {
+        uint32_t te[32], to[32];
+        tmem_ld32(oe + c0, te);
+        tmem_ld32(oe + D + c0, to);
+        tmem_wait_ld();
+        tmem_regs_ready(te);
+        tmem_regs_ready(to);
+        if (rv) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4*>(dst + c0 + c) = make_float4(
+                (__uint_as_float(te[c]) * w_e + __uint_as_float(to[c]) * w_o) * inv,
+                (__uint_as_float(te[c + 1]) * w_e + __uint_as_float(to[c + 1]) * w_o) * inv,
+                (__uint_as_float(te[c + 2]) * w_e + __uint_as_float(to[c + 2]) * w_o) * inv,
+                (__uint_as_float(te[c + 3]) * w_e + __uint_as_float(to[c + 3]) * w_o) * inv);
+        }
+      }
+    } else if (!CASCADE && !__any_sync(0xffffffffu, !ok)) {
       tmem_fence_after_sync();
       __half* dst = a.out + (static_cast<int64_t>(row0 + qbase + qi) * a.num_q_heads +
                              g * a.group + hg) * D + par * kOHalf;
@@ -855,13 +955,14 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(C::kTmemCols)
                  : "memory");
+  if constexpr (CASCADE) grid_dependency_wait();  // see the pair kernel
 }
 
 // Both kernels share the launch shape rules: 384 threads, one CTA per SM (TMEM and shared
 // memory), and a register split that must fit the launch allocation.
 template <typename C, typename K>
 cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                       int q_tiles, cudaStream_t stream) {
+                       int q_tiles, cudaStream_t stream, bool cascade = false) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -875,8 +976,25 @@ cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const
   // Query tokens per CTA: whole tokens per Q tile (128 / group rounds down), times the tiles.
   const int rows_q = q_tiles * (C::kRows / a.group);
   dim3 grid((a.max_query_len + rows_q - 1) / rows_q, a.num_kv_heads, a.prefill_seqs);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
-  return cudaGetLastError();
+  if (!cascade) {
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
+    return cudaGetLastError();
+  }
+  // The shared-prefix pass: every query row of the batch, every kv head, every prefix
+  // partition; a programmatic dependent of the decode kernel, so its CTAs take SMs as the
+  // decode grid drains.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((a.num_tokens + rows_q - 1) / rows_q),
+                     a.num_kv_heads, a.cascade_parts);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
 // Chunks that fit one Q tile (speculative verify, short chunks) go to the parity kernel, which
@@ -886,12 +1004,37 @@ template <int D, int BS>
 cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
   if (a.max_query_len <= ParityCfg<D>::kRows / a.group)
-    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS>, a, kmap, vmap, 1, stream);
-  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS>, a, kmap, vmap, PairCfg<D>::kQTiles,
-                                stream);
+    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, false>, a, kmap, vmap, 1, stream);
+  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, false>, a, kmap, vmap,
+                                PairCfg<D>::kQTiles, stream);
+}
+
+// The shared-prefix pass does 4 key tiles per CTA.  While the pair kernel's grid would leave
+// SMs idle, one Q tile per CTA (the parity kernel: twice the CTAs, each key tile's softmax on
+// its own warpgroup) finishes sooner; past that, the pair kernel's shared K/V tiles win.
+template <int D, int BS>
+cudaError_t launch_cascade_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             cudaStream_t stream) {
+  const int64_t rows_pair = PairCfg<D>::kQTiles * (PairCfg<D>::kRows / a.group);
+  const int64_t pair_ctas = (a.num_tokens + rows_pair - 1) / rows_pair * a.num_kv_heads *
+                            a.cascade_parts;
+  if (pair_ctas < a.num_sms)
+    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, true>, a, kmap, vmap, 1, stream,
+                                    true);
+  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, true>, a, kmap, vmap,
+                                PairCfg<D>::kQTiles, stream, true);
 }
 
 }  // namespace
+
+cudaError_t launch_shared_prefix(const AttnArgs& a, const CUtensorMap& kmap,
+                                 const CUtensorMap& vmap, cudaStream_t stream) {
+  if (a.head_dim == 128)
+    return a.block_size == 16 ? launch_cascade_t<128, 16>(a, kmap, vmap, stream)
+                              : launch_cascade_t<128, 32>(a, kmap, vmap, stream);
+  return a.block_size == 16 ? launch_cascade_t<64, 16>(a, kmap, vmap, stream)
+                            : launch_cascade_t<64, 32>(a, kmap, vmap, stream);
+}
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            cudaStream_t stream) {

@@ -36,7 +36,7 @@ def test_header_declares_the_abi():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.pa_version() == 2
+    assert lib.pa_version() == 3
 
 
 # --------------------------------------------------------------- hand-made descriptors (no GPU)
@@ -112,10 +112,34 @@ def test_attention_rejects_bad_arguments(lib, kw, status, text):
     assert text in msg(lib), msg(lib)
 
 
+@pytest.mark.parametrize("kw, status, text", [
+    (dict(hint=(1, 1000, 0, -512)), B.PA_ERR_INVALID_ARG, "non-negative"),
+    (dict(hint=(1, 1000, 0, 256)), B.PA_ERR_INVALID_ARG, "multiple of 512"),
+    (dict(hint=(1, 512, 0, 512), bt=T(B.PA_I32, [3, 64])), B.PA_ERR_INVALID_ARG, "below max_seq_len"),
+    (dict(hint=(1, 1000, 0, 512)), B.PA_ERR_INVALID_ARG, "within the block tables"),
+    (dict(hint=(2, 1000, 0, 512), bt=T(B.PA_I32, [3, 64])), B.PA_ERR_UNSUPPORTED, "decode rows"),
+])
+def test_shared_prefix_hint_is_validated(lib, kw, status, text):
+    assert call_attention(lib, **kw) == status
+    assert text in msg(lib), msg(lib)
+
+
+def test_shared_prefix_refused_over_fp8(lib):
+    n, hq, hkv, d, bs, nb, mb = 3, 8, 2, 128, 16, 40, 64
+    args = [ctypes.byref(x) for x in (
+        T(B.PA_F16, [n, hq, d]), T(B.PA_F8E4M3, [nb, hkv, bs, d]), T(B.PA_F8E4M3, [nb, hkv, bs, d]),
+        T(B.PA_I32, [n, mb]), T(B.PA_I32, [n]), T(B.PA_I32, [n + 1]))]
+    r = lib.pa_attention_fp8(*args, ctypes.c_float(0.1), ctypes.byref(T(B.PA_F16, [n, hq, d])),
+                             ctypes.byref(B.PABatchHint(1, 1000, 0, 512)),
+                             ctypes.byref(B.PAKVScales(0.5, 0.5)), None, 0, None)
+    assert r == B.PA_ERR_UNSUPPORTED and "fp16 cache" in msg(lib)
+
+
 def test_timing_hook_rejects_unknown_kernel(lib):
     assert lib.pa_set_timing_events(7, None, None) == B.PA_ERR_INVALID_ARG
     assert "PA_TIMED" in msg(lib)
     assert lib.pa_set_timing_events(1, None, None) == B.PA_OK
+    assert lib.pa_set_timing_events(2, None, None) == B.PA_OK
 
 
 def test_attention_null_tensor(lib):

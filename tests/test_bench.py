@@ -46,6 +46,25 @@ def test_aliased_prefix_counts_unique_blocks_once():
     assert n["kv_unique"] == (shared + sum(s.seq_len - shared for s in b.seqs)) * row
 
 
+def test_shared_prefix_pass_splits_the_kernel_bytes():
+    """With the pass, the decode kernel moves the keys past the prefix and the pass moves the
+    prefix once plus every query row; together they are the step's unique K/V."""
+    b = W.prefix_shared_decode(keep_contiguous=False, keep_pre=False)
+    sp = bench.shared_prefix_tokens(b)
+    assert sp == 2048
+    n0, n = bench.algorithmic_bytes(b), bench.algorithmic_bytes(b, sp)
+    row = b.num_kv_heads * b.head_dim * 4
+    q = b.num_tokens * b.num_q_heads * b.head_dim * 2
+    assert n["shared_prefix_kernel_bytes"] == sp * row + q
+    assert n0["decode_kernel_bytes"] - n["decode_kernel_bytes"] == sp * row
+    assert n["shared_prefix_kernel_flops"] == 4 * b.num_q_heads * b.head_dim * sp * b.num_tokens
+    assert bench.launches_per_step(b, sp) == bench.launches_per_step(b) + 1 == 4
+    # an FP8 cache, prefill rows or no whole shared partition: no pass
+    assert bench.shared_prefix_tokens(W.to_fp8(b)) == 0
+    assert bench.shared_prefix_tokens(small_prefix()) == 0
+    assert bench.shared_prefix_tokens(small_mixed()) == 0
+
+
 def test_mixed_step_counts_prefill_launch():
     b = small_mixed()
     assert bench.launches_per_step(b) == 4
