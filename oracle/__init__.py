@@ -44,13 +44,15 @@ def _load():
             p = ctypes.c_void_p
             lib.pa_oracle_half_to_double.restype = ctypes.c_double
             lib.pa_oracle_half_to_double.argtypes = [ctypes.c_uint16]
+            lib.pa_oracle_bf16_to_double.restype = ctypes.c_double
+            lib.pa_oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.pa_oracle_set_threads.argtypes = [ctypes.c_int]
             lib.pa_oracle_get_threads.restype = ctypes.c_int
             lib.pa_oracle_reshape_and_cache.restype = ctypes.c_int
             lib.pa_oracle_reshape_and_cache.argtypes = [u16p, u16p, u16p, u16p, p, i64, i64,
                                                         i64, i64, i64]
             common = [u16p, u16p, u16p, i32p, i64, i32p, i32p, i64, i64, i64, i64, i64, i64,
-                      ctypes.c_double]
+                      ctypes.c_double, i64]
             lib.pa_oracle_attention.restype = ctypes.c_int
             lib.pa_oracle_attention.argtypes = common + [p, p]
             lib.pa_oracle_attention_split.restype = ctypes.c_int
@@ -58,7 +60,7 @@ def _load():
             lib.pa_oracle_attention_contiguous.restype = ctypes.c_int
             lib.pa_oracle_attention_contiguous.argtypes = [u16p, u16p, u16p, p, i32p, i32p,
                                                            i64, i64, i64, i64,
-                                                           ctypes.c_double, p, p]
+                                                           ctypes.c_double, i64, p, p]
             _lib = lib
     return _lib
 
@@ -73,7 +75,7 @@ def _np(x, dtype):
         import torch
         if isinstance(x, torch.Tensor):
             x = x.detach().cpu().contiguous()
-            if x.dtype == torch.float16:
+            if x.dtype in (torch.float16, torch.bfloat16):
                 x = x.view(torch.int16)
             x = x.numpy()
     except ImportError:  # pragma: no cover
@@ -103,6 +105,29 @@ def half_to_double(bits) -> np.ndarray:
     lib = _load()
     b = np.asarray(bits, dtype=np.uint16).ravel()
     return np.array([lib.pa_oracle_half_to_double(int(x)) for x in b], dtype=np.float64)
+
+
+def bf16_to_double(bits) -> np.ndarray:
+    """Widen raw bfloat16 bit patterns to float64 through the oracle's own decoder."""
+    lib = _load()
+    b = np.asarray(bits, dtype=np.uint16).ravel()
+    return np.array([lib.pa_oracle_bf16_to_double(int(x)) for x in b], dtype=np.float64)
+
+
+FMT_F16, FMT_BF16 = 0, 1
+
+
+def _fmt(*tensors) -> int:
+    """The 16-bit format of q and the pools: bfloat16 when they are torch bfloat16 tensors,
+    else binary16 (torch float16, or raw uint16 patterns, which are read as binary16)."""
+    try:
+        import torch
+        kinds = {isinstance(t, torch.Tensor) and t.dtype == torch.bfloat16 for t in tensors}
+    except ImportError:  # pragma: no cover
+        kinds = {False}
+    if len(kinds) != 1:
+        raise ValueError("q and the pools must all be bfloat16 or all be binary16")
+    return FMT_BF16 if kinds.pop() else FMT_F16
 
 
 def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping):
@@ -246,17 +271,19 @@ def _mask(row_mask, t):
 
 
 def attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale,
-              row_mask=None, partition_size: int = 0) -> np.ndarray:
+              row_mask=None, partition_size: int = 0, fmt=None) -> np.ndarray:
     """fp64 attention over the paged cache, [T, Hq, d].  ``partition_size > 0`` computes it
-    split-context with a log-sum-exp merge instead.  Rows outside ``row_mask`` are NaN."""
+    split-context with a log-sum-exp merge instead.  Rows outside ``row_mask`` are NaN.
+    q and the pools are binary16 or bfloat16 (``fmt`` None: from the torch dtypes)."""
     lib = _load()
+    fmt = _fmt(q, k_cache, v_cache) if fmt is None else int(fmt)
     q16, kc, vc, bt, sl, qsl, (t, hq, hkv, d, bs, nb) = _attn_args(
         q, k_cache, v_cache, block_tables, seq_lens, query_start_loc)
     out = np.full((t, hq, d), np.nan, dtype=np.float64)
     m = _mask(row_mask, t)
     mp = _ptr(m) if m is not None else None
     args = [_ptr(q16), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(sl), _ptr(qsl),
-            sl.shape[0], hq, hkv, d, bs, nb, float(scale)]
+            sl.shape[0], hq, hkv, d, bs, nb, float(scale), fmt]
     if partition_size > 0:
         rc = lib.pa_oracle_attention_split(*args, int(partition_size), mp, _ptr(out))
     else:
@@ -267,9 +294,10 @@ def attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scal
 
 
 def attention_contiguous(q, k, v, kv_start, seq_lens, query_start_loc, scale,
-                         row_mask=None) -> np.ndarray:
+                         row_mask=None, fmt=None) -> np.ndarray:
     """fp64 attention over contiguous per-sequence K/V ``[sum L, Hkv, d]``."""
     lib = _load()
+    fmt = _fmt(q, k, v) if fmt is None else int(fmt)
     q16 = _np(q, np.uint16)
     k16, v16 = _np(k, np.uint16), _np(v, np.uint16)
     ks = _np(kv_start, np.int64)
@@ -280,7 +308,7 @@ def attention_contiguous(q, k, v, kv_start, seq_lens, query_start_loc, scale,
     out = np.full((t, hq, d), np.nan, dtype=np.float64)
     m = _mask(row_mask, t)
     rc = lib.pa_oracle_attention_contiguous(_ptr(q16), _ptr(k16), _ptr(v16), _ptr(ks), _ptr(sl),
-                                            _ptr(qsl), sl.shape[0], hq, hkv, d, float(scale),
+                                            _ptr(qsl), sl.shape[0], hq, hkv, d, float(scale), fmt,
                                             _ptr(m) if m is not None else None, _ptr(out))
     if rc:
         raise OracleError(f"attention_contiguous: code {rc}")

@@ -23,7 +23,9 @@
  *   block_tables int32 [N, MB]        seq_lens int32 [N]   query_start_loc int32 [N+1]
  *   slot_mapping int64 [T_new], slot = block * bs + offset, negative = skip
  * fp16 values arrive as raw IEEE binary16 bit patterns (uint16) and are widened to double
- * exactly by half_to_double.  Arithmetic is fp64 throughout; exp is the C library's exp().
+ * exactly by half_to_double.  A bfloat16 cache (fmt = 1 in the attention entry points) arrives
+ * the same way as raw bfloat16 patterns and is widened exactly by bf16_to_double.  Arithmetic
+ * is fp64 throughout; exp is the C library's exp().
  */
 #include <math.h>
 #include <stdint.h>
@@ -51,6 +53,31 @@ double pa_oracle_half_to_double(uint16_t h) {
     v = ldexp((double)(f + 1024), e - 25);
   }
   return sign ? -v : v;
+}
+
+/* bfloat16 -> double, from the format's definition: the upper half of an IEEE binary32, i.e.
+ * 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits; exponent 0 = subnormal
+ * (fraction * 2^-133), 255 = inf/NaN. */
+double pa_oracle_bf16_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 7) & 255;
+  int f = h & 127;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)f, -133);
+  } else if (e == 255) {
+    v = f ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(f + 128), e - 134);
+  }
+  return sign ? -v : v;
+}
+
+typedef double (*widen_fn)(uint16_t);
+
+/* fmt 0: binary16 values, fmt 1: bfloat16 values; NULL for anything else. */
+static widen_fn widen_for(int64_t fmt) {
+  return fmt == 0 ? pa_oracle_half_to_double : fmt == 1 ? pa_oracle_bf16_to_double : NULL;
 }
 
 void pa_oracle_set_threads(int n) {
@@ -185,7 +212,7 @@ static int check_descriptor(const int32_t *seq_lens, const int32_t *qsl, int64_t
 static int run_group(const uint16_t *q, const double *K, const double *V, int64_t L,
                      int64_t row0, int64_t q_len, int64_t g, int64_t num_q_heads,
                      int64_t group, int64_t d, double scale, int64_t part,
-                     const uint8_t *row_mask, double *out) {
+                     const uint8_t *row_mask, widen_fn widen, double *out) {
   double *qrow = (double *)malloc(sizeof(double) * (size_t)d);
   double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
   int64_t np = part > 0 ? (L + part - 1) / part : 1;
@@ -203,7 +230,7 @@ static int run_group(const uint16_t *q, const double *K, const double *V, int64_
     int64_t n_visible = L - q_len + i + 1;
     for (int64_t h = g * group; h < (g + 1) * group; ++h) {
       const uint16_t *qh = q + (t * num_q_heads + h) * d;
-      for (int64_t j = 0; j < d; ++j) qrow[j] = pa_oracle_half_to_double(qh[j]);
+      for (int64_t j = 0; j < d; ++j) qrow[j] = widen(qh[j]);
       double *o = out + (t * num_q_heads + h) * d;
       if (part > 0)
         attend_one_split(qrow, K, V, n_visible, d, scale, part, s, o_parts, m_parts, l_parts, o);
@@ -219,11 +246,11 @@ static int run_group(const uint16_t *q, const double *K, const double *V, int64_
  * block_tables[s][p / bs] at offset p % bs; kv head g of that token is the row
  * k_cache[blk][g][p % bs][:]. */
 static void depage(const uint16_t *cache, const int32_t *table_row, int64_t L, int64_t g,
-                   int64_t num_kv_heads, int64_t bs, int64_t d, double *dst) {
+                   int64_t num_kv_heads, int64_t bs, int64_t d, widen_fn widen, double *dst) {
   for (int64_t p = 0; p < L; ++p) {
     int64_t blk = table_row[p / bs];
     const uint16_t *src = cache + ((blk * num_kv_heads + g) * bs + p % bs) * d;
-    for (int64_t j = 0; j < d; ++j) dst[p * d + j] = pa_oracle_half_to_double(src[j]);
+    for (int64_t j = 0; j < d; ++j) dst[p * d + j] = widen(src[j]);
   }
 }
 
@@ -232,10 +259,11 @@ static int attention_paged(const uint16_t *q, const uint16_t *k_cache, const uin
                            const int32_t *seq_lens, const int32_t *qsl, int64_t num_seqs,
                            int64_t num_q_heads, int64_t num_kv_heads, int64_t head_dim,
                            int64_t block_size, int64_t num_blocks, double scale, int64_t part,
-                           const uint8_t *row_mask, double *out) {
+                           const uint8_t *row_mask, int64_t fmt, double *out) {
   int rc = check_descriptor(seq_lens, qsl, num_seqs, num_q_heads, num_kv_heads, head_dim);
   if (rc) return rc;
-  if (block_size <= 0 || part < 0) return ORACLE_BAD_ARG;
+  widen_fn widen = widen_for(fmt);
+  if (block_size <= 0 || part < 0 || !widen) return ORACLE_BAD_ARG;
   for (int64_t s = 0; s < num_seqs; ++s) {
     if (qsl[s + 1] == qsl[s]) continue;
     int64_t nb = (seq_lens[s] + block_size - 1) / block_size;
@@ -258,10 +286,12 @@ static int attention_paged(const uint16_t *q, const uint16_t *k_cache, const uin
     double *V = (double *)malloc(sizeof(double) * (size_t)(L * head_dim));
     int r = ORACLE_NO_MEMORY;
     if (K && V) {
-      depage(k_cache, block_tables + s * max_blocks, L, g, num_kv_heads, block_size, head_dim, K);
-      depage(v_cache, block_tables + s * max_blocks, L, g, num_kv_heads, block_size, head_dim, V);
+      depage(k_cache, block_tables + s * max_blocks, L, g, num_kv_heads, block_size, head_dim,
+             widen, K);
+      depage(v_cache, block_tables + s * max_blocks, L, g, num_kv_heads, block_size, head_dim,
+             widen, V);
       r = run_group(q, K, V, L, qsl[s], q_len, g, num_q_heads, group, head_dim, scale, part,
-                    row_mask, out);
+                    row_mask, widen, out);
     }
     free(K);
     free(V);
@@ -274,15 +304,17 @@ static int attention_paged(const uint16_t *q, const uint16_t *k_cache, const uin
 }
 
 /* Attention over the paged cache (textbook, unsplit).  Output fp64 [T, Hq, d]; rows with
- * row_mask[t] == 0 (row_mask may be NULL = all rows) are left untouched. */
+ * row_mask[t] == 0 (row_mask may be NULL = all rows) are left untouched.  q and the pools hold
+ * binary16 (fmt 0) or bfloat16 (fmt 1) patterns. */
 int pa_oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                         const int32_t *block_tables, int64_t max_blocks, const int32_t *seq_lens,
                         const int32_t *qsl, int64_t num_seqs, int64_t num_q_heads,
                         int64_t num_kv_heads, int64_t head_dim, int64_t block_size,
-                        int64_t num_blocks, double scale, const uint8_t *row_mask, double *out) {
+                        int64_t num_blocks, double scale, int64_t fmt, const uint8_t *row_mask,
+                        double *out) {
   return attention_paged(q, k_cache, v_cache, block_tables, max_blocks, seq_lens, qsl, num_seqs,
                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, 0,
-                         row_mask, out);
+                         row_mask, fmt, out);
 }
 
 /* The same attention computed split-context (partitions of `partition_size` key positions,
@@ -292,12 +324,12 @@ int pa_oracle_attention_split(const uint16_t *q, const uint16_t *k_cache,
                               int64_t max_blocks, const int32_t *seq_lens, const int32_t *qsl,
                               int64_t num_seqs, int64_t num_q_heads, int64_t num_kv_heads,
                               int64_t head_dim, int64_t block_size, int64_t num_blocks,
-                              double scale, int64_t partition_size, const uint8_t *row_mask,
-                              double *out) {
+                              double scale, int64_t fmt, int64_t partition_size,
+                              const uint8_t *row_mask, double *out) {
   if (partition_size <= 0) return ORACLE_BAD_ARG;
   return attention_paged(q, k_cache, v_cache, block_tables, max_blocks, seq_lens, qsl, num_seqs,
                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                         partition_size, row_mask, out);
+                         partition_size, row_mask, fmt, out);
 }
 
 /* Attention over contiguous per-sequence K/V (the "one region per request" layout the pages
@@ -308,9 +340,11 @@ int pa_oracle_attention_contiguous(const uint16_t *q, const uint16_t *k, const u
                                    const int64_t *kv_start, const int32_t *seq_lens,
                                    const int32_t *qsl, int64_t num_seqs, int64_t num_q_heads,
                                    int64_t num_kv_heads, int64_t head_dim, double scale,
-                                   const uint8_t *row_mask, double *out) {
+                                   int64_t fmt, const uint8_t *row_mask, double *out) {
   int rc = check_descriptor(seq_lens, qsl, num_seqs, num_q_heads, num_kv_heads, head_dim);
   if (rc) return rc;
+  widen_fn widen = widen_for(fmt);
+  if (!widen) return ORACLE_BAD_ARG;
   int64_t group = num_q_heads / num_kv_heads;
   int64_t ntask = num_seqs * num_kv_heads;
   int err = 0;
@@ -328,12 +362,12 @@ int pa_oracle_attention_contiguous(const uint16_t *q, const uint16_t *k, const u
         const uint16_t *ks = k + ((kv_start[s] + p) * num_kv_heads + g) * head_dim;
         const uint16_t *vs = v + ((kv_start[s] + p) * num_kv_heads + g) * head_dim;
         for (int64_t j = 0; j < head_dim; ++j) {
-          K[p * head_dim + j] = pa_oracle_half_to_double(ks[j]);
-          V[p * head_dim + j] = pa_oracle_half_to_double(vs[j]);
+          K[p * head_dim + j] = widen(ks[j]);
+          V[p * head_dim + j] = widen(vs[j]);
         }
       }
       r = run_group(q, K, V, L, qsl[s], q_len, g, num_q_heads, group, head_dim, scale, 0,
-                    row_mask, out);
+                    row_mask, widen, out);
     }
     free(K);
     free(V);

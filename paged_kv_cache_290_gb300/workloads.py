@@ -89,7 +89,8 @@ class PagedBatch:
     v_contig: Optional[torch.Tensor] = None
     kv_start: Optional[torch.Tensor] = None   # int64 [N], row of k_contig where seq s starts
     meta: dict = field(default_factory=dict)
-    # "f16", or "e4m3": the pools hold E4M3 codes (uint8) standing for k_scale * value (v_scale)
+    # "f16"; "bf16": q, the new tokens and the pools are bfloat16; or "e4m3": the pools hold
+    # E4M3 codes (uint8) standing for k_scale * value (v_scale)
     kv_dtype: str = "f16"
     k_scale: float = 1.0
     v_scale: float = 1.0
@@ -328,6 +329,22 @@ def to_fp8(b: PagedBatch, k_scale: float = 1.0 / 32, v_scale: float = 1.0 / 32) 
     return out
 
 
+def to_bf16(b: PagedBatch) -> PagedBatch:
+    """The same batch in bfloat16: q, the new tokens, the pools and the contiguous copies are
+    rounded from fp16 to bfloat16 (torch's conversion, round to nearest even).  Rounding the
+    pool and the new tokens the same way keeps the pool's new slots equal to what the
+    scatter-write stores; NaN sentinels stay NaN."""
+    def bf(t):
+        return None if t is None else t.to(torch.bfloat16)
+    out = PagedBatch(**{**b.__dict__})
+    out.name = b.name + "_bf16"
+    for f in ("q", "k_new", "v_new", "k_cache_pre", "v_cache_pre", "k_cache", "v_cache",
+              "k_contig", "v_contig"):
+        setattr(out, f, bf(getattr(b, f)))
+    out.kv_dtype = "bf16"
+    return out
+
+
 # ---------------------------------------------------------------------------------------------
 # The five workloads.  Model names only fix head counts and head_dim.
 
@@ -415,5 +432,7 @@ WORKLOADS = {
     "mixed_step_bs16_8dec": lambda **kw: mixed_step(16, num_decode=8, **kw),
     "spec_verify": spec_verify,
     "llama70b_32x8k_decode_fp8": lambda **kw: to_fp8(llama70b_decode(**kw)),
+    "llama70b_32x8k_decode_bf16": lambda **kw: to_bf16(llama70b_decode(**kw)),
+    "mixed_step_bs16_bf16": lambda **kw: to_bf16(mixed_step(16, **kw)),
     "llama70b_8x8k_decode_fp8": lambda **kw: to_fp8(llama70b_decode(8, **kw)),
 }

@@ -8,7 +8,7 @@ import numpy as np
 
 
 def _f64(t):
-    return t.detach().cpu().numpy().astype(np.float64)
+    return t.detach().cpu().double().numpy()  # exact for fp16, bfloat16 and float64
 
 
 def brute_attention(q, k_contig, v_contig, kv_start, seq_lens, query_start_loc, scale):

@@ -408,3 +408,49 @@ def test_fp8_attention_matches_brute_force_on_dequantised_kv(make):
     ref = brute_attention(b.q, deq(b.k_contig, b.k_scale), deq(b.v_contig, b.v_scale),
                           b.kv_start, b.seq_lens, b.query_start_loc, b.scale)
     assert np.allclose(o, ref, rtol=0, atol=1e-12, equal_nan=True)
+
+
+# ---------------------------------------------------------------- bfloat16 KV cache
+
+def test_bf16_to_double_all_patterns():
+    """The oracle's bfloat16 decoder against torch's bfloat16 -> float64 conversion, every bit
+    pattern, plus values the format fixes by hand."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    mine = oracle.bf16_to_double(bits.numpy().view(np.uint16))
+    ref = bits.view(torch.bfloat16).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert oracle.bf16_to_double([0x3F80])[0] == 1.0
+    assert oracle.bf16_to_double([0xC000])[0] == -2.0
+    assert oracle.bf16_to_double([0x0001])[0] == 2.0 ** -133
+    assert oracle.bf16_to_double([0x7F7F])[0] == (2 - 2.0 ** -7) * 2.0 ** 127
+
+
+@pytest.mark.parametrize("make", [small_decode, small_mixed, small_spec,
+                                  lambda: small_decode(d=64, bs=32, hq=32, hkv=2, seed=9106)])
+def test_bf16_attention_matches_numpy_brute_force(make):
+    b = W.to_bf16(make())
+    assert b.q.dtype == b.k_cache.dtype == torch.bfloat16
+    o = oracle.attention_batch(b)
+    ref = brute_attention(b.q, b.k_contig, b.v_contig, b.kv_start, b.seq_lens,
+                          b.query_start_loc, b.scale)
+    assert np.allclose(o, ref, rtol=0, atol=1e-12, equal_nan=True)
+
+
+def test_bf16_and_fp16_patterns_of_the_same_values_agree_bitwise():
+    """Values exact in both formats (multiples of 1/64 in [-4, 4]) give bit-identical fp64
+    attention whichever 16-bit format carries them: the format only changes the widening."""
+    b = small_mixed(d=64, hq=8, hkv=2, seed=9233)
+    snap = lambda t: (t.float() * 64).round().clamp(-256, 256).div(64).half()
+    for f in ("q", "k_cache", "v_cache"):
+        t = getattr(b, f)
+        setattr(b, f, torch.where(torch.isnan(t), t, snap(t)))
+    h = oracle.attention_batch(b)
+    bb = W.to_bf16(b)
+    assert torch.equal(bb.q.float(), b.q.float())                  # conversion was exact
+    assert np.array_equal(oracle.attention_batch(bb), h, equal_nan=True)
+    with pytest.raises(ValueError):
+        oracle.attention(b.q, bb.k_cache, bb.v_cache, b.block_tables, b.seq_lens,
+                         b.query_start_loc, b.scale)
+
