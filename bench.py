@@ -370,7 +370,9 @@ def run_ours(args, world, rank, local):
     result = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if b.kv_dtype == "bf16" else "f16",  # E4M3 codes run fp16 MMAs
+        "data": "synthetic",
         "config": {"workload": args.workload, "num_seqs": b.num_seqs,
                    "max_seq_len": b.max_seq_len, "max_query_len": b.max_query_len,
                    "num_tokens": b.num_tokens, "num_q_heads": b.num_q_heads,

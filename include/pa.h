@@ -19,7 +19,9 @@
  *     owns no buffer and allocates no device memory; the caller owns everything, including
  *     the attention workspace.
  *   - Strides are in elements.  The innermost dimension must be contiguous (stride 1).
- *   - fp16 is IEEE binary16.  Accumulation is fp32; outputs are rounded to nearest-even.
+ *   - fp16 is IEEE binary16; bf16 is bfloat16 (the upper half of an IEEE binary32).  A call
+ *     works in one 16-bit type: k, v, q, out and the pools all fp16 or all bf16 (FP8 pools take
+ *     fp16 tokens, q and out).  Accumulation is fp32; outputs are rounded to nearest-even.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream), like a
  *     kernel launch.  Nothing synchronises except pa_get_device_error.
  *   - Host-checkable errors are returned synchronously and nothing is launched.  Device-data
@@ -60,11 +62,12 @@ typedef enum pa_dtype {
   PA_F16 = 0,
   PA_I32 = 1,
   PA_I64 = 2,
-  PA_F8E4M3 = 3 /* one byte: 1 sign, 4 exponent (bias 7), 3 mantissa bits; 0x7F/0xFF NaN, max 448 */
+  PA_F8E4M3 = 3, /* one byte: 1 sign, 4 exponent (bias 7), 3 mantissa bits; 0x7F/0xFF NaN, max 448 */
+  PA_BF16 = 4    /* bfloat16: 1 sign, 8 exponent (bias 127), 7 mantissa bits */
 } pa_dtype;
 
 typedef struct pa_tensor {
-  void* data;                 /* device pointer, 16-byte aligned for fp16 tensors */
+  void* data;                 /* device pointer, 16-byte aligned for fp16 / bf16 tensors */
   int32_t dtype;              /* pa_dtype */
   int32_t ndim;
   int64_t shape[PA_MAX_DIMS];
@@ -88,7 +91,8 @@ typedef struct pa_batch_hint {
                                agree there), so they are attended once for all query rows (p1:
                                requests that start alike share pages; p2 prefix-caching slide)
                                and merged with each sequence's own keys by the log-sum-exp rule.
-                               Decode rows and fp16 caches only (else PA_ERR_UNSUPPORTED); a
+                               Decode rows over fp16 or bf16 caches only (else
+                               PA_ERR_UNSUPPORTED); a
                                sequence whose table differs there, or with no key past the
                                prefix, is reported as PA_ERR_DESCRIPTOR. */
 } pa_batch_hint;
@@ -99,9 +103,9 @@ typedef struct pa_batch_hint {
  * processed token is stored once; "Local_LLM_03_vLLM_Architecture", paged-KV slide: the store is a
  * set of fixed-size blocks.)
  *
- *   k, v          fp16 [T_new, Hkv, d]; token stride free (multiple of 8), head stride d.
+ *   k, v          fp16 or bf16 [T_new, Hkv, d]; token stride free (multiple of 8), head stride d.
  *   k_cache,
- *   v_cache       fp16 [NB, Hkv, bs, d], contiguous ("HND" per block: one (block, kv head) is a
+ *   v_cache       [NB, Hkv, bs, d] of the same type as k and v, contiguous ("HND" per block: one (block, kv head) is a
  *                 contiguous bs x d tile).  Written in place.
  *   slot_mapping  int64 [T_new]; token t goes to block slot/bs, offset slot%bs.  slot < 0 means
  *                 "padding, skip".  A slot >= NB*bs is skipped and reported on the device.
@@ -127,8 +131,8 @@ size_t pa_attention_workspace_size(int64_t num_tokens, int64_t num_q_heads, int6
  * physical blocks through the block table; chunked-prefill slide; "vLLM: LLM Inference That
  * Doesn't Waste Your GPU", "Continuous batching": prefill and decode in the same step.)
  *
- *   q                fp16 [T, Hq, d]; token stride free (multiple of 8), head stride d.
- *   k_cache, v_cache fp16 [NB, Hkv, bs, d] contiguous, already holding this step's tokens
+ *   q                fp16 or bf16 [T, Hq, d]; token stride free (multiple of 8), head stride d.
+ *   k_cache, v_cache [NB, Hkv, bs, d] of q's type, contiguous, already holding this step's tokens
  *                    (call pa_reshape_and_cache first, on the same stream).
  *   block_tables     int32 [N, MB]; row stride free.  Entry j of row s = physical block of
  *                    logical positions j*bs .. j*bs+bs-1 of sequence s.  Entries past
@@ -139,7 +143,7 @@ size_t pa_attention_workspace_size(int64_t num_tokens, int64_t num_q_heads, int6
  *                    owns rows query_start_loc[s] .. query_start_loc[s+1]-1.  One row is a
  *                    decode step, several a prefill chunk; any mix and order in one call.
  *   scale            multiplies q.k before the softmax (typically 1/sqrt(d)).
- *   out              fp16 [T, Hq, d] contiguous.
+ *   out              [T, Hq, d] of q's type, contiguous.
  *   hint             required; see pa_batch_hint.
  *   workspace        device scratch of at least pa_attention_workspace_size(T, Hq, d,
  *                    hint->max_seq_len) bytes, 256-byte aligned (NULL allowed when that is 0).
@@ -181,8 +185,8 @@ int pa_reshape_and_cache_fp8(const pa_tensor* k, const pa_tensor* v, const pa_te
 
 /*
  * pa_attention_fp8 -- pa_attention over an FP8 cache (q and out stay fp16).  Every E4M3 value
- * is exact in fp16, so the kernel converts a K/V unit to fp16 in shared memory and runs the fp16
- * path with the score scale multiplied by k_scale and the output by v_scale.  Decode rows
+ * is exact in fp16, so the kernel converts the codes to fp16 MMA operands in registers and runs
+ * the fp16 arithmetic with the score scale multiplied by k_scale and the output by v_scale.  Decode rows
  * only: a batch whose hint has max_query_len > 1 is refused with PA_ERR_UNSUPPORTED (prefill
  * over an FP8 cache is not built).  Workspace as for pa_attention.
  */
@@ -232,7 +236,7 @@ int pa_get_device_error(void* stream, uint32_t* bits);
  * pairs[i][0] are copied to block pairs[i][1] ("Local_LLM_03_vLLM_Architecture", prefix-caching
  * slide: shared blocks; a sequence that appends into a partial block it shares gets its own
  * copy first, the copy-on-write the host block manager asks for).
- *   k_cache, v_cache  [NB, Hkv, bs, d], contiguous, fp16 or PA_F8E4M3 (both the same).
+ *   k_cache, v_cache  [NB, Hkv, bs, d], contiguous, fp16, bf16 or PA_F8E4M3 (both the same).
  *   pairs             int32 [n, 2] contiguous device array (src, dst).  Destinations must be
  *                     distinct and never a source of the same call.
  * A pair with an id outside the pool is skipped and reported as PA_ERR_OUT_OF_RANGE by

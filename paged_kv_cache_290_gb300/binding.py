@@ -29,7 +29,7 @@ PA_ERR_NO_BLOCKS = 8
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
                 4: "PA_ERR_TIMEOUT", 5: "PA_ERR_OUT_OF_RANGE", 6: "PA_ERR_WORKSPACE",
                 7: "PA_ERR_DESCRIPTOR", 8: "PA_ERR_NO_BLOCKS"}
-PA_F16, PA_I32, PA_I64, PA_F8E4M3 = 0, 1, 2, 3
+PA_F16, PA_I32, PA_I64, PA_F8E4M3, PA_BF16 = 0, 1, 2, 3, 4
 PARTITION_TOKENS = 512
 EXPORTED = ("pa_reshape_and_cache", "pa_attention_workspace_size", "pa_attention",
             "pa_last_error", "pa_get_device_error", "pa_set_timing_events", "pa_version",
@@ -41,7 +41,7 @@ EXPORTED = ("pa_reshape_and_cache", "pa_attention_workspace_size", "pa_attention
 
 # Byte tensors are E4M3 codes (the only one-byte type of the ABI).
 _DTYPES = {torch.float16: PA_F16, torch.int32: PA_I32, torch.int64: PA_I64,
-           torch.uint8: PA_F8E4M3, torch.float8_e4m3fn: PA_F8E4M3}
+           torch.uint8: PA_F8E4M3, torch.float8_e4m3fn: PA_F8E4M3, torch.bfloat16: PA_BF16}
 
 
 class PATensor(ctypes.Structure):

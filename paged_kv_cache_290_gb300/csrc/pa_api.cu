@@ -83,12 +83,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D view of a pool [NB, Hkv, bs, d] as rows of d fp16 values; TMA box = 16 rows x 64 values
-// (128 B) with the 128-byte swizzle the kernels' fragment loads expect.
-// The pool as a 2-D tensor of NB*Hkv*bs rows x d elements.  fp16: boxes of 16 rows x 64 values
-// (128 bytes), 128-byte swizzle.  FP8: boxes of 16 rows x d bytes, 128-byte swizzle for d = 128
-// and none for d = 64 (a 64-byte row).
-int make_pool_map(CUtensorMap* m, void* base, int64_t rows, int d, bool fp8 = false) {
+// The pool [NB, Hkv, bs, d] as a 2-D tensor of NB*Hkv*bs rows x d elements, in the layout the
+// kernels' fragment loads expect.  fp16 / bf16: boxes of 16 rows x 64 values (128 bytes),
+// 128-byte swizzle.  FP8: boxes of 16 rows x d bytes, 128-byte swizzle for d = 128 and none for
+// d = 64 (a 64-byte row).
+int make_pool_map(CUtensorMap* m, void* base, int64_t rows, int d, int dtype) {
+  const bool fp8 = dtype == PA_F8E4M3;
   auto enc = tensor_map_encoder();
   if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
@@ -97,7 +97,10 @@ int make_pool_map(CUtensorMap* m, void* base, int64_t rows, int d, bool fp8 = fa
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapSwizzle swz =
       !fp8 || d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+  const CUtensorMapDataType ty = fp8               ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(m, ty, 2,
                    base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -111,6 +114,7 @@ const char* dtype_name(int dt) {
     case PA_I32: return "int32";
     case PA_I64: return "int64";
     case PA_F8E4M3: return "float8_e4m3";
+    case PA_BF16: return "bfloat16";
     default: return "unknown";
   }
 }
@@ -149,6 +153,10 @@ int check_contiguous(const pa_tensor* t, const char* name) {
   }
   return PA_OK;
 }
+
+// Element type of a 16-bit pool entry point: bfloat16 when the pool says so, else fp16 (a pool
+// of any other type then fails check_pool with a message naming float16).
+int pool_dtype16(const pa_tensor* kc) { return kc && kc->dtype == PA_BF16 ? PA_BF16 : PA_F16; }
 
 // Pool [NB, Hkv, bs, d] checks shared by both entry points.
 int check_pool(const pa_tensor* kc, const pa_tensor* vc, int dtype = PA_F16) {
@@ -224,9 +232,11 @@ static int reshape_impl(const pa_tensor* k, const pa_tensor* v, const pa_tensor*
   g_last_error.clear();
   int rc;
   if (fp8 && (rc = check_scales(sc))) return rc;
-  if ((rc = check_pool(k_cache, v_cache, fp8 ? PA_F8E4M3 : PA_F16))) return rc;
-  if ((rc = check_tensor(k, "k", PA_F16, 3))) return rc;
-  if ((rc = check_tensor(v, "v", PA_F16, 3))) return rc;
+  // fp16 or bf16 tokens into a pool of the same type; fp16 tokens into an FP8 pool
+  const int in_dt = fp8 ? PA_F16 : pool_dtype16(k_cache);
+  if ((rc = check_pool(k_cache, v_cache, fp8 ? PA_F8E4M3 : in_dt))) return rc;
+  if ((rc = check_tensor(k, "k", in_dt, 3))) return rc;
+  if ((rc = check_tensor(v, "v", in_dt, 3))) return rc;
   if ((rc = check_tensor(slot_mapping, "slot_mapping", PA_I64, 1))) return rc;
   const int64_t t = k->shape[0], hkv = k_cache->shape[1], d = k_cache->shape[3];
   for (const pa_tensor* x : {k, v}) {
@@ -281,7 +291,7 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_
   g_last_error.clear();
   int rc;
   const bool fp8 = k_cache && k_cache->dtype == PA_F8E4M3;
-  if ((rc = check_pool(k_cache, v_cache, fp8 ? PA_F8E4M3 : PA_F16))) return rc;
+  if ((rc = check_pool(k_cache, v_cache, fp8 ? PA_F8E4M3 : pool_dtype16(k_cache)))) return rc;
   if ((rc = check_tensor(pairs, "pairs", PA_I32, 2))) return rc;
   if (pairs->shape[1] != 2 || (pairs->shape[0] > 1 && pairs->stride[0] != 2))
     return fail(PA_ERR_INVALID_ARG, "pairs must be a contiguous int32 [n, 2] array");
@@ -309,9 +319,11 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
   g_last_error.clear();
   int rc;
   if (fp8 && (rc = check_scales(sc))) return rc;
-  if ((rc = check_pool(k_cache, v_cache, fp8 ? PA_F8E4M3 : PA_F16))) return rc;
-  if ((rc = check_tensor(q, "q", PA_F16, 3))) return rc;
-  if ((rc = check_tensor(out, "out", PA_F16, 3))) return rc;
+  // q, out and the pools all fp16 or all bf16; fp16 q and out over an FP8 pool
+  const int in_dt = fp8 ? PA_F16 : pool_dtype16(k_cache);
+  if ((rc = check_pool(k_cache, v_cache, fp8 ? PA_F8E4M3 : in_dt))) return rc;
+  if ((rc = check_tensor(q, "q", in_dt, 3))) return rc;
+  if ((rc = check_tensor(out, "out", in_dt, 3))) return rc;
   if ((rc = check_tensor(block_tables, "block_tables", PA_I32, 2))) return rc;
   if ((rc = check_tensor(seq_lens, "seq_lens", PA_I32, 1))) return rc;
   if ((rc = check_tensor(query_start_loc, "query_start_loc", PA_I32, 1))) return rc;
@@ -355,7 +367,7 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
                                       "the block tables");
     if (fp8 || hint->max_query_len > 1)
       return fail(PA_ERR_UNSUPPORTED, "the shared-prefix pass is built for decode rows over an "
-                                      "fp16 cache");
+                                      "fp16 or bf16 cache");
   }
   if (hint->max_query_len > hint->max_seq_len)
     return fail(PA_ERR_INVALID_ARG, "hint max_query_len exceeds max_seq_len");
@@ -403,6 +415,7 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
   a.scale_log2 = scale * 1.4426950408889634f * (fp8 ? sc->k_scale : 1.f);
   a.v_scale = fp8 ? sc->v_scale : 1.f;
   a.kv_fp8 = fp8 ? 1 : 0;
+  a.bf16 = in_dt == PA_BF16 ? 1 : 0;
   a.cascade_parts = sp / PA_PARTITION_TOKENS;
   cudaError_t e = device_error_word(&a.err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
@@ -411,8 +424,9 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
 
   const int64_t rows = k_cache->shape[0] * hkv * k_cache->shape[2];
   CUtensorMap kmap, vmap;
-  if ((rc = make_pool_map(&kmap, k_cache->data, rows, static_cast<int>(d), fp8))) return rc;
-  if ((rc = make_pool_map(&vmap, v_cache->data, rows, static_cast<int>(d), fp8))) return rc;
+  const int pool_dt = k_cache->dtype;
+  if ((rc = make_pool_map(&kmap, k_cache->data, rows, static_cast<int>(d), pool_dt))) return rc;
+  if ((rc = make_pool_map(&vmap, v_cache->data, rows, static_cast<int>(d), pool_dt))) return rc;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   auto mark = [&](int kernel, bool stop) {

@@ -2,10 +2,11 @@
 //
 // Everything here is inline PTX or plain CUDA: mbarrier waits that give up after a time limit
 // (so a lost copy can never hang the GPU), 2-D tensor (TMA) loads into 128-byte-swizzled shared
-// memory, ldmatrix / movmatrix fragment loads and the m16n8k16 fp16 MMA.
+// memory, ldmatrix / movmatrix fragment loads and the m16n8k16 fp16 / bf16 MMA.
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -166,6 +167,41 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The same three operations for a 16-bit element type chosen at compile time: BF = false is
+// IEEE binary16, BF = true bfloat16 (round to nearest even in both).
+template <bool BF>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  if constexpr (BF) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    mma_f16_16816(d, a, b0, b1);
+  }
+}
+
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    return pack_half2(lo, hi);
+  }
+}
+
+// One value stored as the element type at p (2 bytes).
+template <bool BF>
+__device__ __forceinline__ void store_elem(__half* p, float x) {
+  if constexpr (BF)
+    *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
+  else
+    *p = __float2half_rn(x);
+}
+
 __device__ __forceinline__ float warp_max_xor(float v, int lane_mask) {
   return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, lane_mask));
 }
@@ -187,10 +223,13 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t addr, uint32_t lbo, uint
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor for kind::f16 with fp16 A/B and an fp32 accumulator: D format in
-// [4,6), A/B major-ness in bits 15/16 (1 = MN-major), N >> 3 in [17,23), M >> 4 in [24,29).
-__host__ __device__ constexpr uint32_t umma_idesc_f16(int m, int n, int a_mn, int b_mn) {
-  return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+// Instruction descriptor for kind::f16 with fp16 (or bf16) A/B and an fp32 accumulator: D format
+// in [4,6), A and B formats in [7,10) and [10,13) (0 = f16, 1 = bf16), A/B major-ness in bits
+// 15/16 (1 = MN-major), N >> 3 in [17,23), M >> 4 in [24,29).
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int m, int n, int a_mn, int b_mn,
+                                                      bool bf16 = false) {
+  return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) |  // A and B both bf16, or both f16
+         (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 

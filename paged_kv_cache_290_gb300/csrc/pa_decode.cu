@@ -26,6 +26,8 @@
 // transposing ldmatrix gives 2 tokens x 2 dims, which fill the A fragment of V^T under a
 // permutation of its rows (m-row i <-> dim 2i, m-row i + 8 <-> dim 2i + 1), undone when O is
 // written out.  k_scale is folded into the score scale and v_scale multiplies the outputs.
+// bfloat16 cache (with bf16 q and out): the fp16 data path with bf16 MMAs, P rounded to bf16
+// for the P V product, and bf16 outputs.
 // Both kernels are programmatic dependents of what precedes them on the stream: they may be
 // scheduled early but read nothing from global memory before griddepcontrol.wait.
 #include <algorithm>
@@ -68,10 +70,14 @@ __device__ __forceinline__ uint32_t ldg_u32(const __half* p) {
   return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
-template <int D, int BS, int NT, bool F8>
-__global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
+// What the pools hold: fp16, E4M3 codes (with fp16 q/out), or bf16 (with bf16 q/out).
+enum KvKind : int { kKvF16 = 0, kKvE4M3 = 1, kKvBF16 = 2 };
+
+template <int D, int BS, int NT, int KV>
+__global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
     decode_partition_kernel(const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
+  constexpr bool F8 = KV == kKvE4M3, BF = KV == kKvBF16;
   using C = DecodeCfg<D, BS, NT, F8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[C::kWarps][C::kStages];
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
                                   f16x2_from_e4m3x2(r[2 * h + 1] >> 16)};
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            mma_f16_16816(sacc[nt], af, qf[nt][2 * jj + h][0], qf[nt][2 * jj + h][1]);
+            mma_16816<BF>(sacc[nt], af, qf[nt][2 * jj + h][0], qf[nt][2 * jj + h][1]);
         }
       }
     } else {
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
         uint32_t af[4];
         ldsm_x4(kb + (chunk >> 3) * C::kBoxBytes + swz128(tok, chunk & 7), af);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sacc[nt], af, qf[nt][j][0], qf[nt][j][1]);
+        for (int nt = 0; nt < NT; ++nt) mma_16816<BF>(sacc[nt], af, qf[nt][j][0], qf[nt][j][1]);
       }
     }
 
@@ -270,8 +276,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
         o[nt][dt][2] *= al0;
         o[nt][dt][3] *= al1;
       }
-      pb0[nt] = movmatrix_trans(pack_half2(p00, p01));  // P^T[tok 2cq..2cq+1][head gq]
-      pb1[nt] = movmatrix_trans(pack_half2(p10, p11));  // P^T[tok 2cq+8..][head gq]
+      pb0[nt] = movmatrix_trans(pack2<BF>(p00, p01));  // P^T[tok 2cq..2cq+1][head gq]
+      pb1[nt] = movmatrix_trans(pack2<BF>(p10, p11));  // P^T[tok 2cq+8..][head gq]
     }
 
     // ---- O^T[d][heads] += V^T[d][16 tokens] P^T
@@ -299,7 +305,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
           af[2] &= vm1;
           af[3] &= vm1;
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][2 * dd + h], af, pb0[nt], pb1[nt]);
+          for (int nt = 0; nt < NT; ++nt) mma_16816<BF>(o[nt][2 * dd + h], af, pb0[nt], pb1[nt]);
         }
       }
     } else {
@@ -314,7 +320,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
         af[2] &= vm1;
         af[3] &= vm1;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[nt][dt], af, pb0[nt], pb1[nt]);
+        for (int nt = 0; nt < NT; ++nt) mma_16816<BF>(o[nt][dt], af, pb0[nt], pb1[nt]);
       }
     }
 
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
     const int hq = g * a.group + h;
     const int64_t orow = static_cast<int64_t>(row0) * a.num_q_heads + hq;
     if (nparts == 1) {
-      a.out[orow * D + d] = __float2half_rn(osum / wsum * a.v_scale);
+      store_elem<BF>(a.out + orow * D + d, osum / wsum * a.v_scale);
     } else {
       const int64_t pidx = orow * a.max_parts + part;
       a.part_o[pidx * D + d] = osum / wsum * a.v_scale;
@@ -400,7 +406,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, F8>::kThreads)
 }
 
 // One warp per (decode row, query head): combine the row's partitions.
-template <int D>
+template <int D, bool BF>
 __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a) {
   grid_dependency_wait();  // the partials come from the decode kernel just before
   grid_launch_dependents();
@@ -462,19 +468,19 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a)
   const float inv = 1.f / wsum;
   if constexpr (V == 4) {
     uint2 pk;
-    pk.x = pack_half2(acc[0] * inv, acc[1] * inv);
-    pk.y = pack_half2(acc[2] * inv, acc[3] * inv);
+    pk.x = pack2<BF>(acc[0] * inv, acc[1] * inv);
+    pk.y = pack2<BF>(acc[2] * inv, acc[3] * inv);
     *reinterpret_cast<uint2*>(dst) = pk;
   } else {
-    *reinterpret_cast<uint32_t*>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
+    *reinterpret_cast<uint32_t*>(dst) = pack2<BF>(acc[0] * inv, acc[1] * inv);
   }
 }
 
-template <int D, int BS, int NT, bool F8>
+template <int D, int BS, int NT, int KV>
 cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t stream) {
-  using C = DecodeCfg<D, BS, NT, F8>;
-  auto kern = decode_partition_kernel<D, BS, NT, F8>;
+  using C = DecodeCfg<D, BS, NT, KV == kKvE4M3>;
+  auto kern = decode_partition_kernel<D, BS, NT, KV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -492,17 +498,19 @@ cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CU
   return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
-template <int D, int BS, bool F8>
+template <int D, int BS, int KV>
 cudaError_t launch_decode_g(const AttnArgs& a, const CUtensorMap& k, const CUtensorMap& v,
                             cudaStream_t st) {
-  return a.group <= 8 ? launch_decode_t<D, BS, 1, F8>(a, k, v, st)
-                      : launch_decode_t<D, BS, 2, F8>(a, k, v, st);
+  return a.group <= 8 ? launch_decode_t<D, BS, 1, KV>(a, k, v, st)
+                      : launch_decode_t<D, BS, 2, KV>(a, k, v, st);
 }
 
 template <int D, int BS>
 cudaError_t launch_decode_f(const AttnArgs& a, const CUtensorMap& k, const CUtensorMap& v,
                             cudaStream_t st) {
-  return a.kv_fp8 ? launch_decode_g<D, BS, true>(a, k, v, st) : launch_decode_g<D, BS, false>(a, k, v, st);
+  if (a.kv_fp8) return launch_decode_g<D, BS, kKvE4M3>(a, k, v, st);
+  return a.bf16 ? launch_decode_g<D, BS, kKvBF16>(a, k, v, st)
+                : launch_decode_g<D, BS, kKvF16>(a, k, v, st);
 }
 
 }  // namespace
@@ -526,8 +534,11 @@ cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return a.head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_partitions_kernel<128>, a)
-                           : cudaLaunchKernelEx(&cfg, merge_partitions_kernel<64>, a);
+  if (a.bf16)
+    return a.head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_partitions_kernel<128, true>, a)
+                             : cudaLaunchKernelEx(&cfg, merge_partitions_kernel<64, true>, a);
+  return a.head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_partitions_kernel<128, false>, a)
+                           : cudaLaunchKernelEx(&cfg, merge_partitions_kernel<64, false>, a);
 }
 
 }  // namespace pa

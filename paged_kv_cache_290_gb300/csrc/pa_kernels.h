@@ -56,6 +56,7 @@ struct AttnArgs {
   float scale_log2;  // scale * log2(e) (times k_scale for an FP8 cache)
   float v_scale;     // FP8 cache: multiplies the output; 1 for fp16
   int kv_fp8;        // 1: the pools hold E4M3 codes
+  int bf16;          // 1: q, out and the pools are bfloat16 (else fp16)
   int cascade_parts; // leading 512-key partitions every sequence shares (attended once for all)
   int num_sms;       // SMs of the device (launch-shape choices)
   unsigned* err;

@@ -36,6 +36,8 @@
 //     P_t V_{j-1} is done (it was issued after it), so no softmax step waits on a P V.
 // V rows past the last visible key of the chunk are zeroed in shared memory before the first
 // P V product of the last key tile (0 * NaN would poison the sum).  Every wait is bounded.
+// A bfloat16 batch (q, pools and out bf16) runs the same kernels with bf16 operands in both
+// products (kind::f16 takes A and B both fp16 or both bf16), P packed as bf16 into TMEM.
 #include "pa_common.cuh"
 #include "pa_kernels.h"
 
@@ -152,7 +154,7 @@ struct PairCfg {
 // row i of q), keys are the 512-key partition blockIdx.z of the prefix that every sequence
 // shares (read through sequence 0's table), no causal mask; the epilogue writes the rows'
 // partition partials (m, l, O / l) for the log-sum-exp merge instead of the output.
-template <int D, int BS, bool CASCADE>
+template <int D, int BS, bool CASCADE, bool BF>
 __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
@@ -285,8 +287,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
                                 is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base);
   } else if (warp == kMmaWarp && lane == 0) {
     // ============================================================== MMA issuer (one thread)
-    constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0);
-    constexpr uint32_t kIdO = umma_idesc_f16(C::kRows, D, 0, 1);
+    constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0, BF);
+    constexpr uint32_t kIdO = umma_idesc_f16(C::kRows, D, 0, 1, BF);
     // S_t(j) = Q_t K_j^T into TMEM buffer t (K stage j must have landed).
     auto issue_s = [&](int t, int j) {
       const uint32_t kst = k_s + (j % C::kKStages) * C::kKVBytes;
@@ -447,7 +449,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
           const float p0 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c]), mul, neg_m));
           const float p1 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c + 1]), mul, neg_m));
           ps[c & 3] += p0 + p1;
-          pk[c] = pack_half2(p0, p1);
+          pk[c] = pack2<BF>(p0, p1);
         }
         tmem_st16(sbuf + q4 * 16, pk);
       }
@@ -522,10 +524,10 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {
             uint4 v;
-            v.x = pack_half2(__uint_as_float(tt[c]) * inv, __uint_as_float(tt[c + 1]) * inv);
-            v.y = pack_half2(__uint_as_float(tt[c + 2]) * inv, __uint_as_float(tt[c + 3]) * inv);
-            v.z = pack_half2(__uint_as_float(tt[c + 4]) * inv, __uint_as_float(tt[c + 5]) * inv);
-            v.w = pack_half2(__uint_as_float(tt[c + 6]) * inv, __uint_as_float(tt[c + 7]) * inv);
+            v.x = pack2<BF>(__uint_as_float(tt[c]) * inv, __uint_as_float(tt[c + 1]) * inv);
+            v.y = pack2<BF>(__uint_as_float(tt[c + 2]) * inv, __uint_as_float(tt[c + 3]) * inv);
+            v.z = pack2<BF>(__uint_as_float(tt[c + 4]) * inv, __uint_as_float(tt[c + 5]) * inv);
+            v.w = pack2<BF>(__uint_as_float(tt[c + 6]) * inv, __uint_as_float(tt[c + 7]) * inv);
             *reinterpret_cast<uint4*>(dst + c0 + c) = v;
           }
         }
@@ -573,7 +575,7 @@ struct ParityCfg {
 
 // CASCADE: the shared-prefix pass, as in the pair kernel (rows: every query row of the batch;
 // keys: prefix partition blockIdx.z through sequence 0's table; partials out).
-template <int D, int BS, bool CASCADE>
+template <int D, int BS, bool CASCADE, bool BF>
 __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     prefill_parity_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
@@ -698,8 +700,8 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     // Issuing a tcgen05.mma waits until the pipe takes it and the pipe queues almost nothing,
     // so every other instruction of this thread idles the tensor cores for its duration: the
     // issuer runs alone, with no warp-collective operations.
-    constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0);
-    constexpr uint32_t kIdO = umma_idesc_f16(C::kRows, D, 0, 1);
+    constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0, BF);
+    constexpr uint32_t kIdO = umma_idesc_f16(C::kRows, D, 0, 1, BF);
     // S_j = Q K_j^T into TMEM buffer j % 2; frees its K stage once done.
     auto issue_s = [&](int j) {
       const int st = j % C::kKStages;
@@ -839,7 +841,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
           const float p0 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c]), mul, neg_m));
           const float p1 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c + 1]), mul, neg_m));
           ps[c & 3] += p0 + p1;
-          pk[c] = pack_half2(p0, p1);
+          pk[c] = pack2<BF>(p0, p1);
         }
         tmem_st16(sbuf + q4 * 16, pk);
       }
@@ -937,10 +939,10 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {
             uint4 v;
-            v.x = pack_half2(o(c), o(c + 1));
-            v.y = pack_half2(o(c + 2), o(c + 3));
-            v.z = pack_half2(o(c + 4), o(c + 5));
-            v.w = pack_half2(o(c + 6), o(c + 7));
+            v.x = pack2<BF>(o(c), o(c + 1));
+            v.y = pack2<BF>(o(c + 2), o(c + 3));
+            v.z = pack2<BF>(o(c + 4), o(c + 5));
+            v.w = pack2<BF>(o(c + 6), o(c + 7));
             *reinterpret_cast<uint4*>(dst + c0 + c) = v;
           }
         }
@@ -1000,49 +1002,68 @@ cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const
 // Chunks that fit one Q tile (speculative verify, short chunks) go to the parity kernel, which
 // splits their key tiles between two softmax warpgroups; longer chunks to the pair kernel,
 // which gives each warpgroup its own Q tile and shares every K/V tile between them.
-template <int D, int BS>
+template <int D, int BS, bool BF>
 cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
   if (a.max_query_len <= ParityCfg<D>::kRows / a.group)
-    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, false>, a, kmap, vmap, 1, stream);
-  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, false>, a, kmap, vmap,
+    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, false, BF>, a, kmap, vmap, 1,
+                                    stream);
+  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, false, BF>, a, kmap, vmap,
                                 PairCfg<D>::kQTiles, stream);
 }
 
 // The shared-prefix pass does 4 key tiles per CTA.  While the pair kernel's grid would leave
 // SMs idle, one Q tile per CTA (the parity kernel: twice the CTAs, each key tile's softmax on
 // its own warpgroup) finishes sooner; past that, the pair kernel's shared K/V tiles win.
-template <int D, int BS>
+template <int D, int BS, bool BF>
 cudaError_t launch_cascade_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
   const int64_t rows_pair = PairCfg<D>::kQTiles * (PairCfg<D>::kRows / a.group);
   const int64_t pair_ctas = (a.num_tokens + rows_pair - 1) / rows_pair * a.num_kv_heads *
                             a.cascade_parts;
   if (pair_ctas < a.num_sms)
-    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, true>, a, kmap, vmap, 1, stream,
-                                    true);
-  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, true>, a, kmap, vmap,
+    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, true, BF>, a, kmap, vmap, 1,
+                                    stream, true);
+  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, true, BF>, a, kmap, vmap,
                                 PairCfg<D>::kQTiles, stream, true);
+}
+
+}  // namespace
+
+namespace {
+
+template <bool BF>
+cudaError_t launch_shared_prefix_b(const AttnArgs& a, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, cudaStream_t stream) {
+  if (a.head_dim == 128)
+    return a.block_size == 16 ? launch_cascade_t<128, 16, BF>(a, kmap, vmap, stream)
+                              : launch_cascade_t<128, 32, BF>(a, kmap, vmap, stream);
+  return a.block_size == 16 ? launch_cascade_t<64, 16, BF>(a, kmap, vmap, stream)
+                            : launch_cascade_t<64, 32, BF>(a, kmap, vmap, stream);
+}
+
+template <bool BF>
+cudaError_t launch_prefill_b(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             cudaStream_t stream) {
+  if (a.head_dim == 128)
+    return a.block_size == 16 ? launch_prefill_t<128, 16, BF>(a, kmap, vmap, stream)
+                              : launch_prefill_t<128, 32, BF>(a, kmap, vmap, stream);
+  return a.block_size == 16 ? launch_prefill_t<64, 16, BF>(a, kmap, vmap, stream)
+                            : launch_prefill_t<64, 32, BF>(a, kmap, vmap, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_shared_prefix(const AttnArgs& a, const CUtensorMap& kmap,
                                  const CUtensorMap& vmap, cudaStream_t stream) {
-  if (a.head_dim == 128)
-    return a.block_size == 16 ? launch_cascade_t<128, 16>(a, kmap, vmap, stream)
-                              : launch_cascade_t<128, 32>(a, kmap, vmap, stream);
-  return a.block_size == 16 ? launch_cascade_t<64, 16>(a, kmap, vmap, stream)
-                            : launch_cascade_t<64, 32>(a, kmap, vmap, stream);
+  return a.bf16 ? launch_shared_prefix_b<true>(a, kmap, vmap, stream)
+                : launch_shared_prefix_b<false>(a, kmap, vmap, stream);
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            cudaStream_t stream) {
-  if (a.head_dim == 128)
-    return a.block_size == 16 ? launch_prefill_t<128, 16>(a, kmap, vmap, stream)
-                              : launch_prefill_t<128, 32>(a, kmap, vmap, stream);
-  return a.block_size == 16 ? launch_prefill_t<64, 16>(a, kmap, vmap, stream)
-                            : launch_prefill_t<64, 32>(a, kmap, vmap, stream);
+  return a.bf16 ? launch_prefill_b<true>(a, kmap, vmap, stream)
+                : launch_prefill_b<false>(a, kmap, vmap, stream);
 }
 
 }  // namespace pa

@@ -132,7 +132,7 @@ def test_shared_prefix_refused_over_fp8(lib):
     r = lib.pa_attention_fp8(*args, ctypes.c_float(0.1), ctypes.byref(T(B.PA_F16, [n, hq, d])),
                              ctypes.byref(B.PABatchHint(1, 1000, 0, 512)),
                              ctypes.byref(B.PAKVScales(0.5, 0.5)), None, 0, None)
-    assert r == B.PA_ERR_UNSUPPORTED and "fp16 cache" in msg(lib)
+    assert r == B.PA_ERR_UNSUPPORTED and "bf16 cache" in msg(lib)
 
 
 def test_timing_hook_rejects_unknown_kernel(lib):
