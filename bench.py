@@ -49,6 +49,15 @@ def shared_prefix_tokens(b) -> int:
     return sp if ok else 0
 
 
+def shared_prefix_kernel(b, sp: int, num_sms: int = 152) -> str:
+    """The kernel pa_attention picks for the shared-prefix pass: one Q tile per CTA while the
+    two-tile grid (2 x 128 // G rows per CTA, every kv head and prefix partition) would not
+    fill the GPU's SMs."""
+    rows_pair = 2 * (128 // (b.num_q_heads // b.num_kv_heads))
+    ctas = -(-b.num_tokens // rows_pair) * b.num_kv_heads * (sp // 512)
+    return "prefill_parity_kernel" if ctas < num_sms else "prefill_pair_kernel"
+
+
 def algorithmic_bytes(b, sp: int = 0) -> dict:
     """Bytes the step must move at minimum.  K/V are counted per attended token of every
     sequence ("logical"); "unique" counts each physical (block, offset) slot once, which is what
@@ -257,6 +266,9 @@ def run_ours(args, world, rank, local):
     b = W.WORKLOADS[args.workload](keep_contiguous=False, keep_pre=False)
     sp = 0 if args.no_shared_prefix else shared_prefix_tokens(b)
     nbytes = algorithmic_bytes(b, sp)
+    if sp:
+        nbytes["shared_prefix_kernel"] = shared_prefix_kernel(
+            b, sp, torch.cuda.get_device_properties(dev).multi_processor_count)
     stream = torch.cuda.current_stream()
 
     # device-resident inputs (the pool already holds every token; the scatter rewrites the new
@@ -286,15 +298,16 @@ def run_ours(args, world, rank, local):
     if st != 0:
         raise RuntimeError(f"device error after warm-up: status {st} bits {bits}")
 
-    # -------- device-resident timed region
+    # -------- device-resident timed region: exactly K steps, nothing between the step events
+    # but the step itself
     timed = (([] if all_prefill(b) else ["decode"]) + (["prefill"] if b.max_query_len > 1 else [])
              + (["shared_prefix"] if sp else []))
     mk = lambda: torch.cuda.Event(enable_timing=True)
-    ev = [(mk(), mk(), {k: (mk(), mk()) for k in timed}) for _ in range(args.steps)]
-    for _, _, kev in ev:      # torch creates an event on its first record(); the library then
-        for k0, k1 in kev.values():  # re-records these handles around the kernels it launches
-            k0.record(stream)
-            k1.record(stream)
+    ev = [(mk(), mk()) for _ in range(args.steps)]
+    kev = [{k: (mk(), mk()) for k in timed} for _ in range(args.steps)]
+    for e in ev + [p for d_ in kev for p in d_.values()]:
+        e[0].record(stream)   # torch creates an event on its first record(); the library then
+        e[1].record(stream)   # re-records the kernel events around the kernels it launches
     torch.cuda.synchronize()
     uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", ""))
     clocks = ClockSampler(uuid)
@@ -304,21 +317,34 @@ def run_ours(args, world, rank, local):
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 255)
-        s0, s1, kev = ev[i]
-        for k, (k0, k1) in kev.items():
-            pa.set_timing_events(k0, k1, kernel=k)
-        s0.record(stream)
+        ev[i][0].record(stream)
         step(q, k_new, v_new, slots, bt, sl, qsl, out)
-        s1.record(stream)
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(world)
+    step_ms = [a.elapsed_time(c) for a, c in ev]
+
+    # -------- per-kernel times: K more steps with CUDA events recorded around each attention
+    # kernel on the launching stream (pa_set_timing_events).  An event between two launches
+    # stops the second from starting while the first drains (programmatic dependent launch),
+    # so these steps run a little longer and only their kernel intervals are used.
+    inst_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 255)
+        for k, (k0, k1) in kev[i].items():
+            pa.set_timing_events(k0, k1, kernel=k)
+        a0, a1 = mk(), mk()
+        a0.record(stream)
+        step(q, k_new, v_new, slots, bt, sl, qsl, out)
+        a1.record(stream)
+        inst_ms.append((a0, a1))
+    torch.cuda.synchronize()
     for k in timed:
         pa.set_timing_events(None, None, kernel=k)
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(c) for a, c, _ in ev]
-    kern_ms = {k: statistics.mean(kev[k][0].elapsed_time(kev[k][1]) for _, _, kev in ev)
-               for k in timed}
+    kern_ms = {k: statistics.mean(d_[k][0].elapsed_time(d_[k][1]) for d_ in kev) for k in timed}
+    inst_step_ms = statistics.mean(a.elapsed_time(c) for a, c in inst_ms)
     st, bits = pa.get_device_error()
     if st != 0:
         raise RuntimeError(f"device error in timed region: status {st} bits {bits}")
@@ -389,6 +415,9 @@ def run_ours(args, world, rank, local):
         "roofline_kernels": kernels,
         "gpu_launches": launches_per_step(b, sp) * args.steps,
         "wall_ms_per_step": wall * 1e3 / args.steps,
+        "kernel_timing": {"steps": args.steps, "ms_per_step_with_kernel_events": inst_step_ms,
+                          "note": "per-kernel CUDA events are taken on K further steps; "
+                                  "value and ms_per_step come from K steps without them"},
         "clocks": clk,
         "impl": "ours",
     }
@@ -407,7 +436,8 @@ def kernel_rooflines(nbytes, kern_ms, peaks) -> dict:
     specs = {"decode": ("decode_partition_kernel", nbytes["decode_kernel_bytes"], 0),
              "prefill": (nbytes.get("prefill_kernel", "prefill"), nbytes["prefill_kernel_bytes"],
                          nbytes["prefill_kernel_flops"]),
-             "shared_prefix": ("prefill_pair_kernel (shared-prefix pass)",
+             "shared_prefix": (nbytes.get("shared_prefix_kernel", "prefill kernel") +
+                               " (shared-prefix pass)",
                                nbytes.get("shared_prefix_kernel_bytes", 0),
                                nbytes.get("shared_prefix_kernel_flops", 0))}
     for k, ms in kern_ms.items():

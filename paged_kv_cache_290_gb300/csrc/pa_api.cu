@@ -54,6 +54,35 @@ cudaError_t device_error_word(unsigned** out) {
   return cudaSuccess;
 }
 
+// A side stream (highest priority) and two events per device and host thread: a call with both
+// prefill chunks and decode rows runs the prefill kernel there, beside the decode and merge
+// kernels on the caller's stream (fork and join through the events), so the HBM-bound decode
+// grid fills the SMs the compute-bound prefill grid leaves idle in its tail.  Created on first
+// use and kept for the thread's lifetime.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream g_side[kMaxDevices];
+
+cudaError_t side_stream(SideStream** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideStream& s = g_side[dev];
+  if (!s.stream) {
+    int least = 0, greatest = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithPriority(&s.stream, cudaStreamNonBlocking, greatest)) != cudaSuccess)
+      return e;
+  }
+  *out = &s;
+  return cudaSuccess;
+}
+
 // SM count of the current device (looked up once per device).
 cudaError_t device_sm_count(int* out) {
   int dev = 0;
@@ -429,32 +458,61 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
   if ((rc = make_pool_map(&vmap, v_cache->data, rows, static_cast<int>(d), pool_dt))) return rc;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  auto mark = [&](int kernel, bool stop) {
+  auto mark = [&](int kernel, bool stop, cudaStream_t on) {
     cudaEvent_t ev = stop ? g_time_stop[kernel] : g_time_start[kernel];
-    return ev ? cudaEventRecord(ev, st) : cudaSuccess;
+    return ev ? cudaEventRecord(ev, on) : cudaSuccess;
   };
+  auto prefill = [&](cudaStream_t on) -> int {
+    cudaError_t err;
+    if ((err = mark(PA_TIMED_PREFILL, false, on)) != cudaSuccess) return cuda_fail(err, "timing event");
+    if ((err = pa::launch_prefill(a, kmap, vmap, on)) != cudaSuccess)
+      return cuda_fail(err, "prefill launch");
+    if ((err = mark(PA_TIMED_PREFILL, true, on)) != cudaSuccess) return cuda_fail(err, "timing event");
+    return PA_OK;
+  };
+  // Prefill chunks next to decode rows: the prefill grid goes first, on the side stream, and the
+  // caller's stream waits for it (the join) after its own launches, on every return path.
+  struct Join {
+    SideStream* side = nullptr;
+    cudaStream_t st = nullptr;
+    cudaError_t done() {
+      if (!side) return cudaSuccess;
+      cudaError_t je = cudaEventRecord(side->join, side->stream);
+      if (je == cudaSuccess) je = cudaStreamWaitEvent(st, side->join, 0);
+      side = nullptr;
+      return je;
+    }
+    ~Join() { done(); }
+  } join;
+  if (!all_prefill && hint->max_query_len > 1) {
+    SideStream* side = nullptr;
+    if ((e = side_stream(&side)) != cudaSuccess) return cuda_fail(e, "side stream");
+    if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess)
+      return cuda_fail(e, "stream fork");
+    join.side = side;
+    join.st = st;
+    if ((rc = prefill(side->stream))) return rc;
+  }
+  auto mark_st = [&](int kernel, bool stop) { return mark(kernel, stop, st); };
   if (!all_prefill) {
-    if ((e = mark(PA_TIMED_DECODE, false)) != cudaSuccess) return cuda_fail(e, "timing event");
+    if ((e = mark_st(PA_TIMED_DECODE, false)) != cudaSuccess) return cuda_fail(e, "timing event");
     e = pa::launch_decode(a, kmap, vmap, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    if ((e = mark(PA_TIMED_DECODE, true)) != cudaSuccess) return cuda_fail(e, "timing event");
+    if ((e = mark_st(PA_TIMED_DECODE, true)) != cudaSuccess) return cuda_fail(e, "timing event");
   }
   if (a.cascade_parts > 0) {
-    if ((e = mark(PA_TIMED_SHARED_PREFIX, false)) != cudaSuccess) return cuda_fail(e, "timing event");
+    if ((e = mark_st(PA_TIMED_SHARED_PREFIX, false)) != cudaSuccess) return cuda_fail(e, "timing event");
     e = pa::launch_shared_prefix(a, kmap, vmap, st);
     if (e != cudaSuccess) return cuda_fail(e, "shared-prefix launch");
-    if ((e = mark(PA_TIMED_SHARED_PREFIX, true)) != cudaSuccess) return cuda_fail(e, "timing event");
+    if ((e = mark_st(PA_TIMED_SHARED_PREFIX, true)) != cudaSuccess) return cuda_fail(e, "timing event");
   }
   if (a.max_parts > 1 && !all_prefill) {
     e = pa::launch_merge(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
-  if (hint->max_query_len > 1) {
-    if ((e = mark(PA_TIMED_PREFILL, false)) != cudaSuccess) return cuda_fail(e, "timing event");
-    e = pa::launch_prefill(a, kmap, vmap, st);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-    if ((e = mark(PA_TIMED_PREFILL, true)) != cudaSuccess) return cuda_fail(e, "timing event");
-  }
+  if (all_prefill) return prefill(st);  // only prefill chunks: everything on the caller's stream
+  if ((e = join.done()) != cudaSuccess) return cuda_fail(e, "stream join");
   return PA_OK;
 }
 

@@ -17,9 +17,10 @@
 // a (query token, head of the GQA group) pair, so one K/V tile serves every head of the group,
 // and every K/V tile the CTA loads serves both Q tiles (256 rows).  Warp roles:
 //   * producers (warps 8 and 9): stream 128-key K and V tiles (8 units of 16 tokens gathered
-//     through the block table, 128-byte-swizzled TMA boxes) into separate 2-stage rings; a K
-//     stage is released once both S = Q K^T products that read it are done, a V stage after
-//     both P V products,
+//     through the block table, 128-byte-swizzled TMA boxes) into a 2-stage K ring and a 3-stage
+//     V ring; a K stage is released once both S = Q K^T products that read it are done, a V
+//     stage as soon as both P V products are (before the next S is issued).  The next tile's block ids are read while a producer waits
+//     for its stage, and the MMA issuer waits for K_{j+1} only right before S(j+1),
 //   * MMA issuer (lane 0 of warp 10): per Q tile t, S_t = Q_t K_j^T into TMEM buffer t (M 128,
 //     N 128, K d, both operands K-major from shared memory) and O_t += P_t V_j with P_t read
 //     from TMEM (it overwrites the first 64 columns of S_t's buffer, two fp16 per column) and
@@ -92,17 +93,26 @@ __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap*
                                            uint64_t* empty, uint32_t ring, int key_base = 0) {
   constexpr int kUnits = kKeys / 16, kHalves = D / 64, kKVBytes = kHalves * kKeys * 128;
   const int lane = threadIdx.x & 31;
+  // Block id of unit `lane` of tile j (0 past the keys).  The ids of tile j + 1 are loaded while
+  // tile j waits for its stage, so the table read is off the copy's critical path.
+  auto unit_block = [&](int j) {
+    const int key0 = key_base + j * kKeys;
+    const int units = min(kUnits, (kend - key0 + 15) >> 4);
+    return lane < units
+               ? a.block_tables[static_cast<int64_t>(s) * a.bt_stride + (key0 + 16 * lane) / BS]
+               : 0;
+  };
   int issued = 0;
+  int id_next = ntiles > 0 ? unit_block(0) : 0;
   for (int j = 0; j < ntiles; ++j) {
     const int st = j % stages, round = j / stages;
+    const int id = id_next;
+    if (j + 1 < ntiles) id_next = unit_block(j + 1);
     bool ok = true;
     if (lane == 0 && round > 0) ok = mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err);
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
     const int key0 = key_base + j * kKeys;
     const int units = min(kUnits, (kend - key0 + 15) >> 4);
-    const int id = lane < units
-                       ? a.block_tables[static_cast<int64_t>(s) * a.bt_stride + (key0 + 16 * lane) / BS]
-                       : 0;
     const uint32_t bar = smem_addr(&full[st]);
     if (lane == 0) mbar_arrive_expect_tx(bar, units * kHalves * 2048);
     const uint32_t dst = ring + st * kKVBytes;
@@ -132,7 +142,7 @@ struct PairCfg {
   static constexpr int kQBytes = kHalves * kHalfBytes;    // one Q tile, [half][row][128 B]
   static constexpr int kKVBytes = kHalves * kKeys * 128;  // K (or V) tile, [half][key][128 B]
   static constexpr int kKStages = 2;
-  static constexpr int kVStages = 2;
+  static constexpr int kVStages = 3;
   static constexpr int kSmemBytes =
       kQTiles * kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
   static constexpr int kSoftmax = 256;                    // one warpgroup per Q tile
@@ -147,6 +157,7 @@ struct PairCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 256;
   static_assert(kQTiles * kKeys + kQTiles * D <= 512, "S/P buffers and accumulators fit TMEM");
+  static_assert(kSmemBytes + 1024 <= 232448, "dynamic + static shared memory fit one SM");
   static constexpr float kRescaleLog2 = 8.f;              // raise the max only past 2^8
 };
 
@@ -326,8 +337,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     for (int j = 0; ok && j < ntiles; ++j) {
       const int vst = j % C::kVStages;
       const bool more = j + 1 < ntiles;
-      ok = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err) &&
-           (!more || kwait(j + 1));
+      ok = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err);
+      bool k_ready = false;  // K_{j+1} is waited for just before its first use
 #pragma unroll
       for (int t = 0; ok && t < C::kQTiles; ++t) {
         if (j >= tiles[t]) continue;
@@ -335,10 +346,19 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         if (!ok) break;
         tmem_fence_after_sync();
         issue_pv(t, j);
-        if (j + 1 < tiles[t]) issue_s(t, j + 1);
+        // V_j's stage is free once the last P V that reads it is done: release it before the
+        // next S so the producer can start the refill sooner.
+        if (t == C::kQTiles - 1 || j >= tiles[t + 1]) umma_commit(smem_addr(&v_empty[vst]));
+        if (j + 1 < tiles[t]) {
+          if (!k_ready) {
+            ok = kwait(j + 1);
+            k_ready = true;
+            if (!ok) break;
+          }
+          issue_s(t, j + 1);
+        }
       }
       if (!ok) break;
-      umma_commit(smem_addr(&v_empty[vst]));
       if (more) umma_commit(smem_addr(&k_empty[(j + 1) % C::kKStages]));
     }
     // Every MMA this thread issued has finished before O is read or the CTA tears down.
