@@ -83,6 +83,12 @@ cudaError_t side_stream(SideStream** out) {
   return cudaSuccess;
 }
 
+// CTAs per launch of the two-tile prefill kernel when it runs beside the decode kernel: one
+// wave.  (Measured on the 4 x 512 + 128-decode step: slices of one wave 459 us, one full grid
+// 475 us; smaller slices leave the prefill kernel a long serial chain of short launches,
+// 602 us at half the SMs, 889 us at 40.)
+int prefill_ctas_beside_decode(int num_sms) { return num_sms; }
+
 // SM count of the current device (looked up once per device).
 cudaError_t device_sm_count(int* out) {
   int dev = 0;
@@ -485,6 +491,8 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
     ~Join() { done(); }
   } join;
   if (!all_prefill && hint->max_query_len > 1) {
+    if ((e = device_sm_count(&a.num_sms)) != cudaSuccess) return cuda_fail(e, "device attribute");
+    a.prefill_ctas = prefill_ctas_beside_decode(a.num_sms);
     SideStream* side = nullptr;
     if ((e = side_stream(&side)) != cudaSuccess) return cuda_fail(e, "side stream");
     if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess ||

@@ -405,7 +405,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
   }
 }
 
-// One warp per (decode row, query head): combine the row's partitions.
+// One warp per (decode row, query head): combine the row's partitions.  Two dependent memory
+// rounds: the row's descriptor (query_start_loc and seq_lens together), then every partition's
+// m and l with the first 16 partitions' O rows, all in flight at once.
 template <int D, bool BF>
 __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a) {
   grid_dependency_wait();  // the partials come from the decode kernel just before
@@ -414,50 +416,73 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.x * 4 + warp;
   if (hq >= a.num_q_heads) return;
-  const int row0 = a.query_start_loc[s];
-  if (a.query_start_loc[s + 1] - row0 != 1 || row0 < 0 || row0 + 1 > a.num_tokens) return;
+  const int row0 = a.query_start_loc[s], row1 = a.query_start_loc[s + 1];
   const int L = a.seq_lens[s];
+  if (row1 - row0 != 1 || row0 < 0 || row0 + 1 > a.num_tokens) return;
   const int nparts = (L + kPartitionTokens - 1) / kPartitionTokens;
   if (nparts <= 1 || nparts > a.max_parts || (L + a.block_size - 1) / a.block_size > a.max_blocks)
     return;
   const int64_t base = (static_cast<int64_t>(row0) * a.num_q_heads + hq) * a.max_parts;
 
+  constexpr int V = D / 32;   // output elements per lane
+  constexpr int kBatch = 16;  // partitions whose O rows are in flight at once
+  constexpr int kHeld = 2;    // m and l of partitions lane, lane + 32 held in registers
+  auto load_o = [&](int p, float (&x)[V]) {
+    const float* op = a.part_o + (base + p) * D + lane * V;
+    if constexpr (V == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(op);
+      x[0] = t.x, x[1] = t.y, x[2] = t.z, x[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(op);
+      x[0] = t.x, x[1] = t.y;
+    }
+  };
+  float mh[kHeld], lh[kHeld];
+#pragma unroll
+  for (int k = 0; k < kHeld; ++k) {
+    const int p = lane + 32 * k;
+    mh[k] = p < nparts ? a.part_m[base + p] : -INFINITY;
+    lh[k] = p < nparts ? a.part_l[base + p] : 0.f;
+  }
+  float x[kBatch][V];
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j)
+    if (j < nparts) load_o(j, x[j]);
   float M = -INFINITY;
-  for (int p = lane; p < nparts; p += 32) M = fmaxf(M, a.part_m[base + p]);
+  for (int p = lane + 32 * kHeld; p < nparts; p += 32) M = fmaxf(M, a.part_m[base + p]);
+#pragma unroll
+  for (int k = 0; k < kHeld; ++k) M = fmaxf(M, mh[k]);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  // weight of partition p: 2^(m_p - M) l_p, held by lane p % 32 in register p / 32
+  float wh[kHeld];
+#pragma unroll
+  for (int k = 0; k < kHeld; ++k) wh[k] = exp2f(mh[k] - M) * lh[k];
 
-  constexpr int V = D / 32;  // output elements per lane
-  constexpr int kBatch = 16;  // partitions whose loads are all in flight at once
   float acc[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   for (int p0 = 0; p0 < nparts; p0 += kBatch) {
     const int n = min(kBatch, nparts - p0);
-    const float w = lane < n ? exp2f(a.part_m[base + p0 + lane] - M) * a.part_l[base + p0 + lane] : 0.f;
-    float x[kBatch][V];
+    if (p0 > 0) {
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      if (j < n) {
-        const float* op = a.part_o + (base + p0 + j) * D + lane * V;
-        if constexpr (V == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(op);
-          x[j][0] = t.x;
-          x[j][1] = t.y;
-          x[j][2] = t.z;
-          x[j][3] = t.w;
-        } else {
-          const float2 t = *reinterpret_cast<const float2*>(op);
-          x[j][0] = t.x;
-          x[j][1] = t.y;
-        }
-      }
+      for (int j = 0; j < kBatch; ++j)
+        if (j < n) load_o(p0 + j, x[j]);
     }
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const int p = p0 + j;  // the same for every lane
       if (j < n) {
+        float wj;
+        if (p < 32 * kHeld) {
+          float src = wh[0];
+#pragma unroll
+          for (int k = 1; k < kHeld; ++k) src = (p >> 5) == k ? wh[k] : src;
+          wj = __shfl_sync(0xffffffffu, src, p & 31);
+        } else {  // past 32 * kHeld partitions: read m and l again (the same address in every lane)
+          wj = exp2f(a.part_m[base + p] - M) * a.part_l[base + p];
+        }
         wsum += wj;
 #pragma unroll
         for (int e = 0; e < V; ++e) acc[e] += wj * x[j][e];

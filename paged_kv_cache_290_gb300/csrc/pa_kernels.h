@@ -59,6 +59,10 @@ struct AttnArgs {
   int bf16;          // 1: q, out and the pools are bfloat16 (else fp16)
   int cascade_parts; // leading 512-key partitions every sequence shares (attended once for all)
   int num_sms;       // SMs of the device (launch-shape choices)
+  int items_x;       // > 0: the two-tile prefill kernel runs as launches over slices of its
+                     //   items (x q-tile pairs per (kv head, sequence)); 0: one full grid
+  int item_base;     // first item of such a launch
+  int prefill_ctas;  // CTAs per such launch (0: one full grid)
   unsigned* err;
 };
 

@@ -39,6 +39,8 @@
 // P V product of the last key tile (0 * NaN would poison the sum).  Every wait is bounded.
 // A bfloat16 batch (q, pools and out bf16) runs the same kernels with bf16 operands in both
 // products (kind::f16 takes A and B both fp16 or both bf16), P packed as bf16 into TMEM.
+#include <algorithm>
+
 #include "pa_common.cuh"
 #include "pa_kernels.h"
 
@@ -52,7 +54,7 @@ namespace {
 // a hint error.
 template <int kThreads>
 __device__ __forceinline__ int find_prefill_seq(const AttnArgs& a, int* warp_count,
-                                                int* chosen_seq) {
+                                                int* chosen_seq, int target, bool first) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) *chosen_seq = -1;
   int found = 0;  // prefill sequences seen so far
@@ -61,8 +63,7 @@ __device__ __forceinline__ int find_prefill_seq(const AttnArgs& a, int* warp_cou
     const int ql = si < a.num_seqs ? a.query_start_loc[si + 1] - a.query_start_loc[si] : 0;
     const bool pf = ql > 1;
     const unsigned bal = __ballot_sync(0xffffffffu, pf);
-    if (a.decode_skipped && __any_sync(0xffffffffu, ql == 1) && lane == 0 && blockIdx.x == 0 &&
-        blockIdx.y == 0 && blockIdx.z == 0)
+    if (a.decode_skipped && __any_sync(0xffffffffu, ql == 1) && lane == 0 && first)
       atomicOr(a.err, kErrHint);
     if (lane == 0) warp_count[warp] = __popc(bal);
     __syncthreads();
@@ -72,14 +73,12 @@ __device__ __forceinline__ int find_prefill_seq(const AttnArgs& a, int* warp_cou
       rank += w < warp ? warp_count[w] : 0;
       total += warp_count[w];
     }
-    if (pf && rank == static_cast<int>(blockIdx.z)) *chosen_seq = si;
+    if (pf && rank == target) *chosen_seq = si;
     found += total;
     __syncthreads();
   }
   __syncthreads();
-  if (found > static_cast<int>(gridDim.z) && blockIdx.x == 0 && blockIdx.y == 0 &&
-      blockIdx.z == 0 && tid == 0)
-    atomicOr(a.err, kErrHint);
+  if (found > a.prefill_seqs && first && tid == 0) atomicOr(a.err, kErrHint);
   return *chosen_seq;
 }
 
@@ -187,7 +186,17 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   const uint32_t k_s = q_s + C::kQTiles * C::kQBytes;       // K ring
   const uint32_t v_s = k_s + C::kKStages * C::kKVBytes;     // V ring
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = blockIdx.y;
+  // Work item (q-tile pair x, kv head g, prefill sequence z): the grid's coordinates, or, when
+  // the launch is one of a series that each cover a slice of the items, item_base + blockIdx.x
+  // decoded in the same (x fastest, then g, then z) order.
+  int bx = blockIdx.x, g = blockIdx.y, bz = blockIdx.z, nx = gridDim.x;
+  if (!CASCADE && a.items_x > 0) {
+    const int item = a.item_base + static_cast<int>(blockIdx.x);
+    nx = a.items_x;
+    bx = item % nx;
+    g = (item / nx) % a.num_kv_heads;
+    bz = item / (nx * a.num_kv_heads);
+  }
   const int tile_q = C::kRows / a.group;  // query tokens per Q tile
   int s, qt, row0, q_len, ctx, key_base = 0;
   int tiles[C::kQTiles];
@@ -210,8 +219,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       tiles[t] = qt * C::kQTiles * tile_q + t * tile_q < q_len ? ntiles : 0;
   } else {
     // Later q tiles of a chunk see more keys: dispatch them first so the grid's tail is short.
-    qt = gridDim.x - 1 - blockIdx.x;
-    s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq);
+    qt = nx - 1 - bx;
+    s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq, bz, bx == 0 && g == 0 && bz == 0);
     if (s < 0) return;
     row0 = a.query_start_loc[s];
     q_len = a.query_start_loc[s + 1] - row0;
@@ -222,7 +231,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       if (qt == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
       return;
     }
-    if ((q_len + C::kQTiles * tile_q - 1) / (C::kQTiles * tile_q) > static_cast<int>(gridDim.x)) {
+    if ((q_len + C::kQTiles * tile_q - 1) / (C::kQTiles * tile_q) > nx) {
       if (qt == 0 && tid == 0) atomicOr(a.err, kErrHint);
       return;
     }
@@ -637,7 +646,8 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
   } else {
     // Later q tiles of a chunk see more keys: dispatch them first so the grid's tail is short.
     qt = gridDim.x - 1 - blockIdx.x;
-    s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq);
+    s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq, blockIdx.z,
+                                      blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0);
     if (s < 0) return;
     row0 = a.query_start_loc[s];
     q_len = a.query_start_loc[s + 1] - row0;
@@ -984,7 +994,8 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
 // memory), and a register split that must fit the launch allocation.
 template <typename C, typename K>
 cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                       int q_tiles, cudaStream_t stream, bool cascade = false) {
+                       int q_tiles, cudaStream_t stream, bool cascade = false,
+                       bool sliced = false) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -998,6 +1009,21 @@ cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const
   // Query tokens per CTA: whole tokens per Q tile (128 / group rounds down), times the tiles.
   const int rows_q = q_tiles * (C::kRows / a.group);
   dim3 grid((a.max_query_len + rows_q - 1) / rows_q, a.num_kv_heads, a.prefill_seqs);
+  if (!cascade && sliced && a.prefill_ctas > 0) {
+    // A series of launches of prefill_ctas CTAs, each over the next slice of the items (heavy q
+    // tiles of each chunk first): the prefill kernel then holds about that many SMs at a time,
+    // and the decode kernel beside it (on another stream) gets the rest from the start.
+    AttnArgs b = a;
+    b.items_x = static_cast<int>(grid.x);
+    const int64_t n_items = static_cast<int64_t>(grid.x) * grid.y * grid.z;
+    for (int64_t base = 0; base < n_items; base += a.prefill_ctas) {
+      b.item_base = static_cast<int>(base);
+      const int n = static_cast<int>(std::min<int64_t>(a.prefill_ctas, n_items - base));
+      kern<<<n, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, b);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   if (!cascade) {
     kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
     return cudaGetLastError();
@@ -1029,7 +1055,7 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const C
     return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, false, BF>, a, kmap, vmap, 1,
                                     stream);
   return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, false, BF>, a, kmap, vmap,
-                                PairCfg<D>::kQTiles, stream);
+                                PairCfg<D>::kQTiles, stream, false, true);
 }
 
 // The shared-prefix pass does 4 key tiles per CTA.  While the pair kernel's grid would leave
