@@ -430,6 +430,7 @@ WORKLOADS = {
     "mixed_step_bs16": lambda **kw: mixed_step(16, **kw),
     "mixed_step_bs32": lambda **kw: mixed_step(32, **kw),
     "mixed_step_bs16_8dec": lambda **kw: mixed_step(16, num_decode=8, **kw),
+    "mixed_step_bs16_0dec": lambda **kw: mixed_step(16, num_decode=0, **kw),
     "spec_verify": spec_verify,
     "llama70b_32x8k_decode_fp8": lambda **kw: to_fp8(llama70b_decode(**kw)),
     "llama70b_32x8k_decode_bf16": lambda **kw: to_bf16(llama70b_decode(**kw)),

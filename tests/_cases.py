@@ -45,3 +45,14 @@ def small_spec(d=128, bs=16, hq=32, hkv=4, seed=9400):
             SeqSpec(96, 2), SeqSpec(1, 1), SeqSpec(260, 6)]
     return build_batch(f"small_spec_d{d}_bs{bs}_g{hq // hkv}", seqs, num_q_heads=hq,
                        num_kv_heads=hkv, head_dim=d, block_size=bs, seed_base=seed)
+
+
+def small_long_chunks(d=128, bs=16, hq=8, hkv=2, seed=9500, decode=True):
+    """Chunks over contexts past 4096 and 8192 keys, a short chunk, and (``decode``) decode rows
+    in the same batch: with decode rows the two-tile prefill kernel runs beside the decode
+    kernel in launch slices; without, alone on the caller's stream."""
+    seqs = [SeqSpec(4096 + 40, 100), SeqSpec(8192 + 20, 150), SeqSpec(5000, 64),
+            SeqSpec(300, 33)] + ([SeqSpec(9000, 1), SeqSpec(6000, 1)] if decode else [])
+    return build_batch(f"long_chunks_d{d}_bs{bs}_g{hq // hkv}", seqs, num_q_heads=hq,
+                       num_kv_heads=hkv, head_dim=d, block_size=bs, seed_base=seed)
+

@@ -13,7 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_290_gb300 as pa
 from paged_kv_cache_290_gb300 import workloads as W
-from _cases import small_decode, small_mixed, small_spec
+from _cases import small_decode, small_long_chunks, small_mixed, small_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -89,6 +89,9 @@ CASES = {
     # the shared-prefix pass
     "shared_d128_bs16_g7": (lambda: shared(), 1024),
     "shared_d64_bs32_g8": (lambda: shared(d=64, bs=32, hq=64, hkv=8, seed=9601), 512),
+    # long contexts, beside decode rows and alone
+    "long_d128_bs16_g4": (lambda: small_long_chunks(seed=9502), 0),
+    "long_alone_d128_bs16_g4": (lambda: small_long_chunks(seed=9505, decode=False), 0),
 }
 
 

@@ -13,7 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_290_gb300 as pa
 from paged_kv_cache_290_gb300 import workloads as W
-from _cases import small_decode, small_mixed, small_prefix, small_spec
+from _cases import small_decode, small_long_chunks, small_mixed, small_prefix, small_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -91,6 +91,12 @@ SMALL = {
         "chunk170_g3", [W.SeqSpec(200, 170), W.SeqSpec(90, 1), W.SeqSpec(300, 40)],
         num_q_heads=6, num_kv_heads=2, head_dim=64, block_size=16, seed_base=9213),
     "mixed_d128_bs32_g6": lambda: small_mixed(bs=32, hq=12, hkv=2, seed=9212),
+    # long contexts, beside decode rows (launch slices) and alone
+    "long_d128_bs16_g4": lambda: small_long_chunks(),
+    "long_d64_bs32_g8": lambda: small_long_chunks(d=64, bs=32, hq=16, hkv=2, seed=9501),
+    "long_alone_d128_bs16_g4": lambda: small_long_chunks(seed=9503, decode=False),
+    "long_alone_d64_bs32_g8": lambda: small_long_chunks(d=64, bs=32, hq=16, hkv=2, seed=9504,
+                                                        decode=False),
 }
 
 
