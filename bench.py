@@ -103,13 +103,15 @@ def algorithmic_bytes(b, sp: int = 0) -> dict:
         return (uniq + 2 * rows * b.num_q_heads * d * 2 +
                 int(((lens[idx] + bs - 1) // bs).sum()) * 4 + desc)
 
-    dec, pre = qlens == 1, qlens > 1
+    # the decode kernel serves one-row sequences, and every sequence on the verify path
+    dec = (qlens >= 1) if verify_path(b) else (qlens == 1)
+    pre = (qlens > 1) & ~dec
     return {
         "kv_logical": kv_logical, "kv_unique": kv_unique,
         "attention_logical": kv_logical + attn, "attention_unique": kv_unique + attn,
         "reshape_and_cache": cache,
         "step_logical": kv_logical + attn + cache,
-        "decode_rows": int(dec.sum()),
+        "decode_rows": int((qlens == 1).sum()),
         "flops": flops(active),
         # what each attention kernel must move / compute: the decode-partition kernel serves the
         # one-row sequences, the chunked-prefill kernel the sequences with several rows
@@ -125,9 +127,17 @@ def algorithmic_bytes(b, sp: int = 0) -> dict:
     }
 
 
+def verify_path(b) -> bool:
+    """pa_attention serves every row with the decode kernel when each sequence has at most a
+    few query rows: max_query_len x G <= 8 columns, or <= 32 over an FP8 cache."""
+    cols = b.max_query_len * (b.num_q_heads // b.num_kv_heads)
+    return b.max_query_len > 1 and (cols <= 8 or (b.kv_dtype == "e4m3" and cols <= 32))
+
+
 def all_prefill(b) -> bool:
-    """Every sequence has several query rows: pa_attention then makes no decode launches."""
-    return b.max_query_len > 1 and b.num_prefill_seqs == b.num_seqs
+    """Every sequence has several query rows and the prefill kernel serves them: pa_attention
+    then makes no decode launches."""
+    return not verify_path(b) and b.max_query_len > 1 and b.num_prefill_seqs == b.num_seqs
 
 
 def launches_per_step(b, sp: int = 0) -> int:
@@ -135,7 +145,8 @@ def launches_per_step(b, sp: int = 0) -> int:
     decode = not all_prefill(b)
     n = 1 if b.k_new.shape[0] > 0 else 0        # reshape_and_cache
     n += 1 if decode else 0                       # decode partitions
-    n += 1 if b.max_query_len > 1 else 0          # chunked-prefill tiles
+    prefill = b.max_query_len > 1 and not verify_path(b)
+    n += 1 if prefill else 0                      # chunked-prefill tiles
     n += 1 if parts > 1 and decode else 0         # log-sum-exp merge
     n += 1 if sp else 0                           # shared-prefix pass
     return n
@@ -300,7 +311,8 @@ def run_ours(args, world, rank, local):
 
     # -------- device-resident timed region: exactly K steps, nothing between the step events
     # but the step itself
-    timed = (([] if all_prefill(b) else ["decode"]) + (["prefill"] if b.max_query_len > 1 else [])
+    timed = (([] if all_prefill(b) else ["decode"])
+             + (["prefill"] if b.max_query_len > 1 and not verify_path(b) else [])
              + (["shared_prefix"] if sp else []))
     mk = lambda: torch.cuda.Event(enable_timing=True)
     ev = [(mk(), mk()) for _ in range(args.steps)]

@@ -407,8 +407,18 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
   if (hint->max_query_len > hint->max_seq_len)
     return fail(PA_ERR_INVALID_ARG, "hint max_query_len exceeds max_seq_len");
   if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN");
-  if (fp8 && hint->max_query_len > 1)
-    return fail(PA_ERR_UNSUPPORTED, "prefill rows over an FP8 cache are not built (decode only)");
+  // Verify rows: when every sequence has at most a few query rows, the decode kernel can serve
+  // them all, each column (query row, head) with its own causal limit: one read of a 512-key
+  // partition feeds every column, and no prefill launch is made.  It does so for up to 8
+  // columns (where a 128-row prefill tile would be mostly empty), and over an FP8 cache (which
+  // the prefill kernels do not read) for up to 32.  Between 8 and 32 columns over fp16/bf16 the
+  // key-parity prefill kernel is as fast and needs no merge.
+  const int64_t group_size = hq % hkv == 0 && hkv > 0 ? hq / hkv : 1;
+  const int64_t verify_cols = hint->max_query_len * group_size;
+  const bool verify = hint->max_query_len > 1 && (verify_cols <= 8 || (fp8 && verify_cols <= 32));
+  if (fp8 && hint->max_query_len > 1 && !verify)
+    return fail(PA_ERR_UNSUPPORTED,
+                "over an FP8 cache only decode and verify rows (q_len x G <= 32) are built");
   const WorkspaceLayout ws = workspace_layout(t, hq, d, hint->max_seq_len);
   if (ws.total > 0) {
     if (!workspace || workspace_bytes < ws.total)
@@ -443,9 +453,13 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
       std::max<int64_t>(1, (hint->max_seq_len + PA_PARTITION_TOKENS - 1) / PA_PARTITION_TOKENS));
   a.max_query_len = hint->max_query_len;
   a.prefill_seqs = hint->num_prefill_seqs > 0 ? std::min<int>(hint->num_prefill_seqs, n) : n;
-  // Every sequence has several rows (by the hint): no decode rows, so no decode or merge launch.
-  const bool all_prefill = hint->max_query_len > 1 && hint->num_prefill_seqs >= n;
+  // Every sequence has several rows (by the hint) and the prefill kernel serves them: no decode
+  // rows, so no decode or merge launch.
+  const bool all_prefill = !verify && hint->max_query_len > 1 && hint->num_prefill_seqs >= n;
   a.decode_skipped = all_prefill ? 1 : 0;
+  a.verify_rows = verify ? hint->max_query_len : 1;
+  const int cols_per_cta = group * a.verify_rows <= 8 ? 8 : 16;
+  a.col_groups = static_cast<int>((group * a.verify_rows + cols_per_cta - 1) / cols_per_cta);
   // FP8: K = k_scale * code value, so the score scale takes k_scale; V's scale goes on the output.
   a.scale_log2 = scale * 1.4426950408889634f * (fp8 ? sc->k_scale : 1.f);
   a.v_scale = fp8 ? sc->v_scale : 1.f;
@@ -490,7 +504,7 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
     }
     ~Join() { done(); }
   } join;
-  if (!all_prefill && hint->max_query_len > 1) {
+  if (!all_prefill && !verify && hint->max_query_len > 1) {
     if ((e = device_sm_count(&a.num_sms)) != cudaSuccess) return cuda_fail(e, "device attribute");
     a.prefill_ctas = prefill_ctas_beside_decode(a.num_sms);
     SideStream* side = nullptr;

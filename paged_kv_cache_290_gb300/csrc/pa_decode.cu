@@ -73,7 +73,9 @@ __device__ __forceinline__ uint32_t ldg_u32(const __half* p) {
 // What the pools hold: fp16, E4M3 codes (with fp16 q/out), or bf16 (with bf16 q/out).
 enum KvKind : int { kKvF16 = 0, kKvE4M3 = 1, kKvBF16 = 2 };
 
-template <int D, int BS, int NT, int KV>
+// CAUSAL: the launch serves verify rows (several query rows per sequence), each column with its
+// own causal limit; without it every column sees all L keys (decode rows only).
+template <int D, int BS, int NT, int KV, bool CAUSAL>
 __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
     decode_partition_kernel(const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
@@ -85,30 +87,42 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  // Partitions inside a shared prefix belong to the shared-prefix pass and get no CTA here.
-  const int part = blockIdx.x + a.cascade_parts, g = blockIdx.y, s = blockIdx.z;
+  // Grid x = (partition, column group), column group fastest so the CTAs that read the same
+  // partition run side by side.  A column is one (query row, head of the group) pair, row-major;
+  // a CTA serves 8 * NT of the sequence's q_len * G columns.  Partitions inside a shared prefix
+  // belong to the shared-prefix pass and get no CTA here.
+  const int ncg = a.col_groups;
+  const int cg = static_cast<int>(blockIdx.x) % ncg;
+  const int pidx = static_cast<int>(blockIdx.x) / ncg;
+  const int part = pidx + a.cascade_parts, g = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool lead = blockIdx.x == 0;  // reports the sequence's descriptor errors
   grid_dependency_wait();  // everything the previous kernels wrote is visible from here on
   grid_launch_dependents();
 
   const int row0 = a.query_start_loc[s];
   const int q_len = a.query_start_loc[s + 1] - row0;
-  if (q_len != 1) return;  // prefill chunks and idle sequences are not decode work
+  // decode rows, and verify rows (a few per sequence) when the call routes them here
+  if (q_len < 1 || q_len > a.verify_rows) return;
   if (row0 < 0 || row0 + q_len > a.num_tokens) {
-    if (blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
+    if (lead && tid == 0) atomicOr(a.err, kErrDescriptor);
     return;
   }
   const int L = a.seq_lens[s];
   const int nparts = (L + kPartitionTokens - 1) / kPartitionTokens;
-  if (L < 1 || (L + BS - 1) / BS > a.max_blocks) {
-    if (blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrDescriptor);
+  if (L < q_len || (L + BS - 1) / BS > a.max_blocks) {
+    if (lead && tid == 0) atomicOr(a.err, kErrDescriptor);
     return;
   }
-  if (nparts > static_cast<int>(gridDim.x) + a.cascade_parts) {
-    if (blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrHint);
+  if (nparts > static_cast<int>(gridDim.x) / ncg + a.cascade_parts ||
+      (q_len * a.group + 8 * NT - 1) / (8 * NT) > ncg) {
+    if (lead && tid == 0) atomicOr(a.err, kErrHint);
     return;
   }
-  if (a.cascade_parts > 0 && blockIdx.x == 0 && g == 0) {
+  const int ncols = q_len * a.group, col0 = cg * 8 * NT;
+  if (col0 >= ncols) return;
+  const int ctx = L - q_len;  // row i sees keys 0 .. ctx + i
+  if (a.cascade_parts > 0 && pidx == 0 && cg == 0 && g == 0) {
     // With a shared prefix, the row must have keys past it, and its table must hold sequence
     // 0's blocks inside it (the blocks the shared-prefix pass reads for every row).
     int differs = L <= a.cascade_parts * kPartitionTokens;
@@ -172,15 +186,16 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
     for (int i = 0; i < n0; ++i) issue(i);
   }
 
-  // Q^T as the B operand (k = head_dim, n = the group's heads), kept in registers.
+  // Q^T as the B operand (k = head_dim, n = this CTA's columns), kept in registers.
   const int gq = lane >> 2, cq = lane & 3;
   uint32_t qf[NT][C::kDK][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int hg = nt * 8 + gq;
-    const bool hv = hg < a.group;
-    const __half* qrow = a.q + static_cast<int64_t>(row0) * a.q_stride +
-                         static_cast<int64_t>(g * a.group + (hv ? hg : 0)) * D;
+    const int c = col0 + nt * 8 + gq;
+    const bool hv = c < ncols;
+    const int qi = hv ? c / a.group : 0, hg = hv ? c % a.group : 0;
+    const __half* qrow = a.q + static_cast<int64_t>(row0 + qi) * a.q_stride +
+                         static_cast<int64_t>(g * a.group + hg) * D;
 #pragma unroll
     for (int j = 0; j < C::kDK; ++j) {
       // FP8: k positions (2cq, 2cq+1 | 2cq+8, 2cq+9) hold dims (4cq, 4cq+1 | 4cq+2, 4cq+3)
@@ -188,6 +203,17 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
       qf[nt][j][1] = hv ? ldg_u32(qrow + j * 16 + (F8 ? 4 * cq + 2 : 8 + 2 * cq)) : 0u;
     }
   }
+
+  // Last key position each of this lane's accumulator columns (2cq, 2cq + 1 of each 8) may see:
+  // the causal limit of its query row (L - 1 for a decode row; columns past ncols see all).
+  int lim[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int c = col0 + nt * 8 + 2 * cq + e;
+      lim[nt][e] = c < ncols ? ctx + c / a.group : L - 1;
+    }
 
   float o[NT][C::kDK][4];
   float m_run[NT][2], l_run[NT][2];
@@ -245,15 +271,18 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
       }
     }
 
-    // ---- online softmax over the unit (per head; this lane holds heads 2cq, 2cq+1)
+    // ---- online softmax over the unit (per column; this lane holds columns 2cq, 2cq+1)
+    const int kp0 = tok_begin + u * 16 + gq, kp1 = kp0 + 8;  // key positions of rows gq, gq+8
     const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
     uint32_t pb0[NT], pb1[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float s00 = v0 ? sacc[nt][0] * a.scale_log2 : -INFINITY;
-      const float s01 = v0 ? sacc[nt][1] * a.scale_log2 : -INFINITY;
-      const float s10 = v1 ? sacc[nt][2] * a.scale_log2 : -INFINITY;
-      const float s11 = v1 ? sacc[nt][3] * a.scale_log2 : -INFINITY;
+      const bool c00 = !CAUSAL || kp0 <= lim[nt][0], c01 = !CAUSAL || kp0 <= lim[nt][1];
+      const bool c10 = !CAUSAL || kp1 <= lim[nt][0], c11 = !CAUSAL || kp1 <= lim[nt][1];
+      const float s00 = v0 && c00 ? sacc[nt][0] * a.scale_log2 : -INFINITY;
+      const float s01 = v0 && c01 ? sacc[nt][1] * a.scale_log2 : -INFINITY;
+      const float s10 = v1 && c10 ? sacc[nt][2] * a.scale_log2 : -INFINITY;
+      const float s11 = v1 && c11 ? sacc[nt][3] * a.scale_log2 : -INFINITY;
       float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
       mx0 = warp_max_xor(mx0, 4);
       mx1 = warp_max_xor(mx1, 4);
@@ -262,11 +291,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
       mx0 = warp_max_xor(mx0, 16);
       mx1 = warp_max_xor(mx1, 16);
       const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-      const float al0 = exp2f(m_run[nt][0] - mn0), al1 = exp2f(m_run[nt][1] - mn1);
+      // a verify column with no visible key yet keeps m = -inf; subtract 0 then, so p = 0, not
+      // NaN (a decode column sees a key in every unit it processes)
+      const float b0 = CAUSAL && mn0 == -INFINITY ? 0.f : mn0;
+      const float b1 = CAUSAL && mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2f(m_run[nt][0] - b0), al1 = exp2f(m_run[nt][1] - b1);
       m_run[nt][0] = mn0;
       m_run[nt][1] = mn1;
-      const float p00 = exp2f(s00 - mn0), p10 = exp2f(s10 - mn0);
-      const float p01 = exp2f(s01 - mn1), p11 = exp2f(s11 - mn1);
+      const float p00 = exp2f(s00 - b0), p10 = exp2f(s10 - b0);
+      const float p01 = exp2f(s01 - b1), p11 = exp2f(s11 - b1);
       l_run[nt][0] = l_run[nt][0] * al0 + (p00 + p10);
       l_run[nt][1] = l_run[nt][1] * al1 + (p01 + p11);
 #pragma unroll
@@ -378,51 +411,60 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
   // A warp that timed out has set the error word; the whole CTA then leaves its outputs alone.
   if (__syncthreads_or(failed_at >= 0)) return;
 
-  for (int idx = tid; idx < a.group * D; idx += C::kThreads) {
-    const int h = idx / D, d = idx % D;
+  const int my_cols = min(8 * NT, ncols - col0);
+  for (int idx = tid; idx < my_cols * D; idx += C::kThreads) {
+    const int h = idx / D, d = idx % D;  // h: the CTA's column
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, sm_m[w * H + h]);
+    const float base = M == -INFINITY ? 0.f : M;  // the row sees no key of this partition
     float wsum = 0.f, osum = 0.f;
 #pragma unroll
     for (int w = 0; w < C::kWarps; ++w) {
-      const float f = exp2f(sm_m[w * H + h] - M);
+      const float f = exp2f(sm_m[w * H + h] - base);
       wsum += f * sm_l[w * H + h];
       osum += f * sm_o[(w * H + h) * D + d];
     }
-    const int hq = g * a.group + h;
-    const int64_t orow = static_cast<int64_t>(row0) * a.num_q_heads + hq;
+    const int c = col0 + h;
+    const int hq = g * a.group + c % a.group;
+    const int64_t orow = static_cast<int64_t>(row0 + c / a.group) * a.num_q_heads + hq;
     if (nparts == 1) {
       store_elem<BF>(a.out + orow * D + d, osum / wsum * a.v_scale);
     } else {
-      const int64_t pidx = orow * a.max_parts + part;
-      a.part_o[pidx * D + d] = osum / wsum * a.v_scale;
+      const int64_t pi = orow * a.max_parts + part;
+      a.part_o[pi * D + d] = wsum > 0.f ? osum / wsum * a.v_scale : 0.f;
       if (d == 0) {
-        a.part_m[pidx] = M;
-        a.part_l[pidx] = wsum;
+        a.part_m[pi] = M;
+        a.part_l[pi] = wsum;
       }
     }
   }
 }
 
-// One warp per (decode row, query head): combine the row's partitions.  Two dependent memory
-// rounds: the row's descriptor (query_start_loc and seq_lens together), then every partition's
-// m and l with the first 16 partitions' O rows, all in flight at once.
+// One warp per (query row, head) of the rows the decode kernel served (grid z = row of the
+// sequence): combine the row's partitions.  Two dependent memory rounds: the row's descriptor
+// (query_start_loc and seq_lens together), then every partition's m and l with the first 16
+// partitions' O rows, all in flight at once.  A partition past a verify row's causal limit
+// holds l = 0, O = 0 and weighs nothing.
 template <int D, bool BF>
 __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a) {
   grid_dependency_wait();  // the partials come from the decode kernel just before
   grid_launch_dependents();
-  const int s = blockIdx.y;
+  const int s = blockIdx.y, qi = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.x * 4 + warp;
   if (hq >= a.num_q_heads) return;
   const int row0 = a.query_start_loc[s], row1 = a.query_start_loc[s + 1];
   const int L = a.seq_lens[s];
-  if (row1 - row0 != 1 || row0 < 0 || row0 + 1 > a.num_tokens) return;
+  const int q_len = row1 - row0;
+  if (q_len < 1 || q_len > a.verify_rows || qi >= q_len || row0 < 0 || row1 > a.num_tokens ||
+      L < q_len)
+    return;
   const int nparts = (L + kPartitionTokens - 1) / kPartitionTokens;
   if (nparts <= 1 || nparts > a.max_parts || (L + a.block_size - 1) / a.block_size > a.max_blocks)
     return;
-  const int64_t base = (static_cast<int64_t>(row0) * a.num_q_heads + hq) * a.max_parts;
+  const int row = row0 + qi;
+  const int64_t base = (static_cast<int64_t>(row) * a.num_q_heads + hq) * a.max_parts;
 
   constexpr int V = D / 32;   // output elements per lane
   constexpr int kBatch = 16;  // partitions whose O rows are in flight at once
@@ -489,7 +531,7 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a)
       }
     }
   }
-  __half* dst = a.out + (static_cast<int64_t>(row0) * a.num_q_heads + hq) * D + lane * V;
+  __half* dst = a.out + (static_cast<int64_t>(row) * a.num_q_heads + hq) * D + lane * V;
   const float inv = 1.f / wsum;
   if constexpr (V == 4) {
     uint2 pk;
@@ -501,15 +543,15 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a)
   }
 }
 
-template <int D, int BS, int NT, int KV>
+template <int D, int BS, int NT, int KV, bool CAUSAL>
 cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t stream) {
   using C = DecodeCfg<D, BS, NT, KV == kKvE4M3>;
-  auto kern = decode_partition_kernel<D, BS, NT, KV>;
+  auto kern = decode_partition_kernel<D, BS, NT, KV, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.max_parts - a.cascade_parts, a.num_kv_heads, a.num_seqs);
+  dim3 grid((a.max_parts - a.cascade_parts) * a.col_groups, a.num_kv_heads, a.num_seqs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(C::kThreads);
@@ -526,8 +568,12 @@ cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CU
 template <int D, int BS, int KV>
 cudaError_t launch_decode_g(const AttnArgs& a, const CUtensorMap& k, const CUtensorMap& v,
                             cudaStream_t st) {
-  return a.group <= 8 ? launch_decode_t<D, BS, 1, KV>(a, k, v, st)
-                      : launch_decode_t<D, BS, 2, KV>(a, k, v, st);
+  // 8 columns per CTA while the widest sequence's q_len x G fits, else 16 per CTA
+  if (a.verify_rows > 1)
+    return a.group * a.verify_rows <= 8 ? launch_decode_t<D, BS, 1, KV, true>(a, k, v, st)
+                                        : launch_decode_t<D, BS, 2, KV, true>(a, k, v, st);
+  return a.group <= 8 ? launch_decode_t<D, BS, 1, KV, false>(a, k, v, st)
+                      : launch_decode_t<D, BS, 2, KV, false>(a, k, v, st);
 }
 
 template <int D, int BS>
@@ -551,7 +597,7 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
 
 cudaError_t launch_merge(const AttnArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.num_q_heads + 3) / 4, a.num_seqs);
+  cfg.gridDim = dim3((a.num_q_heads + 3) / 4, a.num_seqs, a.verify_rows);
   cfg.blockDim = dim3(128);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -59,6 +59,9 @@ struct AttnArgs {
   int bf16;          // 1: q, out and the pools are bfloat16 (else fp16)
   int cascade_parts; // leading 512-key partitions every sequence shares (attended once for all)
   int num_sms;       // SMs of the device (launch-shape choices)
+  int verify_rows;   // the decode kernel and its merge serve sequences with 1 .. verify_rows
+                     //   query rows (1: decode rows only)
+  int col_groups;    // decode CTAs per (sequence, kv head, partition): ceil(rows x G / columns)
   int items_x;       // > 0: the two-tile prefill kernel runs as launches over slices of its
                      //   items (x q-tile pairs per (kv head, sequence)); 0: one full grid
   int item_base;     // first item of such a launch

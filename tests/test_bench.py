@@ -110,8 +110,18 @@ def test_spec_verify_shapes_and_launches():
     q = [s.query_len for s in b.seqs]
     assert len(q) == 64 and min(q) >= 2 and max(q) <= 6 and b.num_prefill_seqs == 64
     assert all(512 + s.query_len <= s.seq_len <= 4096 + s.query_len for s in b.seqs)
-    assert bench.launches_per_step(b) == 2  # scatter, verify tiles (no decode rows: no decode/merge)
+    # q_len x G <= 6 x 4 = 24 columns: over fp16 the key-parity prefill kernel serves them
+    # (scatter, verify tiles; no decode launch); over FP8 the decode kernel does (scatter,
+    # partitions, merge) and moves all the attention bytes
+    assert not bench.verify_path(b) and bench.all_prefill(b)
+    assert bench.launches_per_step(b) == 2
     assert bench.algorithmic_bytes(b)["decode_rows"] == 0
+    f8 = W.to_fp8(b)
+    assert bench.verify_path(f8) and not bench.all_prefill(f8)
+    assert bench.launches_per_step(f8) == 3
+    n = bench.algorithmic_bytes(f8)
+    assert n["decode_rows"] == 0 and n["prefill_kernel_bytes"] == 0
+    assert n["decode_kernel_bytes"] == n["attention_unique"]
     sp = small_spec()
     assert {s.query_len for s in sp.seqs if s.query_len > 1} == {2, 3, 4, 5, 6}
 

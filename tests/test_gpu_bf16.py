@@ -92,6 +92,11 @@ CASES = {
     # long contexts, beside decode rows and alone
     "long_d128_bs16_g4": (lambda: small_long_chunks(seed=9502), 0),
     "long_alone_d128_bs16_g4": (lambda: small_long_chunks(seed=9505, decode=False), 0),
+    # verify rows of at most q_len x G = 8 columns: the decode kernel with causal limits
+    "verify_d128_bs16_g2": (lambda: W.build_batch(
+        "bf16_verify", [W.SeqSpec(L, q) for L, q in [(3, 3), (600, 4), (1030, 2), (77, 1),
+                                                     (4, 4), (2000, 3)]],
+        num_q_heads=16, num_kv_heads=8, head_dim=128, block_size=16, seed_base=9606), 0),
 }
 
 

@@ -13,7 +13,7 @@ import oracle
 import paged_kv_cache_290_gb300 as pa
 from paged_kv_cache_290_gb300 import binding as Bd
 from paged_kv_cache_290_gb300 import workloads as W
-from _cases import small_decode, small_mixed
+from _cases import small_decode, small_mixed, small_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -104,6 +104,36 @@ def test_fp8_decode_matches_oracle(name):
 def test_fp8_full_70b_decode():
     """8 sequences of 8192 keys, 64 q / 8 kv heads, 16 partitions each: every row."""
     b = W.WORKLOADS["llama70b_8x8k_decode_fp8"]()
+    kc, vc, out = run_fp8(b)
+    rk, rv = oracle.reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
+                                          b.slot_mapping, b.k_scale, b.v_scale)
+    assert np.array_equal(_u8(kc), rk) and np.array_equal(_u8(vc), rv)
+    ref = oracle.attention_fp8(b.q, rk, rv, b.block_tables, b.seq_lens, b.query_start_loc,
+                               b.scale, b.k_scale, b.v_scale)
+    assert_close(out, ref)
+
+
+@pytest.mark.parametrize("name, make", [
+    ("spec_d128_bs16_g4", lambda: small_spec(hq=16, hkv=4, seed=9242)),
+    ("spec_d64_bs32_g2", lambda: small_spec(d=64, bs=32, hq=8, hkv=4, seed=9243)),
+])
+def test_fp8_verify_rows_match_oracle(name, make):
+    """Speculative-verify rows (q_len x G <= 32) over an FP8 cache run on the decode kernel
+    with a causal limit per query row."""
+    b = W.to_fp8(make(), k_scale=0.03, v_scale=0.02)
+    assert b.max_query_len * (b.num_q_heads // b.num_kv_heads) <= 32
+    kc, vc, out = run_fp8(b)
+    rk, rv = oracle.reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
+                                          b.slot_mapping, b.k_scale, b.v_scale)
+    assert np.array_equal(_u8(kc), rk) and np.array_equal(_u8(vc), rv)
+    ref = oracle.attention_fp8(b.q, rk, rv, b.block_tables, b.seq_lens, b.query_start_loc,
+                               b.scale, b.k_scale, b.v_scale)
+    assert_close(out, ref)
+
+
+def test_fp8_full_spec_verify():
+    """64 sequences verifying 1-5 drafts over 512-4096 keys, 32 q / 8 kv heads: every row."""
+    b = W.to_fp8(W.spec_verify())
     kc, vc, out = run_fp8(b)
     rk, rv = oracle.reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
                                           b.slot_mapping, b.k_scale, b.v_scale)

@@ -128,15 +128,22 @@ def test_zero_and_negative_scale_match_oracle(sign, d):
 
 @pytest.mark.parametrize("d, bs, hq, hkv", [(128, 16, 32, 4), (64, 32, 16, 4), (128, 32, 32, 2)])
 def test_both_prefill_kernels_match_oracle(d, bs, hq, hkv):
-    """Chunks that fit one 128-row Q tile go to the key-parity prefill kernel; a looser hint
-    (an upper bound is allowed) sends the same batch to the two-Q-tile kernel.  Both must agree
-    with the oracle."""
+    """Verify rows take one of three paths by the hint's max_query_len: the decode kernel when
+    q_len x G <= 8 (max_query_len 2, G = 4), the key-parity prefill kernel while a chunk fits
+    one 128-row Q tile, and the two-Q-tile kernel beyond (an upper bound is allowed).  All must
+    agree with the oracle."""
     b = small_spec(d=d, bs=bs, hq=hq, hkv=hkv, seed=9410 + d + bs)
+    if hq // hkv == 4:  # at most 2 rows per sequence: 8 columns, the decode kernel's share
+        b = W.build_batch("spec2", [W.SeqSpec(L, q) for L, q in
+                                    [(2, 2), (37, 2), (515, 2), (130, 1), (17, 2), (96, 2),
+                                     (1, 1), (1100, 2)]],
+                          num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                          seed_base=9415 + d)
     dev = "cuda"
     ref = oracle.attention_batch(b)
     args = [x.to(dev) for x in (b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
                                 b.query_start_loc)]
-    for max_q in (b.max_query_len, 200):
+    for max_q in (b.max_query_len, 16, 200):
         out = torch.full_like(args[0], float("nan"))
         pa.attention(*args, b.scale, out, max_q, b.max_seq_len,
                      num_prefill_seqs=b.num_prefill_seqs)
