@@ -416,9 +416,7 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
   const int64_t group_size = hq % hkv == 0 && hkv > 0 ? hq / hkv : 1;
   const int64_t verify_cols = hint->max_query_len * group_size;
   const bool verify = hint->max_query_len > 1 && (verify_cols <= 8 || (fp8 && verify_cols <= 32));
-  if (fp8 && hint->max_query_len > 1 && !verify)
-    return fail(PA_ERR_UNSUPPORTED,
-                "over an FP8 cache only decode and verify rows (q_len x G <= 32) are built");
+
   const WorkspaceLayout ws = workspace_layout(t, hq, d, hint->max_seq_len);
   if (ws.total > 0) {
     if (!workspace || workspace_bytes < ws.total)

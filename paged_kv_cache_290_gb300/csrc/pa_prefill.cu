@@ -131,7 +131,91 @@ __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap*
       mbar_wait(smem_addr(&full[j % stages]), (j / stages) & 1, a.err);
 }
 
-template <int D>
+// The same producer over an FP8 (E4M3) pool: each tile's codes (16-row TMA boxes of D bytes,
+// 128-byte swizzled for D = 128, plain 64-byte rows for D = 64) land in a one-tile staging
+// buffer; the warp then widens them into the fp16 stage (exact: every E4M3 value is an fp16
+// value) in the same 128-byte-swizzled [64-column chunk][key][128 B] layout as an fp16 tile,
+// and all 32 lanes arrive on the stage's barrier (count 32) after a proxy fence.  The next
+// tile's codes are fetched as soon as the staging buffer is read.  The scales are applied by
+// the kernel (k_scale in the score scale, v_scale on the output).
+template <int D, int BS, int kKeys>
+__device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorMap* map, int s,
+                                              int g, int kend, int ntiles, int stages,
+                                              uint64_t* full, uint64_t* empty, uint32_t ring,
+                                              uint32_t stage8, uint64_t* land, int key_base) {
+  constexpr int kUnits = kKeys / 16, kKVBytes = (D / 64) * kKeys * 128, kUnit8 = 16 * D;
+  constexpr int kChunks = D / 16;  // 16-code chunks of a key row
+  const int lane = threadIdx.x & 31;
+  auto unit_block = [&](int j) {
+    const int key0 = key_base + j * kKeys;
+    const int units = min(kUnits, (kend - key0 + 15) >> 4);
+    return lane < units
+               ? a.block_tables[static_cast<int64_t>(s) * a.bt_stride + (key0 + 16 * lane) / BS]
+               : 0;
+  };
+  const uint32_t landb = smem_addr(land);
+  auto fetch = [&](int j, int id) {  // codes of tile j -> staging, completing on `land`
+    const int key0 = key_base + j * kKeys;
+    const int units = min(kUnits, (kend - key0 + 15) >> 4);
+    if (lane == 0) mbar_arrive_expect_tx(landb, units * kUnit8);
+    for (int u = 0; u < units; ++u) {
+      const int blk = __shfl_sync(0xffffffffu, id, u);
+      if (lane == 0)
+        tma_load_2d(stage8 + u * kUnit8, map, 0, (blk * a.num_kv_heads + g) * BS +
+                                                     ((key0 + 16 * u) % BS), landb);
+    }
+  };
+  int fetched = 0;
+  if (ntiles > 0) {
+    fetch(0, unit_block(0));
+    fetched = 1;
+  }
+  int id_next = ntiles > 1 ? unit_block(1) : 0;
+  for (int j = 0; j < ntiles; ++j) {
+    const int st = j % stages, round = j / stages;
+    const int key0 = key_base + j * kKeys;
+    const int rows = min(kUnits, (kend - key0 + 15) >> 4) * 16;
+    bool ok = mbar_wait(landb, j & 1, a.err);                  // codes of tile j landed
+    if (ok && round > 0) ok = mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const uint32_t dst = ring + st * kKVBytes;
+    for (int idx = lane; idx < rows * kChunks; idx += 32) {
+      const int k = idx / kChunks, c = idx % kChunks, r = k & 15;
+      const uint32_t src = stage8 + (k >> 4) * kUnit8 +
+                           (D == 128 ? r * 128 + ((c ^ (r & 7)) << 4) : r * 64 + c * 16);
+      uint32_t w0, w1, w2, w3;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                   : "r"(src));
+      const uint32_t h[8] = {f16x2_from_e4m3x2(w0), f16x2_from_e4m3x2(w0 >> 16),
+                             f16x2_from_e4m3x2(w1), f16x2_from_e4m3x2(w1 >> 16),
+                             f16x2_from_e4m3x2(w2), f16x2_from_e4m3x2(w2 >> 16),
+                             f16x2_from_e4m3x2(w3), f16x2_from_e4m3x2(w3 >> 16)};
+      const int e8 = (c * 16 % 64) / 8;  // first 8-column chunk of dims c*16 .. c*16+15
+      const uint32_t row = dst + (c * 16 / 64) * (kKeys * 128) + k * 128;
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         row + (((e8 + q) ^ (k & 7)) << 4)),
+                     "r"(h[4 * q]), "r"(h[4 * q + 1]), "r"(h[4 * q + 2]), "r"(h[4 * q + 3])
+                     : "memory");
+    }
+    fence_proxy_async();  // the generic stores -> visible to the MMA's shared-memory reads
+    mbar_arrive(smem_addr(&full[st]));
+    __syncwarp();         // every lane has read the staging buffer before it is refilled
+    if (j + 1 < ntiles) {
+      fetch(j + 1, id_next);
+      fetched = j + 2;
+      if (j + 2 < ntiles) id_next = unit_block(j + 2);
+    }
+  }
+  // a fetch issued but never consumed (a wait gave up) must land before the CTA retires
+  if (lane == 0 && fetched > 0) mbar_wait(landb, (fetched - 1) & 1, a.err);
+}
+
+// F8: the pool holds E4M3 codes, widened into the fp16 stages through a one-tile staging
+// buffer per tensor (so one V stage fewer).
+template <int D, bool F8 = false>
 struct PairCfg {
   static constexpr int kRows = 128;  // MMA M: (query token, head) rows of one Q tile
   static constexpr int kQTiles = 2;  // Q tiles per CTA, sharing every K/V tile
@@ -141,9 +225,10 @@ struct PairCfg {
   static constexpr int kQBytes = kHalves * kHalfBytes;    // one Q tile, [half][row][128 B]
   static constexpr int kKVBytes = kHalves * kKeys * 128;  // K (or V) tile, [half][key][128 B]
   static constexpr int kKStages = 2;
-  static constexpr int kVStages = 3;
+  static constexpr int kVStages = F8 ? 2 : 3;
+  static constexpr int kStage8Bytes = F8 ? kKeys * D : 0;  // one tile of codes
   static constexpr int kSmemBytes =
-      kQTiles * kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
+      kQTiles * kQBytes + (kKStages + kVStages) * kKVBytes + 2 * kStage8Bytes + 1024;
   static constexpr int kSoftmax = 256;                    // one warpgroup per Q tile
   static constexpr int kPerTile = 128;                    // softmax threads of one Q tile
   // + a warpgroup of K producer, V producer, MMA issuer and one idle warp
@@ -164,11 +249,11 @@ struct PairCfg {
 // row i of q), keys are the 512-key partition blockIdx.z of the prefix that every sequence
 // shares (read through sequence 0's table), no causal mask; the epilogue writes the rows'
 // partition partials (m, l, O / l) for the log-sum-exp merge instead of the output.
-template <int D, int BS, bool CASCADE, bool BF>
+template <int D, int BS, bool CASCADE, bool BF, bool F8>
 __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
-  using C = PairCfg<D>;
+  using C = PairCfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[C::kKStages], k_empty[C::kKStages];
   __shared__ __align__(8) uint64_t v_full[C::kVStages], v_empty[C::kVStages];
@@ -176,6 +261,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   // so each of these runs at most one phase ahead of its waiter (no parity ambiguity).
   __shared__ __align__(8) uint64_t s_full[C::kQTiles], p_full[C::kQTiles];
   __shared__ __align__(8) uint64_t q_full, drain;
+  __shared__ __align__(8) uint64_t land[2];  // F8: codes of the K / V tile in staging
   __shared__ uint32_t tmem_base;
   __shared__ int warp_count[C::kThreads / 32];
   __shared__ int chosen_seq;
@@ -185,6 +271,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   const uint32_t q_s = smem_addr(smem);                     // Q tiles A, B
   const uint32_t k_s = q_s + C::kQTiles * C::kQBytes;       // K ring
   const uint32_t v_s = k_s + C::kKStages * C::kKVBytes;     // V ring
+  const uint32_t f8_s = v_s + C::kVStages * C::kKVBytes;    // F8: K, V staging
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Work item (q-tile pair x, kv head g, prefill sequence z): the grid's coordinates, or, when
   // the launch is one of a series that each cover a slice of the items, item_base + blockIdx.x
@@ -272,11 +359,11 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   }
   if (tid == 0) {
     for (int st = 0; st < C::kKStages; ++st) {
-      mbar_init(smem_addr(&k_full[st]), 1);
+      mbar_init(smem_addr(&k_full[st]), F8 ? 32 : 1);
       mbar_init(smem_addr(&k_empty[st]), 1);
     }
     for (int st = 0; st < C::kVStages; ++st) {
-      mbar_init(smem_addr(&v_full[st]), 1);
+      mbar_init(smem_addr(&v_full[st]), F8 ? 32 : 1);
       mbar_init(smem_addr(&v_empty[st]), 1);
     }
     for (int t = 0; t < C::kQTiles; ++t) {
@@ -285,6 +372,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     }
     mbar_init(smem_addr(&q_full), C::kSoftmax);
     mbar_init(smem_addr(&drain), 1);
+    mbar_init(smem_addr(&land[0]), 1);
+    mbar_init(smem_addr(&land[1]), 1);
     mbar_init_fence();
   }
   tmem_fence_before_sync();
@@ -302,9 +391,16 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   if (warp == kKWarp || warp == kVWarp) {
     // ============================================================== producer warps (K, V)
     const bool is_v = warp == kVWarp;
-    produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
-                                is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
-                                is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base);
+    if constexpr (F8)
+      produce_kv_f8<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
+                                     is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
+                                     is_v ? v_empty : k_empty, is_v ? v_s : k_s,
+                                     f8_s + (is_v ? C::kStage8Bytes : 0), &land[is_v ? 1 : 0],
+                                     key_base);
+    else
+      produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
+                                  is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
+                                  is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base);
   } else if (warp == kMmaWarp && lane == 0) {
     // ============================================================== MMA issuer (one thread)
     constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0, BF);
@@ -518,7 +614,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err);
     if (CASCADE && !__any_sync(0xffffffffu, !ok)) {
       tmem_fence_after_sync();
-      const float inv = 1.f / l_run;
+      const float inv = a.v_scale / l_run;  // v_scale: 1, or the FP8 pool's V scale
       const int64_t pidx = (static_cast<int64_t>(row0 + tok) * a.num_q_heads + g * a.group + hg) *
                                a.max_parts + blockIdx.z;
       if (rv) {
@@ -541,7 +637,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       }
     } else if (!CASCADE && !__any_sync(0xffffffffu, !ok)) {
       tmem_fence_after_sync();
-      const float inv = 1.f / l_run;
+      const float inv = a.v_scale / l_run;  // v_scale: 1, or the FP8 pool's V scale
       __half* dst = a.out + (static_cast<int64_t>(row0 + tok) * a.num_q_heads + g * a.group + hg) * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -577,7 +673,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   if constexpr (CASCADE) grid_dependency_wait();
 }
 
-template <int D>
+template <int D, bool F8 = false>
 struct ParityCfg {
   static constexpr int kRows = 128;  // MMA M: (query token, head) rows of the tile
   static constexpr int kKeys = 128;  // keys per K/V tile: N of S, K of P V
@@ -585,9 +681,13 @@ struct ParityCfg {
   static constexpr int kHalfBytes = kRows * 128;          // one 64-column chunk of a 128-row tile
   static constexpr int kQBytes = kHalves * kHalfBytes;    // [half][row][128 B]
   static constexpr int kKVBytes = kHalves * kKeys * 128;  // K (or V) tile, [half][key][128 B]
-  static constexpr int kKStages = 3;
+  static constexpr int kKStages = F8 ? 2 : 3;  // F8: the staging buffers take one K stage
   static constexpr int kVStages = 2;
-  static constexpr int kSmemBytes = kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
+  static constexpr int kStage8Bytes = F8 ? kKeys * D : 0;  // one tile of codes (F8 pools)
+  static constexpr int kSmemBytes =
+      kQBytes + (kKStages + kVStages) * kKVBytes + 2 * kStage8Bytes + 1024;
+  // the kernel's static shared memory (barriers, the two parities' m and l per row) is ~2.3 KB
+  static_assert(kSmemBytes + 2560 <= 232448, "dynamic + static shared memory fit one SM");
   static constexpr int kSoftmax = 256;                    // 8 softmax warps: 2 per row quarter
   static constexpr int kParity = 128;                     // softmax threads per key-tile parity
   // + a warpgroup of K producer, V producer, MMA issuer and one idle warp
@@ -604,16 +704,17 @@ struct ParityCfg {
 
 // CASCADE: the shared-prefix pass, as in the pair kernel (rows: every query row of the batch;
 // keys: prefix partition blockIdx.z through sequence 0's table; partials out).
-template <int D, int BS, bool CASCADE, bool BF>
+template <int D, int BS, bool CASCADE, bool BF, bool F8>
 __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     prefill_parity_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
-  using C = ParityCfg<D>;
+  using C = ParityCfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[C::kKStages], k_empty[C::kKStages];
   __shared__ __align__(8) uint64_t v_full[C::kVStages], v_empty[C::kVStages];
   __shared__ __align__(8) uint64_t s_full[2], p_full[2];  // per key-tile parity
   __shared__ __align__(8) uint64_t q_full, drain;
+  __shared__ __align__(8) uint64_t land[2];  // F8: codes of the K / V tile in staging
   __shared__ uint32_t tmem_base;
   __shared__ float red_m[2][128];  // [parity][row]: running max and sum for the final merge
   __shared__ float red_l[2][128];
@@ -626,6 +727,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
   const uint32_t q_s = smem_addr(smem);
   const uint32_t k_s = q_s + C::kQBytes;                  // K ring
   const uint32_t v_s = k_s + C::kKStages * C::kKVBytes;   // V ring
+  const uint32_t f8_s = v_s + C::kVStages * C::kKVBytes;  // F8: K, V staging
   const int g = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile_q = C::kRows / a.group;  // query tokens per CTA
@@ -691,11 +793,11 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
   }
   if (tid == 0) {
     for (int st = 0; st < C::kKStages; ++st) {
-      mbar_init(smem_addr(&k_full[st]), 1);
+      mbar_init(smem_addr(&k_full[st]), F8 ? 32 : 1);
       mbar_init(smem_addr(&k_empty[st]), 1);
     }
     for (int st = 0; st < C::kVStages; ++st) {
-      mbar_init(smem_addr(&v_full[st]), 1);
+      mbar_init(smem_addr(&v_full[st]), F8 ? 32 : 1);
       mbar_init(smem_addr(&v_empty[st]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -704,6 +806,8 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     }
     mbar_init(smem_addr(&q_full), C::kSoftmax);
     mbar_init(smem_addr(&drain), 1);
+    mbar_init(smem_addr(&land[0]), 1);
+    mbar_init(smem_addr(&land[1]), 1);
     mbar_init_fence();
     softmax_stop = 0;
   }
@@ -722,9 +826,16 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
   if (warp == kKWarp || warp == kVWarp) {
     // ============================================================== producer warps (K, V)
     const bool is_v = warp == kVWarp;
-    produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
-                                is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
-                                is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base);
+    if constexpr (F8)
+      produce_kv_f8<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
+                                     is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
+                                     is_v ? v_empty : k_empty, is_v ? v_s : k_s,
+                                     f8_s + (is_v ? C::kStage8Bytes : 0), &land[is_v ? 1 : 0],
+                                     key_base);
+    else
+      produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
+                                  is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
+                                  is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base);
   } else if (warp == kMmaWarp && lane == 0) {
     // ============================================================== MMA issuer (one thread)
     // Issuing a tcgen05.mma waits until the pipe takes it and the pipe queues almost nothing,
@@ -916,7 +1027,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     const float mm = fmaxf(m_e, m_o);
     const float w_e = ex2_approx(m_e - mm), w_o = two ? ex2_approx(m_o - mm) : 0.f;
     const float l_all = red_l[0][r] * w_e + (two ? red_l[1][r] * w_o : 0.f);
-    const float inv = 1.f / l_all;
+    const float inv = a.v_scale / l_all;  // v_scale: 1, or the FP8 pool's V scale
     bool ok = !*reinterpret_cast<volatile int*>(&softmax_stop);
     if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err);
     if (CASCADE && !__any_sync(0xffffffffu, !ok)) {
@@ -1048,14 +1159,14 @@ cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const
 // Chunks that fit one Q tile (speculative verify, short chunks) go to the parity kernel, which
 // splits their key tiles between two softmax warpgroups; longer chunks to the pair kernel,
 // which gives each warpgroup its own Q tile and shares every K/V tile between them.
-template <int D, int BS, bool BF>
+template <int D, int BS, bool BF, bool F8>
 cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
   if (a.max_query_len <= ParityCfg<D>::kRows / a.group)
-    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, false, BF>, a, kmap, vmap, 1,
-                                    stream);
-  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, false, BF>, a, kmap, vmap,
-                                PairCfg<D>::kQTiles, stream, false, true);
+    return launch_one<ParityCfg<D, F8>>(prefill_parity_kernel<D, BS, false, BF, F8>, a, kmap,
+                                        vmap, 1, stream);
+  return launch_one<PairCfg<D, F8>>(prefill_pair_kernel<D, BS, false, BF, F8>, a, kmap, vmap,
+                                    PairCfg<D>::kQTiles, stream, false, true);
 }
 
 // The shared-prefix pass does 4 key tiles per CTA.  While the pair kernel's grid would leave
@@ -1068,9 +1179,9 @@ cudaError_t launch_cascade_t(const AttnArgs& a, const CUtensorMap& kmap, const C
   const int64_t pair_ctas = (a.num_tokens + rows_pair - 1) / rows_pair * a.num_kv_heads *
                             a.cascade_parts;
   if (pair_ctas < a.num_sms)
-    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, true, BF>, a, kmap, vmap, 1,
-                                    stream, true);
-  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, true, BF>, a, kmap, vmap,
+    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, true, BF, false>, a, kmap,
+                                    vmap, 1, stream, true);
+  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, true, BF, false>, a, kmap, vmap,
                                 PairCfg<D>::kQTiles, stream, true);
 }
 
@@ -1088,14 +1199,14 @@ cudaError_t launch_shared_prefix_b(const AttnArgs& a, const CUtensorMap& kmap,
                             : launch_cascade_t<64, 32, BF>(a, kmap, vmap, stream);
 }
 
-template <bool BF>
+template <bool BF, bool F8>
 cudaError_t launch_prefill_b(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
   if (a.head_dim == 128)
-    return a.block_size == 16 ? launch_prefill_t<128, 16, BF>(a, kmap, vmap, stream)
-                              : launch_prefill_t<128, 32, BF>(a, kmap, vmap, stream);
-  return a.block_size == 16 ? launch_prefill_t<64, 16, BF>(a, kmap, vmap, stream)
-                            : launch_prefill_t<64, 32, BF>(a, kmap, vmap, stream);
+    return a.block_size == 16 ? launch_prefill_t<128, 16, BF, F8>(a, kmap, vmap, stream)
+                              : launch_prefill_t<128, 32, BF, F8>(a, kmap, vmap, stream);
+  return a.block_size == 16 ? launch_prefill_t<64, 16, BF, F8>(a, kmap, vmap, stream)
+                            : launch_prefill_t<64, 32, BF, F8>(a, kmap, vmap, stream);
 }
 
 }  // namespace
@@ -1108,8 +1219,9 @@ cudaError_t launch_shared_prefix(const AttnArgs& a, const CUtensorMap& kmap,
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            cudaStream_t stream) {
-  return a.bf16 ? launch_prefill_b<true>(a, kmap, vmap, stream)
-                : launch_prefill_b<false>(a, kmap, vmap, stream);
+  if (a.kv_fp8) return launch_prefill_b<false, true>(a, kmap, vmap, stream);
+  return a.bf16 ? launch_prefill_b<true, false>(a, kmap, vmap, stream)
+                : launch_prefill_b<false, false>(a, kmap, vmap, stream);
 }
 
 }  // namespace pa

@@ -226,7 +226,6 @@ def call_attention_fp8(lib, k_scale=0.05, v_scale=0.02, hint=(1, 100), pool_dtyp
     (dict(k_scale=float("nan")), B.PA_ERR_INVALID_ARG, "finite and > 0"),
     (dict(v_scale=float("inf")), B.PA_ERR_INVALID_ARG, "finite and > 0"),
     (dict(null_scales=True), B.PA_ERR_INVALID_ARG, "scales is NULL"),
-    (dict(hint=(16, 100)), B.PA_ERR_UNSUPPORTED, "FP8"),  # 16 rows x G 4 > 32 columns
 ])
 def test_attention_fp8_rejects_bad_arguments(lib, kw, status, text):
     assert call_attention_fp8(lib, **kw) == status

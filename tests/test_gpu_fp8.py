@@ -1,9 +1,9 @@
 """GPU parity of the FP8 (E4M3) KV cache against the oracle.
 
 The scatter-write must store exactly the oracle's codes (round to nearest even of x * (1/scale),
-saturating at +-448), bit for bit over the whole pool.  Decode attention over the FP8 pool is
-compared with the oracle's fp64 attention over the dequantised cache, under the same bar as the
-fp16 path.
+saturating at +-448), bit for bit over the whole pool.  Decode, verify and prefill attention over
+the FP8 pool are compared with the oracle's fp64 attention over the dequantised cache, under the
+same bar as the fp16 path.
 """
 import numpy as np
 import pytest
@@ -13,7 +13,7 @@ import oracle
 import paged_kv_cache_290_gb300 as pa
 from paged_kv_cache_290_gb300 import binding as Bd
 from paged_kv_cache_290_gb300 import workloads as W
-from _cases import small_decode, small_mixed, small_spec
+from _cases import small_decode, small_long_chunks, small_mixed, small_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -143,8 +143,46 @@ def test_fp8_full_spec_verify():
     assert_close(out, ref)
 
 
-def test_fp8_prefill_is_refused():
-    b = W.to_fp8(small_mixed(hq=16, hkv=4, seed=9241))
-    with pytest.raises(Bd.PAError) as ex:
-        run_fp8(b, write=False)
-    assert ex.value.status == Bd.PA_ERR_UNSUPPORTED
+PREFILL = {
+    # chunks longer than one Q tile (two-tile kernel) next to decode rows
+    "mixed_d128_bs16_g4": lambda: small_mixed(hq=16, hkv=4, seed=9241),
+    "mixed_d64_bs32_g8": lambda: small_mixed(d=64, bs=32, hq=16, hkv=2, seed=9244),
+    # verify rows past 32 columns (key-parity kernel)
+    "spec_d128_bs16_g8": lambda: small_spec(seed=9245),
+    # long contexts, chunks alone
+    "long_alone_d128_bs16_g4": lambda: small_long_chunks(seed=9246, decode=False),
+}
+
+
+@pytest.mark.parametrize("name", list(PREFILL))
+def test_fp8_prefill_matches_oracle(name):
+    """Prefill chunks over an FP8 pool: the prefill kernels widen each K/V tile of codes into
+    fp16 in shared memory (exact) and apply the scales; the bar is the fp16 one."""
+    b = W.to_fp8(PREFILL[name](), k_scale=0.03, v_scale=0.02)
+    kc, vc, out = run_fp8(b)
+    rk, rv = oracle.reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
+                                          b.slot_mapping, b.k_scale, b.v_scale)
+    assert np.array_equal(_u8(kc), rk) and np.array_equal(_u8(vc), rv)
+    ref = oracle.attention_fp8(b.q, rk, rv, b.block_tables, b.seq_lens, b.query_start_loc,
+                               b.scale, b.k_scale, b.v_scale)
+    assert_close(out, ref)
+
+
+def test_fp8_full_mixed_step_sampled_rows():
+    """The mixed step over an FP8 pool: every decode row and a seeded sample of each chunk's
+    rows (with its first and last)."""
+    b = W.to_fp8(W.mixed_step(16))
+    kc, vc, out = run_fp8(b)
+    rk, rv = oracle.reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
+                                          b.slot_mapping, b.k_scale, b.v_scale)
+    assert np.array_equal(_u8(kc), rk) and np.array_equal(_u8(vc), rv)
+    g = torch.Generator().manual_seed(4244)
+    mask = np.zeros(b.num_tokens, dtype=np.uint8)
+    for s, spec in enumerate(b.seqs):
+        r0 = int(b.query_start_loc[s])
+        pick = torch.randperm(spec.query_len, generator=g)[:24].tolist()
+        for i in set(pick) | {0, spec.query_len - 1}:
+            mask[r0 + i] = 1
+    ref = oracle.attention_fp8(b.q, rk, rv, b.block_tables, b.seq_lens, b.query_start_loc,
+                               b.scale, b.k_scale, b.v_scale, row_mask=mask)
+    assert_close(out, ref, np.nonzero(mask)[0])
