@@ -43,9 +43,9 @@ FLUSH_BYTES = 512 << 20
 
 def shared_prefix_tokens(b) -> int:
     """Keys of the prefix every sequence shares, rounded down to whole 512-key partitions, when
-    the batch qualifies for the shared-prefix pass (fp16 cache, decode rows only); else 0."""
+    the batch qualifies for the shared-prefix pass (decode rows only); else 0."""
     sp = (int(b.meta.get("shared_prefix_len", 0)) // 512) * 512
-    ok = b.kv_dtype != "e4m3" and b.max_query_len == 1 and sp < b.max_seq_len
+    ok = b.max_query_len == 1 and sp < b.max_seq_len
     return sp if ok else 0
 
 

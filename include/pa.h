@@ -91,8 +91,7 @@ typedef struct pa_batch_hint {
                                agree there), so they are attended once for all query rows (p1:
                                requests that start alike share pages; p2 prefix-caching slide)
                                and merged with each sequence's own keys by the log-sum-exp rule.
-                               Decode rows over fp16 or bf16 caches only (else
-                               PA_ERR_UNSUPPORTED); a
+                               Decode rows only (else PA_ERR_UNSUPPORTED); a
                                sequence whose table differs there, or with no key past the
                                prefix, is reported as PA_ERR_DESCRIPTOR. */
 } pa_batch_hint;

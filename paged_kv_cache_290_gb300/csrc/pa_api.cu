@@ -400,9 +400,8 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
     if (sp >= hint->max_seq_len || sp / bs > block_tables->shape[1])
       return fail(PA_ERR_INVALID_ARG, "shared_prefix_tokens must be below max_seq_len and within "
                                       "the block tables");
-    if (fp8 || hint->max_query_len > 1)
-      return fail(PA_ERR_UNSUPPORTED, "the shared-prefix pass is built for decode rows over an "
-                                      "fp16 or bf16 cache");
+    if (hint->max_query_len > 1)
+      return fail(PA_ERR_UNSUPPORTED, "the shared-prefix pass is built for decode rows");
   }
   if (hint->max_query_len > hint->max_seq_len)
     return fail(PA_ERR_INVALID_ARG, "hint max_query_len exceeds max_seq_len");

@@ -1172,31 +1172,31 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const C
 // The shared-prefix pass does 4 key tiles per CTA.  While the pair kernel's grid would leave
 // SMs idle, one Q tile per CTA (the parity kernel: twice the CTAs, each key tile's softmax on
 // its own warpgroup) finishes sooner; past that, the pair kernel's shared K/V tiles win.
-template <int D, int BS, bool BF>
+template <int D, int BS, bool BF, bool F8>
 cudaError_t launch_cascade_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
   const int64_t rows_pair = PairCfg<D>::kQTiles * (PairCfg<D>::kRows / a.group);
   const int64_t pair_ctas = (a.num_tokens + rows_pair - 1) / rows_pair * a.num_kv_heads *
                             a.cascade_parts;
   if (pair_ctas < a.num_sms)
-    return launch_one<ParityCfg<D>>(prefill_parity_kernel<D, BS, true, BF, false>, a, kmap,
-                                    vmap, 1, stream, true);
-  return launch_one<PairCfg<D>>(prefill_pair_kernel<D, BS, true, BF, false>, a, kmap, vmap,
-                                PairCfg<D>::kQTiles, stream, true);
+    return launch_one<ParityCfg<D, F8>>(prefill_parity_kernel<D, BS, true, BF, F8>, a, kmap,
+                                        vmap, 1, stream, true);
+  return launch_one<PairCfg<D, F8>>(prefill_pair_kernel<D, BS, true, BF, F8>, a, kmap, vmap,
+                                    PairCfg<D>::kQTiles, stream, true);
 }
 
 }  // namespace
 
 namespace {
 
-template <bool BF>
+template <bool BF, bool F8>
 cudaError_t launch_shared_prefix_b(const AttnArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, cudaStream_t stream) {
   if (a.head_dim == 128)
-    return a.block_size == 16 ? launch_cascade_t<128, 16, BF>(a, kmap, vmap, stream)
-                              : launch_cascade_t<128, 32, BF>(a, kmap, vmap, stream);
-  return a.block_size == 16 ? launch_cascade_t<64, 16, BF>(a, kmap, vmap, stream)
-                            : launch_cascade_t<64, 32, BF>(a, kmap, vmap, stream);
+    return a.block_size == 16 ? launch_cascade_t<128, 16, BF, F8>(a, kmap, vmap, stream)
+                              : launch_cascade_t<128, 32, BF, F8>(a, kmap, vmap, stream);
+  return a.block_size == 16 ? launch_cascade_t<64, 16, BF, F8>(a, kmap, vmap, stream)
+                            : launch_cascade_t<64, 32, BF, F8>(a, kmap, vmap, stream);
 }
 
 template <bool BF, bool F8>
@@ -1213,8 +1213,9 @@ cudaError_t launch_prefill_b(const AttnArgs& a, const CUtensorMap& kmap, const C
 
 cudaError_t launch_shared_prefix(const AttnArgs& a, const CUtensorMap& kmap,
                                  const CUtensorMap& vmap, cudaStream_t stream) {
-  return a.bf16 ? launch_shared_prefix_b<true>(a, kmap, vmap, stream)
-                : launch_shared_prefix_b<false>(a, kmap, vmap, stream);
+  if (a.kv_fp8) return launch_shared_prefix_b<false, true>(a, kmap, vmap, stream);
+  return a.bf16 ? launch_shared_prefix_b<true, false>(a, kmap, vmap, stream)
+                : launch_shared_prefix_b<false, false>(a, kmap, vmap, stream);
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,

@@ -439,4 +439,5 @@ WORKLOADS = {
     "llama70b_8x8k_decode_bf16": lambda **kw: to_bf16(llama70b_decode(8, **kw)),
     "spec_verify_fp8": lambda **kw: to_fp8(spec_verify(**kw)),
     "mixed_step_bs16_fp8": lambda **kw: to_fp8(mixed_step(16, **kw)),
+    "prefix_shared_decode_fp8": lambda **kw: to_fp8(prefix_shared_decode(**kw)),
 }

@@ -124,15 +124,15 @@ def test_shared_prefix_hint_is_validated(lib, kw, status, text):
     assert text in msg(lib), msg(lib)
 
 
-def test_shared_prefix_refused_over_fp8(lib):
+def test_shared_prefix_with_prefill_rows_refused_over_fp8(lib):
     n, hq, hkv, d, bs, nb, mb = 3, 8, 2, 128, 16, 40, 64
     args = [ctypes.byref(x) for x in (
         T(B.PA_F16, [n, hq, d]), T(B.PA_F8E4M3, [nb, hkv, bs, d]), T(B.PA_F8E4M3, [nb, hkv, bs, d]),
         T(B.PA_I32, [n, mb]), T(B.PA_I32, [n]), T(B.PA_I32, [n + 1]))]
     r = lib.pa_attention_fp8(*args, ctypes.c_float(0.1), ctypes.byref(T(B.PA_F16, [n, hq, d])),
-                             ctypes.byref(B.PABatchHint(1, 1000, 0, 512)),
+                             ctypes.byref(B.PABatchHint(2, 1000, 0, 512)),
                              ctypes.byref(B.PAKVScales(0.5, 0.5)), None, 0, None)
-    assert r == B.PA_ERR_UNSUPPORTED and "bf16 cache" in msg(lib)
+    assert r == B.PA_ERR_UNSUPPORTED and "decode rows" in msg(lib)
 
 
 def test_timing_hook_rejects_unknown_kernel(lib):

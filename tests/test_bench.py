@@ -59,8 +59,8 @@ def test_shared_prefix_pass_splits_the_kernel_bytes():
     assert n0["decode_kernel_bytes"] - n["decode_kernel_bytes"] == sp * row
     assert n["shared_prefix_kernel_flops"] == 4 * b.num_q_heads * b.head_dim * sp * b.num_tokens
     assert bench.launches_per_step(b, sp) == bench.launches_per_step(b) + 1 == 4
-    # an FP8 cache, prefill rows or no whole shared partition: no pass
-    assert bench.shared_prefix_tokens(W.to_fp8(b)) == 0
+    # prefill rows or no whole shared partition: no pass (an FP8 cache is fine)
+    assert bench.shared_prefix_tokens(W.to_fp8(b)) == 2048
     assert bench.shared_prefix_tokens(small_prefix()) == 0
     assert bench.shared_prefix_tokens(small_mixed()) == 0
 

@@ -101,6 +101,30 @@ def test_shared_prefix_pass_matches_oracle(name):
     assert_close(plain, ref)
 
 
+@pytest.mark.parametrize("name", ["g7_d128_bs16_p512", "g8_d64_bs16_p512"])
+def test_shared_prefix_pass_over_fp8(name):
+    """Over an FP8 pool the pass widens the prefix's codes into fp16 in shared memory."""
+    n, prefix, d, bs, hq, hkv = CASES[name]
+    b = W.to_fp8(shared_case(n, prefix, d, bs, hq, hkv, seed=9700 + d), k_scale=0.03,
+                 v_scale=0.02)
+    dev = "cuda"
+    kc, vc = b.k_cache_pre.to(dev), b.v_cache_pre.to(dev)
+    pa.reshape_and_cache(b.k_new.to(dev), b.v_new.to(dev), kc, vc, b.slot_mapping.to(dev),
+                         k_scale=b.k_scale, v_scale=b.v_scale)
+    q = b.q.to(dev)
+    out = torch.full_like(q, float("nan"))
+    pa.attention(q, kc, vc, b.block_tables.to(dev), b.seq_lens.to(dev),
+                 b.query_start_loc.to(dev), b.scale, out, b.max_query_len, b.max_seq_len,
+                 shared_prefix_tokens=prefix, k_scale=b.k_scale, v_scale=b.v_scale)
+    st, bits = pa.get_device_error()
+    assert st == 0, (st, bits, pa.last_error())
+    rk, rv = oracle.reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
+                                          b.slot_mapping, b.k_scale, b.v_scale)
+    ref = oracle.attention_fp8(b.q, rk, rv, b.block_tables, b.seq_lens, b.query_start_loc,
+                               b.scale, b.k_scale, b.v_scale)
+    assert_close(out, ref)
+
+
 def test_full_prefix_shared_decode_with_the_pass():
     """160 rows behind a 2048-key prefix (4 shared partitions), 28 q / 4 kv heads: every row."""
     b = W.WORKLOADS["prefix_shared_decode"]()
