@@ -440,4 +440,5 @@ WORKLOADS = {
     "spec_verify_fp8": lambda **kw: to_fp8(spec_verify(**kw)),
     "mixed_step_bs16_fp8": lambda **kw: to_fp8(mixed_step(16, **kw)),
     "prefix_shared_decode_fp8": lambda **kw: to_fp8(prefix_shared_decode(**kw)),
+    "mixed_step_bs16_0dec_fp8": lambda **kw: to_fp8(mixed_step(16, num_decode=0, **kw)),
 }
