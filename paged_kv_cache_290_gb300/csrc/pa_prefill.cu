@@ -131,90 +131,111 @@ __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap*
       mbar_wait(smem_addr(&full[j % stages]), (j / stages) & 1, a.err);
 }
 
-// The same producer over an FP8 (E4M3) pool: each tile's codes (16-row TMA boxes of D bytes,
-// 128-byte swizzled for D = 128, plain 64-byte rows for D = 64) land in a one-tile staging
-// buffer; the warp then widens them into the fp16 stage (exact: every E4M3 value is an fp16
-// value) in the same 128-byte-swizzled [64-column chunk][key][128 B] layout as an fp16 tile,
-// and all 32 lanes arrive on the stage's barrier (count 32) after a proxy fence.  The next
-// tile's codes are fetched as soon as the staging buffer is read.  The scales are applied by
-// the kernel (k_scale in the score scale, v_scale on the output).
+// The same producer over an FP8 (E4M3) pool, with no extra shared memory: a tile's codes
+// (16-row TMA boxes of D bytes, 128-byte swizzled for D = 128, plain 64-byte rows for D = 64)
+// land in the upper half of the tile's own fp16 stage, completing on the stage's `land`
+// barrier, and the warp widens them in place (exact: every E4M3 value is an fp16 value) into
+// the 128-byte-swizzled [64-column chunk][key][128 B] layout of an fp16 tile, one key row per
+// lane.  In place is safe: for D = 128 row k's fp16 bytes cover exactly row k's own codes,
+// which its lane has loaded before it stores; for D = 64 they cover code rows 2k - 128 and
+// 2k - 127, never above k, and every lane of a pass loads its row before any lane stores.
+// Tile j + 1's copy is issued before tile j is widened, so the copy's latency overlaps the
+// widening; then a proxy fence and all 32 lanes arrive on the stage's `full` barrier (count
+// 32).  The scales are applied by the kernel (k_scale in the score scale, v_scale on the
+// output).
 template <int D, int BS, int kKeys>
 __device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorMap* map, int s,
                                               int g, int kend, int ntiles, int stages,
                                               uint64_t* full, uint64_t* empty, uint32_t ring,
-                                              uint32_t stage8, uint64_t* land, int key_base) {
+                                              uint64_t* land, int key_base) {
   constexpr int kUnits = kKeys / 16, kKVBytes = (D / 64) * kKeys * 128, kUnit8 = 16 * D;
-  constexpr int kChunks = D / 16;  // 16-code chunks of a key row
+  constexpr int kCodes = kKVBytes / 2;  // where a stage's codes land
+  constexpr int kChunks = D / 16;       // 16-code chunks of a key row
   const int lane = threadIdx.x & 31;
+  auto units_of = [&](int j) { return min(kUnits, (kend - (key_base + j * kKeys) + 15) >> 4); };
   auto unit_block = [&](int j) {
     const int key0 = key_base + j * kKeys;
-    const int units = min(kUnits, (kend - key0 + 15) >> 4);
-    return lane < units
+    return lane < units_of(j)
                ? a.block_tables[static_cast<int64_t>(s) * a.bt_stride + (key0 + 16 * lane) / BS]
                : 0;
   };
-  const uint32_t landb = smem_addr(land);
-  auto fetch = [&](int j, int id) {  // codes of tile j -> staging, completing on `land`
-    const int key0 = key_base + j * kKeys;
-    const int units = min(kUnits, (kend - key0 + 15) >> 4);
-    if (lane == 0) mbar_arrive_expect_tx(landb, units * kUnit8);
+  // tile j's codes -> the upper half of its stage, completing on land[stage]
+  auto fetch = [&](int j, int id) {
+    const int st = j % stages, key0 = key_base + j * kKeys, units = units_of(j);
+    const uint32_t bar = smem_addr(&land[st]);
+    const uint32_t dst = ring + st * kKVBytes + kCodes;
+    if (lane == 0) mbar_arrive_expect_tx(bar, units * kUnit8);
     for (int u = 0; u < units; ++u) {
       const int blk = __shfl_sync(0xffffffffu, id, u);
       if (lane == 0)
-        tma_load_2d(stage8 + u * kUnit8, map, 0, (blk * a.num_kv_heads + g) * BS +
-                                                     ((key0 + 16 * u) % BS), landb);
+        tma_load_2d(dst + u * kUnit8, map, 0,
+                    (blk * a.num_kv_heads + g) * BS + ((key0 + 16 * u) % BS), bar);
     }
   };
-  int fetched = 0;
-  if (ntiles > 0) {
-    fetch(0, unit_block(0));
-    fetched = 1;
-  }
-  int id_next = ntiles > 1 ? unit_block(1) : 0;
-  for (int j = 0; j < ntiles; ++j) {
-    const int st = j % stages, round = j / stages;
-    const int key0 = key_base + j * kKeys;
-    const int rows = min(kUnits, (kend - key0 + 15) >> 4) * 16;
-    bool ok = mbar_wait(landb, j & 1, a.err);                  // codes of tile j landed
-    if (ok && round > 0) ok = mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err);
-    if (!__all_sync(0xffffffffu, ok)) break;
+  // tile j (landed) widened in place; false when a wait gave up
+  auto widen = [&](int j) -> bool {
+    const int st = j % stages;
+    const bool ok = mbar_wait(smem_addr(&land[st]), (j / stages) & 1, a.err);
+    if (!__all_sync(0xffffffffu, ok)) return false;
     const uint32_t dst = ring + st * kKVBytes;
-    for (int idx = lane; idx < rows * kChunks; idx += 32) {
-      const int k = idx / kChunks, c = idx % kChunks, r = k & 15;
-      const uint32_t src = stage8 + (k >> 4) * kUnit8 +
-                           (D == 128 ? r * 128 + ((c ^ (r & 7)) << 4) : r * 64 + c * 16);
-      uint32_t w0, w1, w2, w3;
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                   : "r"(src));
-      const uint32_t h[8] = {f16x2_from_e4m3x2(w0), f16x2_from_e4m3x2(w0 >> 16),
-                             f16x2_from_e4m3x2(w1), f16x2_from_e4m3x2(w1 >> 16),
-                             f16x2_from_e4m3x2(w2), f16x2_from_e4m3x2(w2 >> 16),
-                             f16x2_from_e4m3x2(w3), f16x2_from_e4m3x2(w3 >> 16)};
-      const int e8 = (c * 16 % 64) / 8;  // first 8-column chunk of dims c*16 .. c*16+15
-      const uint32_t row = dst + (c * 16 / 64) * (kKeys * 128) + k * 128;
+    const int rows = units_of(j) * 16;
+    for (int k0 = 0; k0 < rows; k0 += 32) {
+      const int k = k0 + lane;
+      uint32_t w[kChunks][4];
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                         row + (((e8 + q) ^ (k & 7)) << 4)),
-                     "r"(h[4 * q]), "r"(h[4 * q + 1]), "r"(h[4 * q + 2]), "r"(h[4 * q + 3])
+      for (int c = 0; c < kChunks; ++c) {
+        const uint32_t src = dst + kCodes +
+                             (D == 128 ? k * 128 + ((c ^ (k & 7)) << 4) : k * 64 + c * 16);
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[c][0]), "=r"(w[c][1]), "=r"(w[c][2]), "=r"(w[c][3])
+                     : "r"(src)
                      : "memory");
+      }
+      if (D == 64) __syncwarp();  // rows 2k - 128, 2k - 127 may belong to other lanes
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int e8 = (c * 16 % 64) / 8;  // first 8-column chunk of dims c*16 .. c*16+15
+        const uint32_t row = dst + (c * 16 / 64) * (kKeys * 128) + k * 128;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           row + (((e8 + q) ^ (k & 7)) << 4)),
+                       "r"(f16x2_from_e4m3x2(w[c][2 * q])),
+                       "r"(f16x2_from_e4m3x2(w[c][2 * q] >> 16)),
+                       "r"(f16x2_from_e4m3x2(w[c][2 * q + 1])),
+                       "r"(f16x2_from_e4m3x2(w[c][2 * q + 1] >> 16))
+                       : "memory");
+      }
+      if (D == 64) __syncwarp();  // this pass's stores are done before the next pass loads
     }
     fence_proxy_async();  // the generic stores -> visible to the MMA's shared-memory reads
     mbar_arrive(smem_addr(&full[st]));
-    __syncwarp();         // every lane has read the staging buffer before it is refilled
-    if (j + 1 < ntiles) {
-      fetch(j + 1, id_next);
-      fetched = j + 2;
-      if (j + 2 < ntiles) id_next = unit_block(j + 2);
+    return true;
+  };
+  int fetched = 0;
+  int id_next = ntiles > 0 ? unit_block(0) : 0;
+  bool ok = true;
+  for (int j = 0; j < ntiles && ok; ++j) {
+    const int st = j % stages, round = j / stages;
+    const int id = id_next;
+    if (j + 1 < ntiles) id_next = unit_block(j + 1);
+    ok = round == 0 || mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err);
+    if (!__all_sync(0xffffffffu, ok)) {
+      ok = false;
+      break;
     }
+    fetch(j, id);
+    fetched = j + 1;
+    if (j >= 1) ok = widen(j - 1);
   }
-  // a fetch issued but never consumed (a wait gave up) must land before the CTA retires
-  if (lane == 0 && fetched > 0) mbar_wait(landb, (fetched - 1) & 1, a.err);
+  if (ok && ntiles > 0) widen(ntiles - 1);
+  // copies requested but never widened (a wait gave up) must land before the CTA retires
+  if (lane == 0)
+    for (int j = max(0, fetched - stages); j < fetched; ++j)
+      mbar_wait(smem_addr(&land[j % stages]), (j / stages) & 1, a.err);
 }
 
-// F8: the pool holds E4M3 codes, widened into the fp16 stages through a one-tile staging
-// buffer per tensor (so one V stage fewer).
+// F8: the pool holds E4M3 codes, widened in place in the fp16 stages (no extra memory).
 template <int D, bool F8 = false>
 struct PairCfg {
   static constexpr int kRows = 128;  // MMA M: (query token, head) rows of one Q tile
@@ -225,10 +246,9 @@ struct PairCfg {
   static constexpr int kQBytes = kHalves * kHalfBytes;    // one Q tile, [half][row][128 B]
   static constexpr int kKVBytes = kHalves * kKeys * 128;  // K (or V) tile, [half][key][128 B]
   static constexpr int kKStages = 2;
-  static constexpr int kVStages = F8 ? 2 : 3;
-  static constexpr int kStage8Bytes = F8 ? kKeys * D : 0;  // one tile of codes
+  static constexpr int kVStages = 3;
   static constexpr int kSmemBytes =
-      kQTiles * kQBytes + (kKStages + kVStages) * kKVBytes + 2 * kStage8Bytes + 1024;
+      kQTiles * kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
   static constexpr int kSoftmax = 256;                    // one warpgroup per Q tile
   static constexpr int kPerTile = 128;                    // softmax threads of one Q tile
   // + a warpgroup of K producer, V producer, MMA issuer and one idle warp
@@ -261,7 +281,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   // so each of these runs at most one phase ahead of its waiter (no parity ambiguity).
   __shared__ __align__(8) uint64_t s_full[C::kQTiles], p_full[C::kQTiles];
   __shared__ __align__(8) uint64_t q_full, drain;
-  __shared__ __align__(8) uint64_t land[2];  // F8: codes of the K / V tile in staging
+  __shared__ __align__(8) uint64_t land[2][3];  // F8: [K / V][stage] codes landed
   __shared__ uint32_t tmem_base;
   __shared__ int warp_count[C::kThreads / 32];
   __shared__ int chosen_seq;
@@ -271,7 +291,6 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   const uint32_t q_s = smem_addr(smem);                     // Q tiles A, B
   const uint32_t k_s = q_s + C::kQTiles * C::kQBytes;       // K ring
   const uint32_t v_s = k_s + C::kKStages * C::kKVBytes;     // V ring
-  const uint32_t f8_s = v_s + C::kVStages * C::kKVBytes;    // F8: K, V staging
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Work item (q-tile pair x, kv head g, prefill sequence z): the grid's coordinates, or, when
   // the launch is one of a series that each cover a slice of the items, item_base + blockIdx.x
@@ -372,8 +391,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     }
     mbar_init(smem_addr(&q_full), C::kSoftmax);
     mbar_init(smem_addr(&drain), 1);
-    mbar_init(smem_addr(&land[0]), 1);
-    mbar_init(smem_addr(&land[1]), 1);
+    for (int b = 0; b < 6; ++b) mbar_init(smem_addr(&land[b / 3][b % 3]), 1);
     mbar_init_fence();
   }
   tmem_fence_before_sync();
@@ -395,8 +413,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       produce_kv_f8<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
                                      is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
                                      is_v ? v_empty : k_empty, is_v ? v_s : k_s,
-                                     f8_s + (is_v ? C::kStage8Bytes : 0), &land[is_v ? 1 : 0],
-                                     key_base);
+                                     land[is_v ? 1 : 0], key_base);
     else
       produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
                                   is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
@@ -681,11 +698,9 @@ struct ParityCfg {
   static constexpr int kHalfBytes = kRows * 128;          // one 64-column chunk of a 128-row tile
   static constexpr int kQBytes = kHalves * kHalfBytes;    // [half][row][128 B]
   static constexpr int kKVBytes = kHalves * kKeys * 128;  // K (or V) tile, [half][key][128 B]
-  static constexpr int kKStages = F8 ? 2 : 3;  // F8: the staging buffers take one K stage
+  static constexpr int kKStages = 3;
   static constexpr int kVStages = 2;
-  static constexpr int kStage8Bytes = F8 ? kKeys * D : 0;  // one tile of codes (F8 pools)
-  static constexpr int kSmemBytes =
-      kQBytes + (kKStages + kVStages) * kKVBytes + 2 * kStage8Bytes + 1024;
+  static constexpr int kSmemBytes = kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
   // the kernel's static shared memory (barriers, the two parities' m and l per row) is ~2.3 KB
   static_assert(kSmemBytes + 2560 <= 232448, "dynamic + static shared memory fit one SM");
   static constexpr int kSoftmax = 256;                    // 8 softmax warps: 2 per row quarter
@@ -714,7 +729,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
   __shared__ __align__(8) uint64_t v_full[C::kVStages], v_empty[C::kVStages];
   __shared__ __align__(8) uint64_t s_full[2], p_full[2];  // per key-tile parity
   __shared__ __align__(8) uint64_t q_full, drain;
-  __shared__ __align__(8) uint64_t land[2];  // F8: codes of the K / V tile in staging
+  __shared__ __align__(8) uint64_t land[2][3];  // F8: [K / V][stage] codes landed
   __shared__ uint32_t tmem_base;
   __shared__ float red_m[2][128];  // [parity][row]: running max and sum for the final merge
   __shared__ float red_l[2][128];
@@ -727,7 +742,6 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
   const uint32_t q_s = smem_addr(smem);
   const uint32_t k_s = q_s + C::kQBytes;                  // K ring
   const uint32_t v_s = k_s + C::kKStages * C::kKVBytes;   // V ring
-  const uint32_t f8_s = v_s + C::kVStages * C::kKVBytes;  // F8: K, V staging
   const int g = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile_q = C::kRows / a.group;  // query tokens per CTA
@@ -806,8 +820,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     }
     mbar_init(smem_addr(&q_full), C::kSoftmax);
     mbar_init(smem_addr(&drain), 1);
-    mbar_init(smem_addr(&land[0]), 1);
-    mbar_init(smem_addr(&land[1]), 1);
+    for (int b = 0; b < 6; ++b) mbar_init(smem_addr(&land[b / 3][b % 3]), 1);
     mbar_init_fence();
     softmax_stop = 0;
   }
@@ -830,8 +843,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
       produce_kv_f8<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
                                      is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
                                      is_v ? v_empty : k_empty, is_v ? v_s : k_s,
-                                     f8_s + (is_v ? C::kStage8Bytes : 0), &land[is_v ? 1 : 0],
-                                     key_base);
+                                     land[is_v ? 1 : 0], key_base);
     else
       produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
                                   is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
