@@ -131,6 +131,43 @@ __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap*
       mbar_wait(smem_addr(&full[j % stages]), (j / stages) & 1, a.err);
 }
 
+// Widen, in place, key rows [32 p0, 32 p1) of a landed tile of E4M3 codes (stage at `dst`, the
+// codes in its upper half) into the tile's fp16 layout, one key row per lane (see below).
+template <int D, int kKeys>
+__device__ __forceinline__ void widen_rows_f8(uint32_t dst, int rows, int p0, int p1) {
+  constexpr int kKVBytes = (D / 64) * kKeys * 128, kCodes = kKVBytes / 2, kChunks = D / 16;
+  const int lane = threadIdx.x & 31;
+  for (int k0 = 32 * p0; k0 < rows && k0 < 32 * p1; k0 += 32) {
+    const int k = k0 + lane;
+    uint32_t w[kChunks][4];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const uint32_t src = dst + kCodes +
+                           (D == 128 ? k * 128 + ((c ^ (k & 7)) << 4) : k * 64 + c * 16);
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[c][0]), "=r"(w[c][1]), "=r"(w[c][2]), "=r"(w[c][3])
+                   : "r"(src)
+                   : "memory");
+    }
+    if (D == 64) __syncwarp();  // rows 2k - 128, 2k - 127 may belong to other lanes
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const int e8 = (c * 16 % 64) / 8;  // first 8-column chunk of dims c*16 .. c*16+15
+      const uint32_t row = dst + (c * 16 / 64) * (kKeys * 128) + k * 128;
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         row + (((e8 + q) ^ (k & 7)) << 4)),
+                     "r"(f16x2_from_e4m3x2(w[c][2 * q])),
+                     "r"(f16x2_from_e4m3x2(w[c][2 * q] >> 16)),
+                     "r"(f16x2_from_e4m3x2(w[c][2 * q + 1])),
+                     "r"(f16x2_from_e4m3x2(w[c][2 * q + 1] >> 16))
+                     : "memory");
+    }
+    if (D == 64) __syncwarp();  // this pass's stores are done before the next pass loads
+  }
+}
+
 // The same producer over an FP8 (E4M3) pool, with no extra shared memory: a tile's codes
 // (16-row TMA boxes of D bytes, 128-byte swizzled for D = 128, plain 64-byte rows for D = 64)
 // land in the upper half of the tile's own fp16 stage, completing on the stage's `land`
@@ -143,6 +180,35 @@ __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap*
 // widening; then a proxy fence and all 32 lanes arrive on the stage's `full` barrier (count
 // 32).  The scales are applied by the kernel (k_scale in the score scale, v_scale on the
 // output).
+// Passes (32 key rows each) of a 128-key tile the producer widens itself; for D = 128 a helper
+// warp widens the rest of each K and V tile (rows never overlap another row's codes there).
+template <int D>
+constexpr int kF8MainPasses = D == 128 ? 2 : 4;
+
+// The helper warp of an FP8 launch with D = 128: widens passes 2 and 3 of every K tile and every
+// V tile in the order the MMA issuer consumes them (K_j, then V_j), each after the tile's codes
+// landed, and arrives on the stage's `full` barrier (which then counts 64 arrivals).
+template <int D, int kKeys>
+__device__ __forceinline__ void widen_helper_f8(const AttnArgs& a, int kend, int ntiles,
+                                                int key_base, int k_stages, int v_stages,
+                                                uint32_t k_ring, uint32_t v_ring,
+                                                uint64_t* k_full, uint64_t* v_full,
+                                                uint64_t (*land)[3]) {
+  constexpr int kKVBytes = (D / 64) * kKeys * 128;
+  for (int j = 0; j < ntiles; ++j) {
+    const int rows = min(kKeys / 16, (kend - (key_base + j * kKeys) + 15) >> 4) * 16;
+    for (int t = 0; t < 2; ++t) {  // K, then V
+      const int stages = t == 0 ? k_stages : v_stages, st = j % stages;
+      const bool ok = mbar_wait(smem_addr(&land[t][st]), (j / stages) & 1, a.err);
+      if (!__all_sync(0xffffffffu, ok)) return;
+      widen_rows_f8<D, kKeys>((t == 0 ? k_ring : v_ring) + st * kKVBytes, rows,
+                              kF8MainPasses<D>, 4);
+      fence_proxy_async();
+      mbar_arrive(smem_addr(&(t == 0 ? k_full : v_full)[st]));
+    }
+  }
+}
+
 template <int D, int BS, int kKeys>
 __device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorMap* map, int s,
                                               int g, int kend, int ntiles, int stages,
@@ -177,37 +243,7 @@ __device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorM
     const int st = j % stages;
     const bool ok = mbar_wait(smem_addr(&land[st]), (j / stages) & 1, a.err);
     if (!__all_sync(0xffffffffu, ok)) return false;
-    const uint32_t dst = ring + st * kKVBytes;
-    const int rows = units_of(j) * 16;
-    for (int k0 = 0; k0 < rows; k0 += 32) {
-      const int k = k0 + lane;
-      uint32_t w[kChunks][4];
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const uint32_t src = dst + kCodes +
-                             (D == 128 ? k * 128 + ((c ^ (k & 7)) << 4) : k * 64 + c * 16);
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[c][0]), "=r"(w[c][1]), "=r"(w[c][2]), "=r"(w[c][3])
-                     : "r"(src)
-                     : "memory");
-      }
-      if (D == 64) __syncwarp();  // rows 2k - 128, 2k - 127 may belong to other lanes
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const int e8 = (c * 16 % 64) / 8;  // first 8-column chunk of dims c*16 .. c*16+15
-        const uint32_t row = dst + (c * 16 / 64) * (kKeys * 128) + k * 128;
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           row + (((e8 + q) ^ (k & 7)) << 4)),
-                       "r"(f16x2_from_e4m3x2(w[c][2 * q])),
-                       "r"(f16x2_from_e4m3x2(w[c][2 * q] >> 16)),
-                       "r"(f16x2_from_e4m3x2(w[c][2 * q + 1])),
-                       "r"(f16x2_from_e4m3x2(w[c][2 * q + 1] >> 16))
-                       : "memory");
-      }
-      if (D == 64) __syncwarp();  // this pass's stores are done before the next pass loads
-    }
+    widen_rows_f8<D, kKeys>(ring + st * kKVBytes, units_of(j) * 16, 0, kF8MainPasses<D>);
     fence_proxy_async();  // the generic stores -> visible to the MMA's shared-memory reads
     mbar_arrive(smem_addr(&full[st]));
     return true;
@@ -378,11 +414,11 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   }
   if (tid == 0) {
     for (int st = 0; st < C::kKStages; ++st) {
-      mbar_init(smem_addr(&k_full[st]), F8 ? 32 : 1);
+      mbar_init(smem_addr(&k_full[st]), F8 ? (D == 128 ? 64 : 32) : 1);
       mbar_init(smem_addr(&k_empty[st]), 1);
     }
     for (int st = 0; st < C::kVStages; ++st) {
-      mbar_init(smem_addr(&v_full[st]), F8 ? 32 : 1);
+      mbar_init(smem_addr(&v_full[st]), F8 ? (D == 128 ? 64 : 32) : 1);
       mbar_init(smem_addr(&v_empty[st]), 1);
     }
     for (int t = 0; t < C::kQTiles; ++t) {
@@ -486,7 +522,11 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     // Every MMA this thread issued has finished before O is read or the CTA tears down.
     umma_commit(smem_addr(&drain));
     mbar_wait(smem_addr(&drain), 0, a.err);
-  }  // warp 11 and lanes 1-31 of warp 10 have no role
+  } else if (F8 && D == 128 && warp == kMmaWarp + 1) {
+    // ============================================================== FP8 widening helper
+    widen_helper_f8<D, C::kKeys>(a, kend, ntiles, key_base, C::kKStages, C::kVStages, k_s, v_s,
+                                 k_full, v_full, land);
+  }  // lanes 1-31 of warp 10 have no role (warp 11 neither, unless it helps widen FP8 tiles)
   } else {
     // ============================================================== softmax warps 0-7
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
@@ -807,11 +847,11 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
   }
   if (tid == 0) {
     for (int st = 0; st < C::kKStages; ++st) {
-      mbar_init(smem_addr(&k_full[st]), F8 ? 32 : 1);
+      mbar_init(smem_addr(&k_full[st]), F8 ? (D == 128 ? 64 : 32) : 1);
       mbar_init(smem_addr(&k_empty[st]), 1);
     }
     for (int st = 0; st < C::kVStages; ++st) {
-      mbar_init(smem_addr(&v_full[st]), F8 ? 32 : 1);
+      mbar_init(smem_addr(&v_full[st]), F8 ? (D == 128 ? 64 : 32) : 1);
       mbar_init(smem_addr(&v_empty[st]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -891,7 +931,11 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     // Every MMA this thread issued has finished before O is read or the CTA tears down.
     umma_commit(smem_addr(&drain));
     mbar_wait(smem_addr(&drain), 0, a.err);
-  }  // warp 11 has no role
+  } else if (F8 && D == 128 && warp == kMmaWarp + 1) {
+    // ============================================================== FP8 widening helper
+    widen_helper_f8<D, C::kKeys>(a, kend, ntiles, key_base, C::kKStages, C::kVStages, k_s, v_s,
+                                 k_full, v_full, land);
+  }  // warp 11 has no role unless it helps widen FP8 tiles
   } else {
     // ============================================================== softmax warps 0-7
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
