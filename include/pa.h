@@ -151,7 +151,10 @@ size_t pa_attention_workspace_size(int64_t num_tokens, int64_t num_q_heads, int6
  * 0 .. seq_lens[s] - q_len + i (bottom-right causal; q_len = 1 attends to all keys).  Query
  * head h reads kv head h / (Hq / Hkv).  out = softmax(scale * q K^T) V per row and head.
  * Rows with q_len = 1 and more than 512 keys are computed in 512-key partitions merged with
- * the log-sum-exp rule.
+ * the log-sum-exp rule; so are verify rows (every sequence with at most a few rows: q_len x G
+ * <= 8, or <= 32 over an FP8 cache), each with its own causal limit.  Longer chunks run on the
+ * tensor-core prefill kernels, beside the decode work when the call has both (a side stream of
+ * the library's, forked from and joined back into `stream` with events).
  * Supported: d in {64, 128}, bs in {16, 32}, Hq / Hkv in 1..16.
  */
 int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
@@ -184,10 +187,10 @@ int pa_reshape_and_cache_fp8(const pa_tensor* k, const pa_tensor* v, const pa_te
 
 /*
  * pa_attention_fp8 -- pa_attention over an FP8 cache (q and out stay fp16).  Every E4M3 value
- * is exact in fp16, so the kernel converts the codes to fp16 MMA operands in registers and runs
- * the fp16 arithmetic with the score scale multiplied by k_scale and the output by v_scale.  Decode rows
- * only: a batch whose hint has max_query_len > 1 is refused with PA_ERR_UNSUPPORTED (prefill
- * over an FP8 cache is not built).  Workspace as for pa_attention.
+ * is exact in fp16, so the kernels widen the codes to fp16 (decode: into MMA operands in
+ * registers; prefill: tile by tile in shared memory) and run the fp16 arithmetic with the score
+ * scale multiplied by k_scale and the output by v_scale.  Any mix of decode, verify and prefill
+ * rows, and the shared-prefix pass, as for pa_attention.  Workspace as for pa_attention.
  */
 int pa_attention_fp8(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                      const pa_tensor* block_tables, const pa_tensor* seq_lens,
