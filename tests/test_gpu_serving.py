@@ -151,3 +151,51 @@ def test_block_manager_drives_a_serving_loop():
         del srv.toks[s]
     assert srv.add(6, system + [7, 7, 7]) == 64
     srv.step({6: 73 - 64, 1: 1})
+
+
+@pytest.mark.parametrize("make", ["mixed", "decode"])
+def test_step_replays_in_a_cuda_graph(make):
+    """A serving step (scatter-write, then attention) captured once in a CUDA graph and
+    replayed: the mixed step forks the prefill launch onto the library's side stream and joins
+    it back with events, which a capture records as a fork and a join.  The replay must give
+    the oracle's result, like an eager call."""
+    from _cases import small_decode, small_mixed
+    b = small_mixed(seed=9250) if make == "mixed" else small_decode(seed=9251)
+    dev = "cuda"
+    kc, vc = b.k_cache_pre.to(dev), b.v_cache_pre.to(dev)
+    k_new, v_new, slots = b.k_new.to(dev), b.v_new.to(dev), b.slot_mapping.to(dev)
+    q = b.q.to(dev)
+    bt, sl, qsl = b.block_tables.to(dev), b.seq_lens.to(dev), b.query_start_loc.to(dev)
+    out = torch.full_like(q, float("nan"))
+    ws = torch.empty(max(1, pa.workspace_size(b.num_tokens, b.num_q_heads, b.head_dim,
+                                              b.max_seq_len)), dtype=torch.uint8, device=dev)
+
+    def step():
+        pa.reshape_and_cache(k_new, v_new, kc, vc, slots)
+        pa.attention(q, kc, vc, bt, sl, qsl, b.scale, out, b.max_query_len, b.max_seq_len,
+                     workspace=ws, num_prefill_seqs=b.num_prefill_seqs)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up off the default stream (creates the side stream)
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    out.fill_(float("nan"))
+    kc.copy_(b.k_cache_pre.to(dev))
+    vc.copy_(b.v_cache_pre.to(dev))
+    graph.replay()
+    torch.cuda.synchronize()
+    st, bits = pa.get_device_error()
+    assert st == 0, (st, bits, pa.last_error())
+    rk, rv = oracle.reshape_and_cache(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
+                                      b.slot_mapping)
+    assert np.array_equal(_u16(kc), rk) and np.array_equal(_u16(vc), rv)
+    ref = oracle.attention_batch(b)
+    o = out.cpu().double().numpy()
+    assert np.isfinite(o).all()
+    err = np.abs(o - ref)
+    assert err.max() <= 2e-3 and np.linalg.norm(err) <= 1e-3 * np.linalg.norm(ref)
