@@ -55,6 +55,9 @@ struct DecodeCfg {
   static constexpr int kHeads = NT * 8;
   static constexpr int kMergeBytes = kWarps * kHeads * (D + 2) * 4;
   static constexpr int kSmemBytes = (kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes) + 1024;
+  // The running max is raised only past 2^8: p < 256 is exact enough in fp16 / bf16 (the same
+  // relative rounding at every magnitude) and 512 keys of it stay far from fp32 overflow.
+  static constexpr float kRaiseLog2 = 8.f;
   static_assert(kStages >= 1, "stage ring");
   static_assert(BS % 16 == 0, "block size must be a multiple of the 16-token unit");
 };
@@ -76,7 +79,7 @@ enum KvKind : int { kKvF16 = 0, kKvE4M3 = 1, kKvBF16 = 2 };
 // CAUSAL: the launch serves verify rows (several query rows per sequence), each column with its
 // own causal limit; without it every column sees all L keys (decode rows only).
 template <int D, int BS, int NT, int KV, bool CAUSAL>
-__global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
+__global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads, NT == 1 ? 4 : 0)
     decode_partition_kernel(const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
   constexpr bool F8 = KV == kKvE4M3, BF = KV == kKvBF16;
@@ -271,44 +274,65 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads)
       }
     }
 
-    // ---- online softmax over the unit (per column; this lane holds columns 2cq, 2cq+1)
+    // ---- online softmax over the unit (per column; this lane holds columns 2cq, 2cq+1).
+    // The running max m is a reference, not the exact max: it is raised (with the exact max of
+    // the columns so far, rescaling l and O) only when some score of the warp passes it by more
+    // than kRaiseLog2, so p = 2^(s - m) stays below 2^kRaiseLog2 and the usual unit needs no
+    // cross-lane reduction and no rescale.  l and O are sums against the same m, so O / l is
+    // the same quotient whatever m is.
     const int kp0 = tok_begin + u * 16 + gq, kp1 = kp0 + 8;  // key positions of rows gq, gq+8
     const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
-    uint32_t pb0[NT], pb1[NT];
+    float sc[NT][4];
+    bool raise = false;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const bool c00 = !CAUSAL || kp0 <= lim[nt][0], c01 = !CAUSAL || kp0 <= lim[nt][1];
       const bool c10 = !CAUSAL || kp1 <= lim[nt][0], c11 = !CAUSAL || kp1 <= lim[nt][1];
-      const float s00 = v0 && c00 ? sacc[nt][0] * a.scale_log2 : -INFINITY;
-      const float s01 = v0 && c01 ? sacc[nt][1] * a.scale_log2 : -INFINITY;
-      const float s10 = v1 && c10 ? sacc[nt][2] * a.scale_log2 : -INFINITY;
-      const float s11 = v1 && c11 ? sacc[nt][3] * a.scale_log2 : -INFINITY;
-      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
-      mx0 = warp_max_xor(mx0, 4);
-      mx1 = warp_max_xor(mx1, 4);
-      mx0 = warp_max_xor(mx0, 8);
-      mx1 = warp_max_xor(mx1, 8);
-      mx0 = warp_max_xor(mx0, 16);
-      mx1 = warp_max_xor(mx1, 16);
-      const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-      // a verify column with no visible key yet keeps m = -inf; subtract 0 then, so p = 0, not
-      // NaN (a decode column sees a key in every unit it processes)
-      const float b0 = CAUSAL && mn0 == -INFINITY ? 0.f : mn0;
-      const float b1 = CAUSAL && mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = exp2f(m_run[nt][0] - b0), al1 = exp2f(m_run[nt][1] - b1);
-      m_run[nt][0] = mn0;
-      m_run[nt][1] = mn1;
-      const float p00 = exp2f(s00 - b0), p10 = exp2f(s10 - b0);
-      const float p01 = exp2f(s01 - b1), p11 = exp2f(s11 - b1);
-      l_run[nt][0] = l_run[nt][0] * al0 + (p00 + p10);
-      l_run[nt][1] = l_run[nt][1] * al1 + (p01 + p11);
+      sc[nt][0] = v0 && c00 ? sacc[nt][0] * a.scale_log2 : -INFINITY;
+      sc[nt][1] = v0 && c01 ? sacc[nt][1] * a.scale_log2 : -INFINITY;
+      sc[nt][2] = v1 && c10 ? sacc[nt][2] * a.scale_log2 : -INFINITY;
+      sc[nt][3] = v1 && c11 ? sacc[nt][3] * a.scale_log2 : -INFINITY;
+      // m = -inf (no key seen yet) is passed by any visible score
+      raise |= fmaxf(sc[nt][0], sc[nt][2]) > m_run[nt][0] + C::kRaiseLog2;
+      raise |= fmaxf(sc[nt][1], sc[nt][3]) > m_run[nt][1] + C::kRaiseLog2;
+    }
+    if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
-      for (int dt = 0; dt < C::kDK; ++dt) {
-        o[nt][dt][0] *= al0;
-        o[nt][dt][1] *= al1;
-        o[nt][dt][2] *= al0;
-        o[nt][dt][3] *= al1;
+      for (int nt = 0; nt < NT; ++nt) {
+        float mx0 = fmaxf(sc[nt][0], sc[nt][2]), mx1 = fmaxf(sc[nt][1], sc[nt][3]);
+        mx0 = warp_max_xor(mx0, 4);
+        mx1 = warp_max_xor(mx1, 4);
+        mx0 = warp_max_xor(mx0, 8);
+        mx1 = warp_max_xor(mx1, 8);
+        mx0 = warp_max_xor(mx0, 16);
+        mx1 = warp_max_xor(mx1, 16);
+        const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+        // a verify column with no visible key yet keeps m = -inf; its l and O are still 0
+        const float al0 = mn0 == -INFINITY ? 1.f : exp2f(m_run[nt][0] - mn0);
+        const float al1 = mn1 == -INFINITY ? 1.f : exp2f(m_run[nt][1] - mn1);
+        m_run[nt][0] = mn0;
+        m_run[nt][1] = mn1;
+        l_run[nt][0] *= al0;
+        l_run[nt][1] *= al1;
+#pragma unroll
+        for (int dt = 0; dt < C::kDK; ++dt) {
+          o[nt][dt][0] *= al0;
+          o[nt][dt][1] *= al1;
+          o[nt][dt][2] *= al0;
+          o[nt][dt][3] *= al1;
+        }
       }
+    }
+    uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      // subtract 0 from a column still at m = -inf, so its (all -inf) scores give p = 0, not NaN
+      const float b0 = CAUSAL && m_run[nt][0] == -INFINITY ? 0.f : m_run[nt][0];
+      const float b1 = CAUSAL && m_run[nt][1] == -INFINITY ? 0.f : m_run[nt][1];
+      const float p00 = exp2f(sc[nt][0] - b0), p10 = exp2f(sc[nt][2] - b0);
+      const float p01 = exp2f(sc[nt][1] - b1), p11 = exp2f(sc[nt][3] - b1);
+      l_run[nt][0] += p00 + p10;
+      l_run[nt][1] += p01 + p11;
       pb0[nt] = movmatrix_trans(pack2<BF>(p00, p01));  // P^T[tok 2cq..2cq+1][head gq]
       pb1[nt] = movmatrix_trans(pack2<BF>(p10, p11));  // P^T[tok 2cq+8..][head gq]
     }
