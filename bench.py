@@ -446,10 +446,17 @@ def run_ours(args, world, rank, local):
     return result
 
 
+# The GB300's nominal figures, reported beside the measured ones: HBM3e ~8 TB/s and dense
+# fp16/bf16 tensor throughput 2.25 PFLOP/s.
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_TFLOPS = 2250.0
+
+
 def kernel_rooflines(nbytes, kern_ms, peaks) -> dict:
     """Roofline of each timed attention kernel from its algorithmic bytes / flops and its mean
     live launch time.  The bound is whichever roof the kernel's arithmetic intensity hits first
-    (HBM copy bandwidth vs fp16 dense tensor throughput, both measured)."""
+    (HBM copy bandwidth vs fp16 dense tensor throughput, both measured); the fraction of the
+    nominal figure of the same roof is reported too."""
     out = {}
     specs = {"decode": ("decode_partition_kernel", nbytes["decode_kernel_bytes"], 0),
              "prefill": (nbytes.get("prefill_kernel", "prefill"), nbytes["prefill_kernel_bytes"],
@@ -466,8 +473,10 @@ def kernel_rooflines(nbytes, kern_ms, peaks) -> dict:
             achieved, peak, unit, src = fl / t / 1e12, peaks["tflops"], "TFLOP/s", peaks["tflops_src"]
         else:
             achieved, peak, unit, src = nb / t / 1e9, peaks["hbm_gbs"], "GB/s", peaks["hbm_src"]
+        nominal = NOMINAL_TFLOPS if tensor else NOMINAL_HBM_GBS
         out[k] = {"kernel": name, "bound": "tensor" if tensor else "hbm", "achieved": achieved,
                   "peak": peak, "unit": unit, "frac": achieved / peak, "peak_source": src,
+                  "nominal_peak": nominal, "frac_of_nominal": achieved / nominal,
                   "traffic": None, "ms_per_launch": ms, "bytes_per_launch": nb,
                   "flops_per_launch": fl}
     return out

@@ -99,6 +99,9 @@ def test_roofline_bound_follows_arithmetic_intensity():
     assert abs(r["decode"]["achieved"] - 5000.0) < 1e-6
     assert r["prefill"]["bound"] == "tensor" and r["prefill"]["unit"] == "TFLOP/s"
     assert abs(r["prefill"]["frac"] - 0.4) < 1e-9  # 800 TFLOP/s of 2000
+    # beside the measured peaks: the nominal 8 TB/s and 2.25 PFLOP/s
+    assert abs(r["decode"]["frac_of_nominal"] - 5000.0 / 8000.0) < 1e-12
+    assert abs(r["prefill"]["frac_of_nominal"] - 800.0 / 2250.0) < 1e-12
     # a few rows per sequence (speculative verify) stays on the HBM roof
     n["prefill_kernel_flops"] = 10 ** 9
     r = bench.kernel_rooflines(n, {"prefill": 0.02}, peaks)
