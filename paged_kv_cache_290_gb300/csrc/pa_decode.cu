@@ -13,8 +13,8 @@
 //   * S^T = K Q^T on tensor cores (m16n8k16: 16 tokens x 8 heads x 16 dims), scores scaled by
 //     scale*log2(e), masked past seq_len with a select (never arithmetic), online softmax
 //     (running max / sum per head, exp2), P^T moved into the B-operand layout by movmatrix,
-//     O^T += V^T P^T on tensor cores with V^T fed by ldmatrix.trans and V rows past seq_len
-//     zeroed in the fragment (0 * NaN would poison the sum),
+//     O^T += V^T P^T on tensor cores with V^T fed by ldmatrix.trans and the V rows past seq_len
+//     (last unit only) zeroed in shared memory first (0 * NaN would poison the sum),
 //   * the 4 warps' (m, l, O) are combined in shared memory; a single-partition sequence writes
 //     fp16 output directly, otherwise the partition writes fp32 (m, l, O/l) partials that the
 //     merge kernel combines:  M = max m_p,  w_p = 2^(m_p - M) l_p,  out = sum w_p o_p / sum w_p.
@@ -67,6 +67,10 @@ struct DecodeCfg {
 template <int D>
 __device__ __forceinline__ uint32_t f8_row_chunk(uint32_t base, int tok, int chunk) {
   return D == 128 ? base + tok * 128 + ((chunk ^ (tok & 7)) << 4) : base + tok * 64 + chunk * 16;
+}
+
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
 }
 
 __device__ __forceinline__ uint32_t ldg_u32(const __half* p) {
@@ -337,11 +341,18 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
       pb1[nt] = movmatrix_trans(pack2<BF>(p10, p11));  // P^T[tok 2cq+8..][head gq]
     }
 
-    // ---- O^T[d][heads] += V^T[d][16 tokens] P^T
-    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+    // ---- O^T[d][heads] += V^T[d][16 tokens] P^T.  In a sequence's last, partial unit the V
+    // rows past its end are zeroed in the stage first: their p is 0, but the rows may hold any
+    // bits, and 0 * NaN would poison the sum.  (A whole token row is zeroed, so the swizzle of
+    // its 16-byte chunks does not matter.)
     if (nvalid < 16) {
-      vm0 = (2 * cq < nvalid ? 0x0000ffffu : 0u) | (2 * cq + 1 < nvalid ? 0xffff0000u : 0u);
-      vm1 = (2 * cq + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * cq + 9 < nvalid ? 0xffff0000u : 0u);
+      constexpr int kRowChunks = F8 ? D / 16 : 2 * D / 16;  // 16-byte chunks per token row
+      for (int c = lane; c < (16 - nvalid) * kRowChunks; c += 32) {
+        const int row = nvalid + c / kRowChunks, k = c % kRowChunks;
+        st_shared_zero16(F8 ? vb + row * D + k * 16
+                            : vb + (k >> 3) * C::kBoxBytes + row * 128 + (k & 7) * 16);
+      }
+      __syncwarp();
     }
     if constexpr (F8) {
       // one ldmatrix.x4.trans = two 16-dim blocks x two 8-token halves; a lane holds, per
@@ -353,14 +364,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
         ldsm_x4_trans(f8_row_chunk<D>(vb, mr + ((mi & 1) << 3), 2 * dd + (mi >> 1)), r);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t af[4] = {f16x2_from_e4m3x2(__byte_perm(r[2 * h], 0, 0x3320)),
-                            f16x2_from_e4m3x2(__byte_perm(r[2 * h], 0, 0x3331)),
-                            f16x2_from_e4m3x2(__byte_perm(r[2 * h + 1], 0, 0x3320)),
-                            f16x2_from_e4m3x2(__byte_perm(r[2 * h + 1], 0, 0x3331))};
-          af[0] &= vm0;
-          af[1] &= vm0;
-          af[2] &= vm1;
-          af[3] &= vm1;
+          const uint32_t af[4] = {f16x2_from_e4m3x2(__byte_perm(r[2 * h], 0, 0x3320)),
+                                  f16x2_from_e4m3x2(__byte_perm(r[2 * h], 0, 0x3331)),
+                                  f16x2_from_e4m3x2(__byte_perm(r[2 * h + 1], 0, 0x3320)),
+                                  f16x2_from_e4m3x2(__byte_perm(r[2 * h + 1], 0, 0x3331))};
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_16816<BF>(o[nt][2 * dd + h], af, pb0[nt], pb1[nt]);
         }
@@ -372,10 +379,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
         const int chunk = 2 * dt + (mi & 1);
         uint32_t af[4];
         ldsm_x4_trans(vb + (chunk >> 3) * C::kBoxBytes + swz128(tok, chunk & 7), af);
-        af[0] &= vm0;
-        af[1] &= vm0;
-        af[2] &= vm1;
-        af[3] &= vm1;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_16816<BF>(o[nt][dt], af, pb0[nt], pb1[nt]);
       }
