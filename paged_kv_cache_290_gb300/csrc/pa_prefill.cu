@@ -82,6 +82,38 @@ __device__ __forceinline__ int find_prefill_seq(const AttnArgs& a, int* warp_cou
   return *chosen_seq;
 }
 
+// As find_prefill_seq, but grid row z serves the prefill sequence of rank z when they are
+// ordered longest first (ties: batch order), so the longest CTAs are dispatched first and the
+// grid's tail is short.  For the one-Q-tile kernel, whose CTAs share no K/V tile, so the order
+// costs no L2 reuse.  The ranks are taken in one pass over at most kThreads sequences, through
+// `scratch` (kThreads ints of dynamic shared memory that nothing uses yet); a larger batch keeps
+// batch order.
+template <int kThreads>
+__device__ __forceinline__ int find_prefill_seq_longest_first(const AttnArgs& a, int* warp_count,
+                                                              int* chosen_seq, int* scratch,
+                                                              int target, bool first) {
+  if (a.num_seqs > kThreads) return find_prefill_seq<kThreads>(a, warp_count, chosen_seq, target, first);
+  const int tid = threadIdx.x;
+  if (tid == 0) *chosen_seq = -1;
+  const int ql = tid < a.num_seqs ? a.query_start_loc[tid + 1] - a.query_start_loc[tid] : 0;
+  const bool pf = ql > 1;
+  const int key = pf ? max(a.seq_lens[tid], 0) : -1;  // -1: not a prefill sequence
+  if (first && a.decode_skipped && ql == 1) atomicOr(a.err, kErrHint);
+  scratch[tid] = key;
+  __syncthreads();
+  int rank = 0, found = 0;
+  for (int j = 0; j < a.num_seqs; ++j) {  // every thread reads the same word: a broadcast
+    const int kj = scratch[j];
+    found += kj >= 0;
+    rank += kj > key || (kj == key && j < tid);
+  }
+  if (pf && rank == target) *chosen_seq = tid;
+  if (first && tid == 0 && found > a.prefill_seqs) atomicOr(a.err, kErrHint);
+  fence_proxy_async();  // the scratch words are overwritten by TMA copies later
+  __syncthreads();
+  return *chosen_seq;
+}
+
 // A producer warp: streams the K (or V) tiles 0 .. ntiles-1 of sequence s, kv head g, keys
 // [key_base, kend), into a ring of `stages` stages of kKVBytes each.  Each 16-token unit is found
 // through the block table and fetched as 128-byte-swizzled TMA boxes (one per 64 columns).
@@ -216,7 +248,6 @@ __device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorM
                                               uint64_t* land, int key_base) {
   constexpr int kUnits = kKeys / 16, kKVBytes = (D / 64) * kKeys * 128, kUnit8 = 16 * D;
   constexpr int kCodes = kKVBytes / 2;  // where a stage's codes land
-  constexpr int kChunks = D / 16;       // 16-code chunks of a key row
   const int lane = threadIdx.x & 31;
   auto units_of = [&](int j) { return min(kUnits, (kend - (key_base + j * kKeys) + 15) >> 4); };
   auto unit_block = [&](int j) {
@@ -800,10 +831,12 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
       return;
     }
   } else {
-    // Later q tiles of a chunk see more keys: dispatch them first so the grid's tail is short.
+    // Later q tiles of a chunk see more keys, and longer sequences more tiles: dispatch them
+    // first so the grid's tail is short.
     qt = gridDim.x - 1 - blockIdx.x;
-    s = find_prefill_seq<C::kThreads>(a, warp_count, &chosen_seq, blockIdx.z,
-                                      blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0);
+    s = find_prefill_seq_longest_first<C::kThreads>(
+        a, warp_count, &chosen_seq, reinterpret_cast<int*>(smem), blockIdx.z,
+        blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0);
     if (s < 0) return;
     row0 = a.query_start_loc[s];
     q_len = a.query_start_loc[s + 1] - row0;
