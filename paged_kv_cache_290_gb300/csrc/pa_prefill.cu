@@ -11,16 +11,19 @@
 //     the same warp roles and TMEM layout, but its two softmax warpgroups take the even and the
 //     odd key tiles of the one Q tile, each with its own online softmax and O accumulator, merged
 //     at the end with the log-sum-exp rule (S_{j+2} reuses S_j's buffer after P_j V_j).
-// Both find their sequence with the same scan and feed K/V with the same producer warps.
+// Both find their sequence with a scan of the descriptor (the pair kernel in batch order, the
+// parity kernel longest sequence first) and feed K/V with the same producer warps.
 //
-// prefill_pair_kernel: work item = one CTA = (two Q tiles, kv head g, prefill sequence).  A Q tile is 128 rows, each
-// a (query token, head of the GQA group) pair, so one K/V tile serves every head of the group,
-// and every K/V tile the CTA loads serves both Q tiles (256 rows).  Warp roles:
+// prefill_pair_kernel: work item = one CTA = (two Q tiles, kv head g, prefill sequence).  A Q
+// tile is 128 rows, each a (query token, head of the GQA group) pair, so one K/V tile serves
+// every head of the group, and every K/V tile the CTA loads serves both Q tiles (256 rows).
+// Warp roles:
 //   * producers (warps 8 and 9): stream 128-key K and V tiles (8 units of 16 tokens gathered
 //     through the block table, 128-byte-swizzled TMA boxes) into a 2-stage K ring and a 3-stage
 //     V ring; a K stage is released once both S = Q K^T products that read it are done, a V
-//     stage as soon as both P V products are (before the next S is issued).  The next tile's block ids are read while a producer waits
-//     for its stage, and the MMA issuer waits for K_{j+1} only right before S(j+1),
+//     stage as soon as both P V products are (before the next S is issued).  The next tile's
+//     block ids are read while a producer waits for its stage, and the MMA issuer waits for
+//     K_{j+1} only right before S(j+1),
 //   * MMA issuer (lane 0 of warp 10): per Q tile t, S_t = Q_t K_j^T into TMEM buffer t (M 128,
 //     N 128, K d, both operands K-major from shared memory) and O_t += P_t V_j with P_t read
 //     from TMEM (it overwrites the first 64 columns of S_t's buffer, two fp16 per column) and
