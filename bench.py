@@ -140,13 +140,25 @@ def all_prefill(b) -> bool:
     return not verify_path(b) and b.max_query_len > 1 and b.num_prefill_seqs == b.num_seqs
 
 
-def launches_per_step(b, sp: int = 0) -> int:
+def prefill_launches(b, decode: bool, num_sms: int = 152) -> int:
+    """Launches of the chunked-prefill kernel in one call: one, except for the two-tile kernel
+    beside decode rows, which goes as launches of one wave (num_sms CTAs) each over its items
+    (pairs of 128-row Q tiles x kv heads x prefill sequences)."""
+    if b.max_query_len <= 1 or verify_path(b):
+        return 0
+    group = b.num_q_heads // b.num_kv_heads
+    if b.max_query_len <= 128 // group or not decode:
+        return 1
+    items = -(-b.max_query_len // (2 * (128 // group))) * b.num_kv_heads * b.num_prefill_seqs
+    return -(-items // num_sms)
+
+
+def launches_per_step(b, sp: int = 0, num_sms: int = 152) -> int:
     parts = max(1, math.ceil(b.max_seq_len / 512))
     decode = not all_prefill(b)
     n = 1 if b.k_new.shape[0] > 0 else 0        # reshape_and_cache
     n += 1 if decode else 0                       # decode partitions
-    prefill = b.max_query_len > 1 and not verify_path(b)
-    n += 1 if prefill else 0                      # chunked-prefill tiles
+    n += prefill_launches(b, decode, num_sms)     # chunked-prefill tiles
     n += 1 if parts > 1 and decode else 0         # log-sum-exp merge
     n += 1 if sp else 0                           # shared-prefix pass
     return n
@@ -431,7 +443,8 @@ def run_ours(args, world, rank, local):
         "bytes": nbytes,
         "roofline": kernels[dominant],
         "roofline_kernels": kernels,
-        "gpu_launches": launches_per_step(b, sp) * args.steps,
+        "gpu_launches": launches_per_step(
+            b, sp, torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps,
         "wall_ms_per_step": wall * 1e3 / args.steps,
         "kernel_timing": {"steps": args.steps, "ms_per_step_with_kernel_events": inst_step_ms,
                           "note": "per-kernel CUDA events are taken on K further steps; "
@@ -550,11 +563,20 @@ def cpu_baseline(b, nbytes, budget_s=12.0):
     times = [_oracle_sample_seconds(b, seqs) for _ in range(3)]
     t = statistics.median(times)
     sb = _sample_bytes(b, seqs)
-    return {"value": sb / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"attention of {len(seqs)} of {b.num_seqs} sequences (all their query rows "
-                      f"and heads; the scatter-write's copy is left out), fp64 C oracle with "
-                      f"OpenMP, median of 3 runs of {t:.2f} s",
-            "seconds": t}
+    res = {"value": sb / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": f"attention of {len(seqs)} of {b.num_seqs} sequences (all their query rows "
+                     f"and heads; the scatter-write's copy is left out), fp64 C oracle with "
+                     f"OpenMP, median of 3 runs of {t:.2f} s",
+           "seconds": t}
+    if t * threads < budget_s / 3:
+        # a small sample (the tiny workload): its single-core time too
+        oracle.set_threads(1)
+        try:
+            t1 = statistics.median(_oracle_sample_seconds(b, seqs) for _ in range(3))
+        finally:
+            oracle.set_threads(threads)
+        res["single_core"] = {"value": sb / t1 / 1e9, "unit": "GB/s", "cores": 1, "seconds": t1}
+    return res
 
 
 def run_reference(args, world, rank):

@@ -68,6 +68,15 @@ def test_shared_prefix_pass_splits_the_kernel_bytes():
 def test_mixed_step_counts_prefill_launch():
     b = small_mixed()
     assert bench.launches_per_step(b) == 4
+    # the full mixed step: 4 chunks x 8 pairs of 32-token Q tiles x 8 kv heads = 256 items of
+    # the two-tile kernel, which beside decode rows go as launches of one wave (152 + 104)
+    m = W.mixed_step(16, keep_contiguous=False, keep_pre=False)
+    assert bench.prefill_launches(m, decode=True) == 2
+    assert bench.launches_per_step(m) == 5
+    assert bench.launches_per_step(m, num_sms=256) == 4
+    # alone (no decode rows) it is one full grid
+    assert bench.prefill_launches(W.mixed_step(16, num_decode=0, keep_contiguous=False,
+                                               keep_pre=False), decode=False) == 1
     n = bench.algorithmic_bytes(b)
     assert n["decode_rows"] == sum(1 for s in b.seqs if s.query_len == 1)
 
@@ -183,3 +192,14 @@ def test_max_over_ranks_with_two_gloo_ranks():
 
 def test_single_rank_reduction_is_identity():
     assert bench.reduce_max(3.25, 1) == 3.25
+
+
+def test_cpu_baseline_reports_a_single_core_time_for_a_small_sample():
+    """The oracle's host timing on the tiny workload: the whole batch fits the sample, and its
+    single-core time is reported beside the all-core one."""
+    b = W.WORKLOADS["tiny_decode"](keep_contiguous=False, keep_pre=False)
+    r = bench.cpu_baseline(b, bench.algorithmic_bytes(b), budget_s=3.0)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0 and r["cores"] >= 1
+    assert f"of {b.num_seqs} of {b.num_seqs} sequences" in r["sample"]
+    one = r["single_core"]
+    assert one["cores"] == 1 and one["value"] > 0
