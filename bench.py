@@ -236,7 +236,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark_load(self, t0: float, t1: float):
+        """The host-clock window of a stretch of back-to-back GPU work (the clock soak)."""
+        self.load = (t0, t1)
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -248,9 +252,10 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, smax, power, reasons = [], [], [], set()
+        sm, smax, power, reasons, load_sm, load_power = [], [], [], set(), [], []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        lo, hi = getattr(self, "load", (None, None))
+        for t, line in self.lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -263,35 +268,57 @@ class ClockSampler:
                 power.append(float(f[3]))
             except ValueError:
                 continue
+            # a sample read in the soak window, past its first 100 ms, was taken under load
+            if lo is not None and lo + 0.1 <= t <= hi:
+                load_sm.append(sm[-1])
+                load_power.append(power[-1])
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        res = {"sm_mhz": statistics.median(load_sm or sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None,
+               "power_w_max": max(power) if power else None,
+               "samples": len(sm), "samples_under_load": len(load_sm),
+               "sm_mhz_under_load_median": statistics.median(load_sm) if load_sm else None,
+               "power_w_under_load_median": statistics.median(load_power) if load_power else None,
+               "reasons": sorted(reasons)}
+        return res
 
 
 # ------------------------------------------------------------------------------ our arm
 
-def run_ours(args, world, rank, local):
+def workload_config(name, b, sp, world) -> dict:
+    """The ``config`` object of a line (both arms echo the same keys)."""
+    return {"workload": name, "num_seqs": b.num_seqs, "max_seq_len": b.max_seq_len,
+            "max_query_len": b.max_query_len, "num_tokens": b.num_tokens,
+            "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads,
+            "head_dim": b.head_dim, "block_size": b.block_size, "num_blocks": b.num_blocks,
+            "kv_cache_dtype": b.kv_dtype, "partition_tokens": 512,
+            "shared_prefix_tokens": sp,
+            "parallelism": f"replicas x{world}",
+            "l2": "flushed before every timed step (512 MiB write, outside the events)"}
+
+
+# The other workloads of the task's configurations, measured beside the default line: the tiny
+# GQA decode, the Llama-3-8B decode, the prefix-shared decode and the mixed continuous-batching
+# step over 16- and 32-token blocks.
+EXTRA_WORKLOADS = ("tiny_decode", "llama8b_decode", "prefix_shared_decode", "mixed_step_bs16",
+                   "mixed_step_bs32")
+
+
+def measure(name, args, world, rank, dev, soak_s=0.0, clocks=None, cpu_seconds=None) -> dict:
+    """One workload: K timed steps (device-resident inputs), K steps with per-kernel events,
+    optionally a clock soak, the end-to-end pass from pinned host buffers and the oracle's CPU
+    baseline.  Returns the workload's line (without ``clocks``)."""
     import paged_kv_cache_290_gb300 as pa
-    from paged_kv_cache_290_gb300 import build as pa_build
     from paged_kv_cache_290_gb300 import workloads as W
 
-    if rank == 0 or not os.path.exists(pa_build.LIB):
-        pa_build.build()
-    barrier(world)
-    pa.load_library()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-
-    b = W.WORKLOADS[args.workload](keep_contiguous=False, keep_pre=False)
+    b = W.WORKLOADS[name](keep_contiguous=False, keep_pre=False)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     sp = 0 if args.no_shared_prefix else shared_prefix_tokens(b)
     nbytes = algorithmic_bytes(b, sp)
     if sp:
-        nbytes["shared_prefix_kernel"] = shared_prefix_kernel(
-            b, sp, torch.cuda.get_device_properties(dev).multi_processor_count)
+        nbytes["shared_prefix_kernel"] = shared_prefix_kernel(b, sp, num_sms)
     stream = torch.cuda.current_stream()
 
     # device-resident inputs (the pool already holds every token; the scatter rewrites the new
@@ -319,7 +346,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     st, bits = pa.get_device_error()
     if st != 0:
-        raise RuntimeError(f"device error after warm-up: status {st} bits {bits}")
+        raise RuntimeError(f"{name}: device error after warm-up: status {st} bits {bits}")
 
     # -------- device-resident timed region: exactly K steps, nothing between the step events
     # but the step itself
@@ -333,9 +360,6 @@ def run_ours(args, world, rank, local):
         e[0].record(stream)   # torch creates an event on its first record(); the library then
         e[1].record(stream)   # re-records the kernel events around the kernels it launches
     torch.cuda.synchronize()
-    uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", ""))
-    clocks = ClockSampler(uuid)
-    clocks.start()
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
@@ -366,12 +390,32 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     for k in timed:
         pa.set_timing_events(None, None, kernel=k)
-    clk = clocks.stop()
     kern_ms = {k: statistics.mean(d_[k][0].elapsed_time(d_[k][1]) for d_ in kev) for k in timed}
     inst_step_ms = statistics.mean(a.elapsed_time(c) for a, c in inst_ms)
+
+    # -------- clock soak: identical steps back to back (no flush) for soak_s seconds, outside
+    # the reported timing, so the clock sampler sees the SMs under this workload's load
+    soak = None
+    if soak_s > 0 and clocks is not None:
+        s0, s1 = mk(), mk()
+        n_soak = 0
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        s0.record(stream)
+        while time.perf_counter() - t0 < soak_s:
+            for _ in range(16):
+                step(q, k_new, v_new, slots, bt, sl, qsl, out)
+            n_soak += 16
+        s1.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        clocks.mark_load(t0, t1)
+        soak = {"steps": n_soak, "seconds": t1 - t0,
+                "ms_per_step": s0.elapsed_time(s1) / n_soak,
+                "note": "back-to-back steps without L2 flush, outside the reported timing"}
     st, bits = pa.get_device_error()
     if st != 0:
-        raise RuntimeError(f"device error in timed region: status {st} bits {bits}")
+        raise RuntimeError(f"{name}: device error in timed region: status {st} bits {bits}")
     ms = statistics.mean(step_ms)
     ms_max = reduce_max(ms, world)
 
@@ -416,10 +460,10 @@ def run_ours(args, world, rank, local):
                "steps": n_e2e}
 
     peaks = load_peaks()
-    peak, peak_src = peaks["hbm_gbs"], peaks["hbm_src"]
+    peak = peaks["hbm_gbs"]
     kernels = kernel_rooflines(nbytes, kern_ms, peaks)
     for k in kernels:
-        kernels[k]["traffic"] = load_traffic(args.workload, k)
+        kernels[k]["traffic"] = load_traffic(name, k)
     dominant = max(kernels, key=lambda k: kernels[k]["ms_per_launch"])
     value = world * nbytes["step_logical"] / (ms_max * 1e-3) / 1e9
     tok_s = world * nbytes["decode_rows"] / (ms_max * 1e-3)
@@ -429,33 +473,76 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if b.kv_dtype == "bf16" else "f16",  # E4M3 codes run fp16 MMAs
         "data": "synthetic",
-        "config": {"workload": args.workload, "num_seqs": b.num_seqs,
-                   "max_seq_len": b.max_seq_len, "max_query_len": b.max_query_len,
-                   "num_tokens": b.num_tokens, "num_q_heads": b.num_q_heads,
-                   "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
-                   "block_size": b.block_size, "num_blocks": b.num_blocks,
-                   "kv_cache_dtype": b.kv_dtype, "partition_tokens": 512,
-                   "shared_prefix_tokens": sp,
-                   "parallelism": f"replicas x{world}",
-                   "l2": "flushed before every timed step (512 MiB write, outside the events)"},
+        "config": workload_config(name, b, sp, world),
         "decode_tok_s_per_layer": tok_s,
         "hbm_roofline_frac_step": (nbytes["step_logical"] / (ms * 1e-3) / 1e9) / peak,
         "bytes": nbytes,
         "roofline": kernels[dominant],
         "roofline_kernels": kernels,
-        "gpu_launches": launches_per_step(
-            b, sp, torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps,
+        "gpu_launches": launches_per_step(b, sp, num_sms) * args.steps,
         "wall_ms_per_step": wall * 1e3 / args.steps,
         "kernel_timing": {"steps": args.steps, "ms_per_step_with_kernel_events": inst_step_ms,
                           "note": "per-kernel CUDA events are taken on K further steps; "
                                   "value and ms_per_step come from K steps without them"},
-        "clocks": clk,
         "impl": "ours",
     }
+    if nbytes["kv_unique"] != nbytes["kv_logical"]:
+        # aliased prefix blocks: the unique bytes are what the HBM roofline divides
+        result["value_unique"] = world * (nbytes["attention_unique"] +
+                                          nbytes["reshape_and_cache"]) / (ms_max * 1e-3) / 1e9
+        result["hbm_roofline_frac_step_unique"] = result["value_unique"] / world / peak
+    if soak is not None:
+        result["clock_soak"] = soak
     if e2e is not None:
         result["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(b, nbytes, budget_s=args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(
+            b, nbytes, budget_s=args.cpu_seconds if cpu_seconds is None else cpu_seconds)
+    return result
+
+
+def summary(res: dict) -> dict:
+    """The fields of a workload's line kept in the ``workloads`` object of the default line."""
+    keep = ("value", "unit", "ms_per_step", "value_unique", "decode_tok_s_per_layer",
+            "hbm_roofline_frac_step", "hbm_roofline_frac_step_unique", "roofline",
+            "roofline_kernels", "gpu_launches", "e2e", "cpu_baseline", "config", "dtype",
+            "steps", "warmup")
+    return {k: res[k] for k in keep if k in res}
+
+
+def run_ours(args, world, rank, local):
+    import paged_kv_cache_290_gb300 as pa
+    from paged_kv_cache_290_gb300 import build as pa_build
+
+    if rank == 0 or not os.path.exists(pa_build.LIB):
+        pa_build.build()
+    barrier(world)
+    pa.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", ""))
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    result = measure(args.workload, args, world, rank, dev, soak_s=args.soak_seconds,
+                     clocks=clocks)
+    result["clocks"] = clocks.stop()
+    if "clock_soak" in result and "decode" in result["roofline_kernels"]:
+        mhz = result["clocks"]["sm_mhz_under_load_median"]
+        if mhz:  # the decode kernel's time in SM clock cycles at the median clock under load
+            result["clock_soak"]["decode_kcycles_at_median_mhz"] = (
+                result["roofline_kernels"]["decode"]["ms_per_launch"] * 1e-3 * mhz * 1e3)
+    if args.workload == DEFAULT_WORKLOAD and not args.no_workloads:
+        extra = {}
+        for name in EXTRA_WORKLOADS:
+            torch.cuda.empty_cache()
+            c2 = ClockSampler(uuid)
+            c2.start()
+            r = measure(name, args, world, rank, dev,
+                        cpu_seconds=min(args.cpu_seconds, args.extra_cpu_seconds))
+            r["clocks"] = c2.stop()
+            extra[name] = summary(r)
+            extra[name]["clocks"] = r["clocks"]
+        result["workloads"] = extra
     return result
 
 
@@ -580,23 +667,27 @@ def cpu_baseline(b, nbytes, budget_s=12.0):
 
 
 def run_reference(args, world, rank):
-    """The oracle timed as the reference arm: each step = the oracle on one bounded sample."""
+    """The oracle timed as the reference arm: each step = the oracle on a bounded sample of the
+    workload, enough sequences that their (sequence, kv head) tasks occupy every host core
+    twice over (the oracle's OpenMP loop runs over those tasks)."""
     if rank != 0:
         return None
     import oracle
     from paged_kv_cache_290_gb300 import workloads as W
     oracle.build()
     b = W.WORKLOADS[args.workload](keep_contiguous=False, keep_pre=False)
+    sp = 0 if args.no_shared_prefix else shared_prefix_tokens(b)
     threads = oracle.get_threads()
     g = torch.Generator().manual_seed(11)
     order = [i for i in torch.randperm(b.num_seqs, generator=g).tolist()
              if b.seqs[i].query_len > 0]
-    # one sequence per step, cycling through the batch; keeps the default run within minutes
+    per_step = max(1, min(len(order), -(-2 * threads // b.num_kv_heads)))
+    sample = lambda i: [order[(i * per_step + j) % len(order)] for j in range(per_step)]
     for i in range(args.warmup):
-        _oracle_sample_seconds(b, [order[i % len(order)]])
+        _oracle_sample_seconds(b, sample(i))
     times, bytes_ = [], []
     for i in range(args.steps):
-        seqs = [order[i % len(order)]]
+        seqs = sample(args.warmup + i)
         times.append(_oracle_sample_seconds(b, seqs))
         bytes_.append(_sample_bytes(b, seqs))
     total_t = sum(times)
@@ -606,14 +697,13 @@ def run_reference(args, world, rank):
         "warmup": args.warmup, "ms_per_step": total_t * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "num_seqs": b.num_seqs,
-                   "max_seq_len": b.max_seq_len, "num_q_heads": b.num_q_heads,
-                   "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
-                   "block_size": b.block_size, "parallelism": "host cores"},
+        "config": workload_config(args.workload, b, sp, world),
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": "attention of one sequence of the workload per step (all "
-                                   "its rows and heads), cycling through the batch"},
+                         "sample": f"attention of {per_step} sequences of the workload per step "
+                                   f"({per_step * b.num_kv_heads} (sequence, kv head) tasks "
+                                   f"for {threads} cores; all their rows and heads), cycling "
+                                   f"through the batch; fp64 C oracle with OpenMP"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -630,6 +720,13 @@ def main(argv=None):
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="attend an aliased prefix per sequence instead of once for all rows")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--extra-cpu-seconds", type=float, default=4.0,
+                    help="oracle budget of each extra workload's CPU baseline")
+    ap.add_argument("--soak-seconds", type=float, default=1.5,
+                    help="back-to-back steps after the timed region, for the clock sampler")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure only --workload (the default line also measures the other "
+                         "workloads of the task's configurations)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -28,7 +28,8 @@
  *     errors (a slot or block id outside the pool, query_len > seq_len, a sequence longer than
  *     the hint) make the affected work item skip its memory accesses, set a bit in a device
  *     error word and leave its output rows unwritten; pa_get_device_error reports them.
- *   - Every wait inside a kernel gives up after two seconds and reports PA_ERR_TIMEOUT.
+ *   - Every wait inside a kernel gives up after two seconds (pa_set_wait_limit) and reports
+ *     PA_ERR_TIMEOUT.
  *   - Thread-safety: functions may be called from several host threads; pa_last_error is
  *     per thread.
  */
@@ -212,6 +213,9 @@ int pa_attention_fp8(const pa_tensor* q, const pa_tensor* k_cache, const pa_tens
  *     hint->max_seq_len) > 32 MiB) is rejected with PA_ERR_WORKSPACE and a message; nothing runs.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
  *     with that device current) and caches it; make that first call before any stream capture.
+ *     The cached address belongs to the device's primary context as it was then: after
+ *     cudaDeviceReset (or any teardown of that context) this entry point must not be called
+ *     again in the same process.
  *   - All calls on a device share the array, which keeps the last call's contents; nothing in it
  *     needs to start at zero.  Calls that overlap on the GPU race on it: order them.
  * Results are those of pa_attention on the same inputs.
@@ -261,6 +265,19 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_
 #define PA_TIMED_PREFILL 1
 #define PA_TIMED_SHARED_PREFIX 2
 int pa_set_timing_events(int kernel, void* start, void* stop);
+
+/*
+ * pa_set_wait_limit -- how long every bounded wait inside the kernels of later pa_attention and
+ * pa_attention_fp8 calls on this host thread may last before it gives up: the waiting work item
+ * then lets its own copies in flight land, leaves its output rows unwritten and sets the
+ * timeout bit that pa_get_device_error reports as PA_ERR_TIMEOUT (the CUDA context stays
+ * usable).  A legitimate wait lasts microseconds; the default is 2 s.  Returns PA_OK, or
+ * PA_ERR_INVALID_ARG (limit unchanged) outside [PA_WAIT_LIMIT_MIN_NS, PA_WAIT_LIMIT_MAX_NS].
+ */
+#define PA_WAIT_LIMIT_DEFAULT_NS 2000000000ull
+#define PA_WAIT_LIMIT_MIN_NS 1000ull
+#define PA_WAIT_LIMIT_MAX_NS 10000000000ull
+int pa_set_wait_limit(uint64_t limit_ns);
 
 /* PA_VERSION of the built library. */
 int pa_version(void);

@@ -101,6 +101,23 @@ int pa_bm_step_descriptor(const pa_block_manager* bm, const int64_t* seq_ids,
                           int32_t pad_block, int32_t* block_tables, int32_t* seq_lens,
                           int32_t* query_start_loc, int64_t* slot_mapping);
 
+/* pa_step_slot_mapping -- the same descriptor arithmetic for a scheduler that keeps its own
+ * block tables (no manager): from host arrays of n sequences (seq_lens[i] keys after the step,
+ * the last query_lens[i] of them new; block_tables int32 rows of max_blocks entries, bt_stride
+ * apart) it writes
+ *   query_start_loc  int32 [n + 1] (prefix sums of query_lens),
+ *   slot_mapping     int64 [sum query_lens]: block_tables[i][p / block_size] * block_size +
+ *                    p % block_size for p = seq_lens[i] - query_lens[i] .. seq_lens[i] - 1
+ *                    ("Local_LLM_03_vLLM_Architecture", paged-KV slide: logical position p of a
+ *                    sequence lives at offset p % block_size of its (p / block_size)-th block).
+ * Block ids are copied, not checked (the device checks them against the pool).
+ * PA_ERR_INVALID_ARG (nothing written) when a query length is outside 0 .. seq_len, a sequence
+ * with new tokens needs more than max_blocks blocks, or slot_capacity is below the row count. */
+int pa_step_slot_mapping(int32_t n, const int32_t* seq_lens, const int32_t* query_lens,
+                         const int32_t* block_tables, int64_t bt_stride, int32_t max_blocks,
+                         int32_t block_size, int32_t* query_start_loc, int64_t* slot_mapping,
+                         int64_t slot_capacity);
+
 #ifdef __cplusplus
 }
 #endif

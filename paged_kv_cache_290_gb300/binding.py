@@ -30,6 +30,7 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3:
                 4: "PA_ERR_TIMEOUT", 5: "PA_ERR_OUT_OF_RANGE", 6: "PA_ERR_WORKSPACE",
                 7: "PA_ERR_DESCRIPTOR", 8: "PA_ERR_NO_BLOCKS"}
 PA_F16, PA_I32, PA_I64, PA_F8E4M3, PA_BF16 = 0, 1, 2, 3, 4
+PA_WAIT_LIMIT_DEFAULT_NS = 2_000_000_000
 PARTITION_TOKENS = 512
 EXPORTED = ("pa_reshape_and_cache", "pa_attention_workspace_size", "pa_attention",
             "pa_last_error", "pa_get_device_error", "pa_set_timing_events", "pa_version",
@@ -37,7 +38,8 @@ EXPORTED = ("pa_reshape_and_cache", "pa_attention_workspace_size", "pa_attention
             "pa_attention_fp8",
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_append",
             "pa_bm_truncate", "pa_bm_fork", "pa_bm_free", "pa_bm_stats", "pa_bm_sequence",
-            "pa_bm_step_descriptor")
+            "pa_bm_step_descriptor", "pa_step_slot_mapping", "pa_set_wait_limit",
+            "pa_selftest_wait_timeout")
 
 # Byte tensors are E4M3 codes (the only one-byte type of the ABI).
 _DTYPES = {torch.float16: PA_F16, torch.int32: PA_I32, torch.int64: PA_I64,
@@ -92,6 +94,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_attention_static_scratch.restype = ctypes.c_int
         lib.pa_attention_static_scratch.argtypes = [P, P, P, P, P, P, ctypes.c_float, P,
                                                     ctypes.POINTER(PABatchHint), ctypes.c_void_p]
+        lib.pa_set_wait_limit.restype = ctypes.c_int
+        lib.pa_set_wait_limit.argtypes = [ctypes.c_uint64]
+        lib.pa_selftest_wait_timeout.restype = ctypes.c_int
+        lib.pa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, ctypes.c_void_p]
         lib.pa_set_timing_events.restype = ctypes.c_int
         lib.pa_set_timing_events.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.pa_copy_blocks.restype = ctypes.c_int
@@ -116,7 +122,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                 ("pa_bm_stats", ctypes.c_int, [VP, PI32, PI32, PI32, PI32]),
                 ("pa_bm_sequence", ctypes.c_int, [VP, I64, PI32, PI32, I32, PI32]),
                 ("pa_bm_step_descriptor", ctypes.c_int,
-                 [VP, PI64, PI32, I32, I32, I32, PI32, PI32, PI32, PI64])):
+                 [VP, PI64, PI32, I32, I32, I32, PI32, PI32, PI32, PI64]),
+                ("pa_step_slot_mapping", ctypes.c_int,
+                 [I32, PI32, PI32, PI32, I64, I32, I32, PI32, PI64, I64])):
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
@@ -239,6 +247,12 @@ def set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cu
         _check(lib.pa_set_timing_events(TIMED_KERNELS[kernel], start.cuda_event, stop.cuda_event))
 
 
+def set_wait_limit(limit_ns: int) -> None:
+    """``pa_set_wait_limit``: how long any wait inside later attention kernels of this thread
+    may last before it gives up and reports PA_ERR_TIMEOUT (default 2 s)."""
+    _check(load_library().pa_set_wait_limit(int(limit_ns)))
+
+
 def get_device_error(stream=None):
     """Synchronise the stream and return (status, bits) of the device error word (cleared)."""
     lib = load_library()
@@ -270,18 +284,22 @@ class BatchDescriptor:
                   non_blocking: bool = False) -> "BatchDescriptor":
         """Build from host lists: ``seq_lens[s]`` keys after the step, ``query_lens[s]`` new
         rows (the last ones of the sequence), ``block_tables`` int32 [N, MB]."""
-        sl = torch.as_tensor(seq_lens, dtype=torch.int32)
-        ql = torch.as_tensor(query_lens, dtype=torch.int64)
-        if (ql < 0).any() or (ql > sl.to(torch.int64)).any():
-            raise ValueError("need 0 <= query_len <= seq_len")
-        qsl = torch.zeros(len(sl) + 1, dtype=torch.int32)
-        qsl[1:] = torch.cumsum(ql, 0).to(torch.int32)
+        sl = torch.as_tensor(seq_lens, dtype=torch.int32).contiguous()
+        ql = torch.as_tensor(query_lens, dtype=torch.int32).contiguous()
         bt = torch.as_tensor(block_tables, dtype=torch.int32)
-        slots = []
-        for s in range(len(sl)):
-            for p in range(int(sl[s]) - int(ql[s]), int(sl[s])):
-                slots.append(int(bt[s, p // block_size]) * block_size + p % block_size)
-        sm = torch.tensor(slots, dtype=torch.int64)
+        if bt.dim() != 2 or bt.shape[0] != sl.shape[0] or ql.shape != sl.shape:
+            raise ValueError("block_tables must be [N, MB] with N = len(seq_lens) = len(query_lens)")
+        if bt.stride(1) != 1:
+            bt = bt.contiguous()
+        n = int(sl.shape[0])
+        qsl = torch.empty(n + 1, dtype=torch.int32)
+        cap = int(ql.to(torch.int64).clamp(min=0).sum())
+        sm = torch.empty(cap, dtype=torch.int64)
+        ptr = lambda t, c: ctypes.cast(t.data_ptr(), ctypes.POINTER(c)) if t.numel() else None
+        _check(load_library().pa_step_slot_mapping(
+            n, ptr(sl, ctypes.c_int32), ptr(ql, ctypes.c_int32), ptr(bt, ctypes.c_int32),
+            bt.stride(0) if n else 0, int(bt.shape[1]), int(block_size),
+            ptr(qsl, ctypes.c_int32), ptr(sm, ctypes.c_int64), cap))
         dev = lambda x: x.to(device, non_blocking=non_blocking)
-        return cls(dev(qsl), dev(sl), dev(bt), dev(sm), int(ql.max()) if len(ql) else 0,
-                   int(sl.max()) if len(sl) else 0, int((ql > 1).sum()))
+        return cls(dev(qsl), dev(sl), dev(bt), dev(sm), int(ql.max()) if n else 0,
+                   int(sl.max()) if n else 0, int((ql > 1).sum()))

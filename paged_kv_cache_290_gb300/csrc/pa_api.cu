@@ -14,11 +14,14 @@
 #include "pa_common.cuh"
 #include "pa_kernels.h"
 
+static_assert(PA_WAIT_LIMIT_DEFAULT_NS == pa::kWaitLimitNs, "default wait limit");
+
 namespace {
 
 thread_local std::string g_last_error;
 thread_local cudaEvent_t g_time_start[3] = {};  // indexed by PA_TIMED_*
 thread_local cudaEvent_t g_time_stop[3] = {};
+thread_local uint64_t g_wait_limit_ns = pa::kWaitLimitNs;  // pa_set_wait_limit
 
 int fail(int code, const std::string& msg) {
   g_last_error = msg;
@@ -239,6 +242,7 @@ WorkspaceLayout workspace_layout(int64_t t, int64_t hq, int64_t d, int32_t max_s
 
 namespace pa {
 int set_last_error(int status, const std::string& message) { return fail(status, message); }
+cudaError_t error_word(unsigned** out) { return device_error_word(out); }
 }  // namespace pa
 
 extern "C" {
@@ -463,6 +467,7 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
   a.kv_fp8 = fp8 ? 1 : 0;
   a.bf16 = in_dt == PA_BF16 ? 1 : 0;
   a.cascade_parts = sp / PA_PARTITION_TOKENS;
+  a.wait_limit_ns = g_wait_limit_ns;
   cudaError_t e = device_error_word(&a.err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
   if (a.cascade_parts > 0 && (e = device_sm_count(&a.num_sms)) != cudaSuccess)
@@ -561,6 +566,16 @@ int pa_set_timing_events(int kernel, void* start, void* stop) {
   const bool on = start && stop;
   g_time_start[kernel] = on ? static_cast<cudaEvent_t>(start) : nullptr;
   g_time_stop[kernel] = on ? static_cast<cudaEvent_t>(stop) : nullptr;
+  return PA_OK;
+}
+
+int pa_set_wait_limit(uint64_t limit_ns) {
+  g_last_error.clear();
+  if (limit_ns < PA_WAIT_LIMIT_MIN_NS || limit_ns > PA_WAIT_LIMIT_MAX_NS)
+    return fail(PA_ERR_INVALID_ARG, "wait limit must be in [" +
+                                        std::to_string(PA_WAIT_LIMIT_MIN_NS) + ", " +
+                                        std::to_string(PA_WAIT_LIMIT_MAX_NS) + "] ns");
+  g_wait_limit_ns = limit_ns;
   return PA_OK;
 }
 

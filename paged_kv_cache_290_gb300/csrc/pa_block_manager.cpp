@@ -374,4 +374,36 @@ int pa_bm_step_descriptor(const pa_block_manager* bm, const int64_t* seq_ids,
   return ok();
 }
 
+int pa_step_slot_mapping(int32_t n, const int32_t* seq_lens, const int32_t* query_lens,
+                         const int32_t* block_tables, int64_t bt_stride, int32_t max_blocks,
+                         int32_t block_size, int32_t* query_start_loc, int64_t* slot_mapping,
+                         int64_t slot_capacity) {
+  if (n < 0 || block_size < 1 || max_blocks < 0 || bt_stride < max_blocks || !query_start_loc ||
+      (n > 0 && (!seq_lens || !query_lens || (max_blocks > 0 && !block_tables))))
+    return fail(PA_ERR_INVALID_ARG, "step_slot_mapping: NULL argument or bad size");
+  int64_t total = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (query_lens[i] < 0 || query_lens[i] > seq_lens[i])
+      return fail(PA_ERR_INVALID_ARG, "step_slot_mapping: need 0 <= query_len <= seq_len");
+    if ((static_cast<int64_t>(seq_lens[i]) + block_size - 1) / block_size > max_blocks &&
+        query_lens[i] > 0)
+      return fail(PA_ERR_INVALID_ARG, "step_slot_mapping: a block table is too short");
+    total += query_lens[i];
+  }
+  if (total > INT32_MAX) return fail(PA_ERR_INVALID_ARG, "step_slot_mapping: too many rows");
+  if (total > slot_capacity || (total > 0 && !slot_mapping))
+    return fail(PA_ERR_INVALID_ARG, "step_slot_mapping: slot_mapping holds " +
+                                        std::to_string(slot_capacity) + " entries, " +
+                                        std::to_string(total) + " needed");
+  int64_t row = 0;
+  query_start_loc[0] = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t* bt = block_tables + static_cast<int64_t>(i) * bt_stride;
+    for (int64_t p = seq_lens[i] - query_lens[i]; p < seq_lens[i]; ++p)
+      slot_mapping[row++] = static_cast<int64_t>(bt[p / block_size]) * block_size + p % block_size;
+    query_start_loc[i + 1] = static_cast<int32_t>(row);
+  }
+  return ok();
+}
+
 }  // extern "C"

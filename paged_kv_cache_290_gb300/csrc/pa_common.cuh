@@ -23,7 +23,9 @@ enum : unsigned {
 };
 
 constexpr int kPartitionTokens = 512;   // split-context partition length (keys)
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s, far beyond any legitimate wait
+// Default limit of every bounded wait: 2 s, far beyond any legitimate wait.  A call carries its
+// own limit (AttnArgs::wait_limit_ns), which the host may lower.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -84,14 +86,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, giving up after kWaitLimitNs (or an
+// Wait for the phase with the given parity to complete, giving up after limit_ns (or an
 // iteration cap) with kErrTimeout set in *err.  Returns false on give-up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 28); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) break;
+    if ((it & 63u) == 63u && global_timer_ns() - t0 > limit_ns) break;
   }
   atomicOr(err, kErrTimeout);
   return false;

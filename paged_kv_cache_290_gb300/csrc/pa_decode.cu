@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
   int failed_at = -1;
   for (int i = 0; i < my_n; ++i) {
     const int st = i % C::kStages;
-    const bool ok = mbar_wait(bar0 + st * 8, (i / C::kStages) & 1, a.err);
+    const bool ok = mbar_wait(bar0 + st * 8, (i / C::kStages) & 1, a.err, a.wait_limit_ns);
     if (__any_sync(0xffffffffu, !ok)) {
       failed_at = i;
       break;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
     if (lane == 0) {
       const int issued = min(my_n, failed_at + C::kStages);
       for (int i = failed_at + 1; i < issued; ++i)
-        mbar_wait(bar0 + (i % C::kStages) * 8, (i / C::kStages) & 1, a.err);
+        mbar_wait(bar0 + (i % C::kStages) * 8, (i / C::kStages) & 1, a.err, a.wait_limit_ns);
     }
   }
 

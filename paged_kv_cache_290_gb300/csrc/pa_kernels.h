@@ -66,11 +66,15 @@ struct AttnArgs {
                      //   items (x q-tile pairs per (kv head, sequence)); 0: one full grid
   int item_base;     // first item of such a launch
   int prefill_ctas;  // CTAs per such launch (0: one full grid)
+  uint64_t wait_limit_ns;  // every bounded wait of the call gives up after this long
   unsigned* err;
 };
 
 // Sets the message pa_last_error() returns on this host thread; returns `status`.
 int set_last_error(int status, const std::string& message);
+
+// Device address of the current device's error word (looked up once per device).
+cudaError_t error_word(unsigned** out);
 
 // Whole-block copies (copy-on-write of shared blocks).
 struct CopyArgs {

@@ -9,8 +9,8 @@
 //
 // The array is a file-scope __device__ object: every GPU that loads the library holds its
 // kStaticScratchBytes until the process exits.  All calls on a device share it and it keeps the
-// last call's contents.  Nothing in it must start at zero: every partial slot the merge reads is
-// written earlier in the same call.  Calls that overlap on the GPU (other streams, other host
+// last call's contents.  Nothing in it needs to start at zero: every partial slot the merge
+// reads is written earlier in the same call.  Calls that overlap on the GPU (other streams, other host
 // threads) race on it, so they must be ordered by the caller.
 #include <cuda_runtime.h>
 

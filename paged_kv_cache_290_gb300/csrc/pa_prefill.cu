@@ -143,7 +143,8 @@ __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap*
     const int id = id_next;
     if (j + 1 < ntiles) id_next = unit_block(j + 1);
     bool ok = true;
-    if (lane == 0 && round > 0) ok = mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err);
+    if (lane == 0 && round > 0) ok = mbar_wait(smem_addr(&empty[st]), (round - 1) & 1,
+                                               a.err, a.wait_limit_ns);
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
     const int key0 = key_base + j * kKeys;
     const int units = min(kUnits, (kend - key0 + 15) >> 4);
@@ -163,7 +164,7 @@ __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap*
   }
   if (lane == 0)
     for (int j = max(0, issued - stages); j < issued; ++j)
-      mbar_wait(smem_addr(&full[j % stages]), (j / stages) & 1, a.err);
+      mbar_wait(smem_addr(&full[j % stages]), (j / stages) & 1, a.err, a.wait_limit_ns);
 }
 
 // Widen, in place, key rows [32 p0, 32 p1) of a landed tile of E4M3 codes (stage at `dst`, the
@@ -234,7 +235,7 @@ __device__ __forceinline__ void widen_helper_f8(const AttnArgs& a, int kend, int
     const int rows = min(kKeys / 16, (kend - (key_base + j * kKeys) + 15) >> 4) * 16;
     for (int t = 0; t < 2; ++t) {  // K, then V
       const int stages = t == 0 ? k_stages : v_stages, st = j % stages;
-      const bool ok = mbar_wait(smem_addr(&land[t][st]), (j / stages) & 1, a.err);
+      const bool ok = mbar_wait(smem_addr(&land[t][st]), (j / stages) & 1, a.err, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, ok)) return;
       widen_rows_f8<D, kKeys>((t == 0 ? k_ring : v_ring) + st * kKVBytes, rows,
                               kF8MainPasses<D>, 4);
@@ -275,7 +276,7 @@ __device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorM
   // tile j (landed) widened in place; false when a wait gave up
   auto widen = [&](int j) -> bool {
     const int st = j % stages;
-    const bool ok = mbar_wait(smem_addr(&land[st]), (j / stages) & 1, a.err);
+    const bool ok = mbar_wait(smem_addr(&land[st]), (j / stages) & 1, a.err, a.wait_limit_ns);
     if (!__all_sync(0xffffffffu, ok)) return false;
     widen_rows_f8<D, kKeys>(ring + st * kKVBytes, units_of(j) * 16, 0, kF8MainPasses<D>);
     fence_proxy_async();  // the generic stores -> visible to the MMA's shared-memory reads
@@ -289,7 +290,7 @@ __device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorM
     const int st = j % stages, round = j / stages;
     const int id = id_next;
     if (j + 1 < ntiles) id_next = unit_block(j + 1);
-    ok = round == 0 || mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err);
+    ok = round == 0 || mbar_wait(smem_addr(&empty[st]), (round - 1) & 1, a.err, a.wait_limit_ns);
     if (!__all_sync(0xffffffffu, ok)) {
       ok = false;
       break;
@@ -302,7 +303,7 @@ __device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorM
   // copies requested but never widened (a wait gave up) must land before the CTA retires
   if (lane == 0)
     for (int j = max(0, fetched - stages); j < fetched; ++j)
-      mbar_wait(smem_addr(&land[j % stages]), (j / stages) & 1, a.err);
+      mbar_wait(smem_addr(&land[j % stages]), (j / stages) & 1, a.err, a.wait_limit_ns);
 }
 
 // F8: the pool holds E4M3 codes, widened in place in the fp16 stages (no extra memory).
@@ -515,11 +516,12 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
                         (j > 0 || k > 0));
     };
     auto kwait = [&](int j) {
-      const bool ok = mbar_wait(smem_addr(&k_full[j % C::kKStages]), (j / C::kKStages) & 1, a.err);
+      const bool ok = mbar_wait(smem_addr(&k_full[j % C::kKStages]), (j / C::kKStages) & 1,
+                                a.err, a.wait_limit_ns);
       tmem_fence_after_sync();
       return ok;
     };
-    bool ok = mbar_wait(smem_addr(&q_full), 0, a.err) && kwait(0);
+    bool ok = mbar_wait(smem_addr(&q_full), 0, a.err, a.wait_limit_ns) && kwait(0);
     if (ok) {
 #pragma unroll
       for (int t = 0; t < C::kQTiles; ++t)
@@ -529,12 +531,12 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     for (int j = 0; ok && j < ntiles; ++j) {
       const int vst = j % C::kVStages;
       const bool more = j + 1 < ntiles;
-      ok = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err);
+      ok = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err, a.wait_limit_ns);
       bool k_ready = false;  // K_{j+1} is waited for just before its first use
 #pragma unroll
       for (int t = 0; ok && t < C::kQTiles; ++t) {
         if (j >= tiles[t]) continue;
-        ok = mbar_wait(smem_addr(&p_full[t]), j & 1, a.err);
+        ok = mbar_wait(smem_addr(&p_full[t]), j & 1, a.err, a.wait_limit_ns);
         if (!ok) break;
         tmem_fence_after_sync();
         issue_pv(t, j);
@@ -555,7 +557,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     }
     // Every MMA this thread issued has finished before O is read or the CTA tears down.
     umma_commit(smem_addr(&drain));
-    mbar_wait(smem_addr(&drain), 0, a.err);
+    mbar_wait(smem_addr(&drain), 0, a.err, a.wait_limit_ns);
   } else if (F8 && D == 128 && warp == kMmaWarp + 1) {
     // ============================================================== FP8 widening helper
     widen_helper_f8<D, C::kKeys>(a, kend, ntiles, key_base, C::kKStages, C::kVStages, k_s, v_s,
@@ -603,7 +605,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     const float mul = prescale ? 1.f : a.scale_log2;  // exponent = fma(score, mul, -m)
     for (int j = 0; j < my_tiles; ++j) {
       // S_t(j) done; it was issued after P_t V_{j-1}, so O_t is settled too.
-      if (!mbar_wait(smem_addr(&s_full[t]), j & 1, a.err)) {
+      if (!mbar_wait(smem_addr(&s_full[t]), j & 1, a.err, a.wait_limit_ns)) {
         stopped = true;
         break;
       }
@@ -676,7 +678,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         // The last key tile: V rows at or past kend may be stale or NaN; zero them once the
         // tile has landed (the MMA reads V only after p_full below).  Thread r clears row r.
         const int vst = j % C::kVStages;
-        const bool landed = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err);
+        const bool landed = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1,
+                                      a.err, a.wait_limit_ns);
         if (landed && tile0 + r >= kend) {
           const uint32_t vrow = v_s + vst * C::kKVBytes + r * 128;
 #pragma unroll
@@ -702,7 +705,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     // Epilogue: O_t / l -> out (fp16, rows of real query tokens only); the shared-prefix pass
     // writes the rows' partials of partition blockIdx.z instead: m (log2 units), l and O / l.
     bool ok = !stopped && my_tiles > 0;
-    if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err);
+    if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err, a.wait_limit_ns);
     if (CASCADE && !__any_sync(0xffffffffu, !ok)) {
       tmem_fence_after_sync();
       const float inv = a.v_scale / l_run;  // v_scale: 1, or the FP8 pool's V scale
@@ -934,7 +937,8 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     // S_j = Q K_j^T into TMEM buffer j % 2; frees its K stage once done.
     auto issue_s = [&](int j) {
       const int st = j % C::kKStages;
-      if (!mbar_wait(smem_addr(&k_full[st]), (j / C::kKStages) & 1, a.err)) return false;
+      if (!mbar_wait(smem_addr(&k_full[st]), (j / C::kKStages) & 1,
+                     a.err, a.wait_limit_ns)) return false;
       tmem_fence_after_sync();
       const uint32_t kst = k_s + st * C::kKVBytes;
 #pragma unroll
@@ -948,11 +952,12 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
       umma_commit(smem_addr(&k_empty[st]));
       return true;
     };
-    bool ok = mbar_wait(smem_addr(&q_full), 0, a.err) && issue_s(0) && (ntiles < 2 || issue_s(1));
+    bool ok = mbar_wait(smem_addr(&q_full), 0,
+                        a.err, a.wait_limit_ns) && issue_s(0) && (ntiles < 2 || issue_s(1));
     for (int j = 0; ok && j < ntiles; ++j) {
       const int vst = j % C::kVStages;
-      ok = mbar_wait(smem_addr(&p_full[j & 1]), (j >> 1) & 1, a.err) &&
-           mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err);
+      ok = mbar_wait(smem_addr(&p_full[j & 1]), (j >> 1) & 1, a.err, a.wait_limit_ns) &&
+           mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err, a.wait_limit_ns);
       if (!ok) break;
       tmem_fence_after_sync();
       const uint32_t vb = v_s + vst * C::kKVBytes;
@@ -966,7 +971,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     }
     // Every MMA this thread issued has finished before O is read or the CTA tears down.
     umma_commit(smem_addr(&drain));
-    mbar_wait(smem_addr(&drain), 0, a.err);
+    mbar_wait(smem_addr(&drain), 0, a.err, a.wait_limit_ns);
   } else if (F8 && D == 128 && warp == kMmaWarp + 1) {
     // ============================================================== FP8 widening helper
     widen_helper_f8<D, C::kKeys>(a, kend, ntiles, key_base, C::kKStages, C::kVStages, k_s, v_s,
@@ -1012,7 +1017,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     for (int j = par; j < ntiles; j += 2) {
       const uint32_t sbuf = tmem + lane_addr + par * 128;
       // S_j done; it was issued after P_{j-2} V_{j-2}, so O_par is settled too.
-      if (!mbar_wait(smem_addr(&s_full[par]), (j >> 1) & 1, a.err)) {
+      if (!mbar_wait(smem_addr(&s_full[par]), (j >> 1) & 1, a.err, a.wait_limit_ns)) {
         stopped = true;
         break;
       }
@@ -1085,7 +1090,8 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
         // The last tile: V rows at or past kend may be stale or NaN; zero them once the tile
         // has landed (the MMA reads V only after p_full below).  Thread r clears V row r.
         const int vst = j % C::kVStages;
-        const bool landed = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err);
+        const bool landed = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1,
+                                      a.err, a.wait_limit_ns);
         if (landed && tile0 + r >= kend) {
           const uint32_t vrow = v_s + vst * C::kKVBytes + r * 128;
 #pragma unroll
@@ -1121,7 +1127,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     const float l_all = red_l[0][r] * w_e + (two ? red_l[1][r] * w_o : 0.f);
     const float inv = a.v_scale / l_all;  // v_scale: 1, or the FP8 pool's V scale
     bool ok = !*reinterpret_cast<volatile int*>(&softmax_stop);
-    if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err);
+    if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err, a.wait_limit_ns);
     if (CASCADE && !__any_sync(0xffffffffu, !ok)) {
       // The rows' partials of partition blockIdx.z: m (log2 units), l, and this thread's half
       // of O / l.

@@ -202,6 +202,32 @@ def test_batch_descriptor_from_host():
     assert d.max_query_len == 5 and d.max_seq_len == 40 and d.num_prefill_seqs == 2
 
 
+def test_step_slot_mapping_rejects_bad_descriptors(lib):
+    with pytest.raises(B.PAError, match="query_len"):
+        pa.BatchDescriptor.from_host([5, 4], [5, 5], [[0], [1]], block_size=16, device="cpu")
+    with pytest.raises(B.PAError, match="too short"):
+        pa.BatchDescriptor.from_host([17], [1], [[0]], block_size=16, device="cpu")
+    i32 = lambda *x: (ctypes.c_int32 * max(1, len(x)))(*x)
+    qsl, sm = i32(0, 0), (ctypes.c_int64 * 1)()
+    assert lib.pa_step_slot_mapping(1, i32(3), i32(2), i32(9), 1, 1, 16, qsl, sm, 1) == \
+        B.PA_ERR_INVALID_ARG
+    assert "holds 1 entries, 2 needed" in msg(lib)
+    assert list(qsl) == [0, 0]  # nothing written
+    # an idle sequence (no new token) needs no table entry
+    d = pa.BatchDescriptor.from_host([0, 3], [0, 1], [[0], [5]], block_size=16, device="cpu")
+    assert d.query_start_loc.tolist() == [0, 0, 1] and d.slot_mapping.tolist() == [5 * 16 + 2]
+
+
+def test_wait_limit_range(lib):
+    assert lib.pa_set_wait_limit(0) == B.PA_ERR_INVALID_ARG
+    assert "wait limit" in msg(lib)
+    assert lib.pa_set_wait_limit(10**11) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_set_wait_limit(2 * 10**9) == B.PA_OK
+    # the self-test hook refuses limits that would hold a GPU for long, before any CUDA call
+    assert lib.pa_selftest_wait_timeout(10**9, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_selftest_wait_timeout(10, None) == B.PA_ERR_INVALID_ARG
+
+
 # --------------------------------------------------------------- FP8 cache entry points
 
 def call_attention_fp8(lib, k_scale=0.05, v_scale=0.02, hint=(1, 100), pool_dtype=B.PA_F8E4M3,

@@ -203,3 +203,35 @@ def test_cpu_baseline_reports_a_single_core_time_for_a_small_sample():
     assert f"of {b.num_seqs} of {b.num_seqs} sequences" in r["sample"]
     one = r["single_core"]
     assert one["cores"] == 1 and one["value"] > 0
+
+
+def test_reference_arm_echoes_our_config_and_fills_the_cores():
+    import argparse
+    args = argparse.Namespace(workload="tiny_decode", steps=2, warmup=1, no_shared_prefix=False)
+    res = bench.run_reference(args, world=1, rank=0)
+    b = W.tiny_decode(keep_contiguous=False, keep_pre=False)
+    assert res["config"] == bench.workload_config("tiny_decode", b, 0, 1)
+    assert res["impl"] == "reference" and res["value"] > 0
+    assert res["e2e"]["h2d_bytes_per_step"] == 0
+    assert "sequences of the workload per step" in res["cpu_baseline"]["sample"]
+    assert bench.run_reference(args, world=2, rank=1) is None  # other ranks do no work
+
+
+def test_clock_sampler_counts_samples_in_the_soak_window():
+    c = bench.ClockSampler("GPU-x")
+    c.proc = None
+    line = "GPU-x, {}, 2070, {}, 0x0, Not Active, Not Active, Not Active, {}"
+    c.lines = [(0.0, line.format(1000, 150, "Not Active")),
+               (1.0, line.format(1980, 900, "Active")),
+               (1.2, line.format(2000, 950, "Active")),
+               (3.0, line.format(900, 160, "Not Active"))]
+    c.mark_load(0.5, 1.5)
+
+    class _P:  # stands in for the finished nvidia-smi process
+        def terminate(self): pass
+        def wait(self, timeout=None): pass
+    c.proc, c.thread = _P(), type("T", (), {"join": lambda self, timeout=None: None})()
+    r = c.stop()
+    assert r["samples"] == 4 and r["samples_under_load"] == 2
+    assert r["sm_mhz"] == 1990.0 and r["sm_mhz_under_load_median"] == 1990.0
+    assert r["reasons"] == ["sw_power_cap"]

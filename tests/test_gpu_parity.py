@@ -314,7 +314,10 @@ def test_prefill_sequence_count_hint():
 
 # ------------------------------------------------------------------ the five full-size workloads
 
-def _full(name, sample_prefill_rows=None):
+def _full(name, sample_prefill_rows=None, whole_longest_chunk=False):
+    """One full-size step against the oracle.  With ``sample_prefill_rows`` the prefill chunks
+    are sampled (first, last and a seeded sample of rows); ``whole_longest_chunk`` adds every
+    row of the chunk with the longest context (all its 128-row tiles at full size)."""
     b = W.WORKLOADS[name]()
     kc, vc, out = gpu_step(b)
     rk, rv = oracle.reshape_and_cache(b.k_new, b.v_new, b.k_cache_pre, b.v_cache_pre,
@@ -334,6 +337,10 @@ def _full(name, sample_prefill_rows=None):
                 pick = torch.randperm(spec.query_len, generator=g)[:sample_prefill_rows].tolist()
                 for i in set(pick) | {0, spec.query_len - 1}:
                     mask[r0 + i] = 1
+        if whole_longest_chunk:
+            s = max((s for s, spec in enumerate(b.seqs) if spec.query_len > 1),
+                    key=lambda s: b.seqs[s].seq_len)
+            mask[int(b.query_start_loc[s]):int(b.query_start_loc[s + 1])] = 1
     ref = oracle.attention_batch(b, row_mask=mask)
     rows = None if mask is None else np.nonzero(mask)[0]
     return assert_close(out, ref, rows)
@@ -357,7 +364,7 @@ def test_full_prefix_shared_decode():
 
 @pytest.mark.parametrize("bs", [16, 32])
 def test_full_mixed_step(bs):
-    _full(f"mixed_step_bs{bs}", sample_prefill_rows=24)
+    _full(f"mixed_step_bs{bs}", sample_prefill_rows=24, whole_longest_chunk=bs == 16)
 
 
 def test_full_spec_verify():
