@@ -320,14 +320,17 @@ struct PairCfg {
   static constexpr int kVStages = 3;
   static constexpr int kSmemBytes =
       kQTiles * kQBytes + (kKStages + kVStages) * kKVBytes + 1024;
-  static constexpr int kSoftmax = 256;                    // one warpgroup per Q tile
-  static constexpr int kPerTile = 128;                    // softmax threads of one Q tile
+  // Two warpgroups per Q tile: one per half of each key tile's columns (and of O's columns),
+  // so a row's softmax is shared by two threads that trade their maxima once per key tile.
+  static constexpr int kSoftmax = 512;
+  static constexpr int kPerTile = 256;                    // softmax threads of one Q tile
   // + a warpgroup of K producer, V producer, MMA issuer and one idle warp
   static constexpr int kThreads = kSoftmax + 4 * 32;
-  // Registers: launched at 168 per thread (384 x 168 = 64512); the producer warpgroup gives
-  // back down to 72 and the two softmax warpgroups take 216: 256 x 216 + 128 x 72 = 64512.
-  static constexpr int kRegsSoftmax = 216;
-  static constexpr int kRegsOther = 72;
+  // Registers: launched at 96 per thread (640 x 96 = 61440); the producer warpgroup gives back
+  // down to 64 and the four softmax warpgroups take 104: 512 x 104 + 128 x 64 = 61440.
+  static constexpr int kLaunchRegs = 96;
+  static constexpr int kRegsSoftmax = 104;
+  static constexpr int kRegsOther = 64;
   // TMEM columns: S/P of Q tile A [0,128), of Q tile B [128,256), O_A, O_B from 256.
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 256;
@@ -356,6 +359,9 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   __shared__ uint32_t tmem_base;
   __shared__ int warp_count[C::kThreads / 32];
   __shared__ int chosen_seq;
+  // [Q tile][column half][row]: each half's key-tile maximum, rounded up to bfloat16 (so both
+  // halves of a row take the same base from the same two stored values)
+  __shared__ __nv_bfloat16 half_max[C::kQTiles][2][C::kRows];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -472,10 +478,10 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
 
   constexpr int kKWarp = C::kSoftmax / 32, kVWarp = kKWarp + 1, kMmaWarp = kKWarp + 2;
   static_assert(C::kRegsSoftmax * C::kSoftmax + C::kRegsOther * (C::kThreads - C::kSoftmax) <=
-                    168 * C::kThreads,
+                    C::kLaunchRegs * C::kThreads,
                 "register split exceeds the launch allocation");
   if (warp >= kKWarp) {
-  // ================================================ producer / MMA warpgroup (warps 8-11)
+  // ================================================ producer / MMA warpgroup (warps 16-19)
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsOther));
   if (warp == kKWarp || warp == kVWarp) {
     // ============================================================== producer warps (K, V)
@@ -564,29 +570,39 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
                                  k_full, v_full, land);
   }  // lanes 1-31 of warp 10 have no role (warp 11 neither, unless it helps widen FP8 tiles)
   } else {
-    // ============================================================== softmax warps 0-7
+    // ============================================================== softmax warps 0-15
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
-    const int t = warp >> 2;                  // Q tile of this warpgroup
-    const int r = (warp & 3) * 32 + lane;     // TMEM lane = row of the Q tile
+    // Warp w: Q tile t = w / 8, column half h = (w / 4) % 2 (keys 64h .. 64h + 63 of every key
+    // tile and O columns h D / 2 .. of the output), TMEM lanes 32 (w % 4) .. + 31, one row per
+    // thread.  The two warps of a row quarter meet at named barrier 1 + 4 t + w % 4 once per key
+    // tile (trading their maxima) and once in the epilogue (trading their sums); every meeting
+    // also ORs the pair's failed waits, so both leave together and neither waits alone.
+    constexpr int kHalfKeys = C::kKeys / 2, kHalfD = D / 2;
+    const int t = warp >> 3;                  // Q tile of this warp
+    const int h = (warp >> 2) & 1;            // column half
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;        // TMEM lane = row of the Q tile
+    const uint32_t pair_bar = 1 + t * 4 + quarter;
     const int qi = r / a.group, hg = r % a.group;
     const int first = qbase + t * tile_q;     // first query token of the Q tile
     const int tok = first + qi;
     const bool rv = qi < tile_q && tok < q_len;
     const int pos = ctx + (rv ? tok : first);  // padding rows mirror the tile's first row
-    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t sbuf = tmem + lane_addr + t * C::kKeys;
-    const uint32_t obuf = tmem + lane_addr + C::kOCol + t * D;
+    const uint32_t obuf = tmem + lane_addr + C::kOCol + t * D + h * kHalfD;
     const int my_tiles = tiles[t];
     // The V rows past kend are zeroed by the Q tile whose P V of the last key tile comes first.
     const bool zeroes_v = !CASCADE && (t == 0 ? tiles[0] == ntiles : tiles[0] < ntiles);
 
-    // The Q row -> shared memory, 128B-swizzled K-major.
+    // Half h of the Q row -> shared memory, 128B-swizzled K-major.
     {
       const __half* qrow = a.q + static_cast<int64_t>(row0 + (rv ? tok : 0)) * a.q_stride +
                            static_cast<int64_t>(g * a.group + hg) * D;
       const uint32_t qb = q_s + t * C::kQBytes;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
+      for (int cc = 0; cc < D / 16; ++cc) {
+        const int c = h * (D / 16) + cc;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (rv) v = __ldg(reinterpret_cast<const uint4*>(qrow + c * 8));
         const uint32_t dst = qb + (c >> 3) * C::kHalfBytes + swz128(r, c & 7);
@@ -598,45 +614,56 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       mbar_arrive(smem_addr(&q_full));
     }
 
-    bool stopped = false;  // a wait of this thread gave up
+    bool stopped = false;  // a wait of this pair of threads gave up
     float m_run = -INFINITY, l_run = 0.f;
     const int min_pos = ctx + first;
     const bool prescale = !(a.scale_log2 > 0.f);
     const float mul = prescale ? 1.f : a.scale_log2;  // exponent = fma(score, mul, -m)
     for (int j = 0; j < my_tiles; ++j) {
       // S_t(j) done; it was issued after P_t V_{j-1}, so O_t is settled too.
-      if (!mbar_wait(smem_addr(&s_full[t]), j & 1, a.err, a.wait_limit_ns)) {
+      const bool got = mbar_wait(smem_addr(&s_full[t]), j & 1, a.err, a.wait_limit_ns);
+      uint32_t sv[kHalfKeys / 32][32];
+      float mloc = -INFINITY;
+      const int key0 = j * C::kKeys + h * kHalfKeys;
+      if (got) {
+        tmem_fence_after_sync();
+#pragma unroll
+        for (int qq = 0; qq < kHalfKeys / 32; ++qq)
+          tmem_ld32(sbuf + h * kHalfKeys + qq * 32, sv[qq]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int qq = 0; qq < kHalfKeys / 32; ++qq) tmem_regs_ready(sv[qq]);
+        // Scores stay raw where scale > 0 (the max commutes with the scale, which is folded
+        // into the exponent's FMA below); otherwise they are scaled here.  Masked keys: -inf.
+        const bool masked = !CASCADE && key0 + kHalfKeys - 1 > min_pos;
+        if (prescale || masked) {
+#pragma unroll
+          for (int c = 0; c < kHalfKeys; ++c) {
+            float v = __uint_as_float(sv[c >> 5][c & 31]);
+            if (prescale) v *= a.scale_log2;
+            if (masked && key0 + c > pos) v = -INFINITY;
+            sv[c >> 5][c & 31] = __float_as_uint(v);
+          }
+        }
+        float m2[2] = {-INFINITY, -INFINITY};  // two chains of three-input maxima
+#pragma unroll
+        for (int c = 0; c < kHalfKeys; c += 2)
+          m2[(c >> 1) & 1] = fmax3(m2[(c >> 1) & 1], __uint_as_float(sv[c >> 5][c & 31]),
+                                   __uint_as_float(sv[c >> 5][(c & 31) + 1]));
+        mloc = fmaxf(m2[0], m2[1]);
+      }
+      // Trade maxima: rounded up, the stored value is >= the half's max, and both threads read
+      // the same two values, so they take the same base.  This half's S columns have been read
+      // (wait::ld above) before the other half may store P over them (after the barrier).
+      half_max[t][h][r] = __float2bfloat16_ru(mloc);
+      tmem_fence_before_sync();
+      if (bar_sync_or(pair_bar, 64, !got)) {
         stopped = true;
         break;
       }
       tmem_fence_after_sync();
-      uint32_t sv[C::kKeys / 32][32];
-#pragma unroll
-      for (int qq = 0; qq < C::kKeys / 32; ++qq) tmem_ld32(sbuf + qq * 32, sv[qq]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int qq = 0; qq < C::kKeys / 32; ++qq) tmem_regs_ready(sv[qq]);
-
-      // Scores stay raw where scale > 0 (the max commutes with the scale, which is folded into
-      // the exponent's FMA below); otherwise they are scaled here.  Masked keys become -inf.
-      const int key0 = j * C::kKeys;
-      const bool masked = !CASCADE && key0 + C::kKeys - 1 > min_pos;
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (prescale || masked) {
-#pragma unroll
-        for (int c = 0; c < C::kKeys; ++c) {
-          float v = __uint_as_float(sv[c >> 5][c & 31]);
-          if (prescale) v *= a.scale_log2;
-          if (masked && key0 + c > pos) v = -INFINITY;
-          sv[c >> 5][c & 31] = __float_as_uint(v);
-          m4[c & 3] = fmaxf(m4[c & 3], v);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < C::kKeys; ++c)
-          m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c >> 5][c & 31]));
-      }
-      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mul;
+      const float mx = fmaxf(__bfloat162float(half_max[t][0][r]),
+                             __bfloat162float(half_max[t][1][r])) * mul;
       float alpha = 1.f;
       if (mx > m_run + C::kRescaleLog2 || (m_run == -INFINITY && mx > -INFINITY)) {
         alpha = ex2_approx(m_run - mx);  // 0 when m_run is still -inf
@@ -644,59 +671,67 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       }
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t tt[32];
-          tmem_ld32(obuf + c0, tt);
+        for (int c0 = 0; c0 < kHalfD; c0 += 8) {
+          uint32_t tt[8];
+          tmem_ld8(obuf + c0, tt);
           tmem_wait_ld();
           tmem_regs_ready(tt);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) tt[c] = __float_as_uint(__uint_as_float(tt[c]) * alpha);
-          tmem_st32(obuf + c0, tt);
+          for (int c = 0; c < 8; ++c) tt[c] = __float_as_uint(__uint_as_float(tt[c]) * alpha);
+          tmem_st8(obuf + c0, tt);
         }
       }
 
-      // P (fp16) -> TMEM columns 0..63 of the buffer, two keys per column; l keeps the
-      // unrounded p.  A row with every key so far masked keeps m = -inf and gets p = 0.
+      // P (fp16) of this half's keys -> TMEM columns h * 32 .. + 31 of the buffer, two keys per
+      // column; l keeps the unrounded p.  A row with every key so far masked keeps m = -inf and
+      // gets p = 0.
       const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      // exponents and sums two keys at a time (packed fp32 pairs: the same roundings as fmaf
+      // and + per key)
+      const uint64_t mul2 = f32x2(mul, mul), negm2 = f32x2(neg_m, neg_m);
+      uint64_t ps2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
-      for (int q4 = 0; q4 < C::kKeys / 32; ++q4) {
-        uint32_t pk[16];
+      for (int q8 = 0; q8 < kHalfKeys / 16; ++q8) {  // 16 keys -> 8 columns of P at a time
+        uint32_t pk[8];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c]), mul, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c + 1]), mul, neg_m));
-          ps[c & 3] += p0 + p1;
+        for (int c = 0; c < 8; ++c) {
+          const int k = q8 * 16 + 2 * c;
+          float x0, x1;
+          f32x2_split(ffma2(f32x2(__uint_as_float(sv[k >> 5][k & 31]),
+                                  __uint_as_float(sv[k >> 5][(k & 31) + 1])),
+                            mul2, negm2),
+                      x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          ps2[c & 1] = fadd2(ps2[c & 1], f32x2(p0, p1));
           pk[c] = pack2<BF>(p0, p1);
         }
-        tmem_st16(sbuf + q4 * 16, pk);
+        tmem_st8(sbuf + h * (kHalfKeys / 2) + q8 * 8, pk);
       }
-      l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      float s0, s1, s2, s3;
+      f32x2_split(ps2[0], s0, s1);
+      f32x2_split(ps2[1], s2, s3);
+      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
 
       const int tile0 = j * C::kKeys;
       if (zeroes_v && j == ntiles - 1 && tile0 + C::kKeys > kend) {
         // The last key tile: V rows at or past kend may be stale or NaN; zero them once the
-        // tile has landed (the MMA reads V only after p_full below).  Thread r clears row r.
+        // tile has landed (the MMA reads V only after p_full below).  The thread of row r and
+        // half h clears half h of V row r (its 64-column chunk; D = 64 has one chunk).
         const int vst = j % C::kVStages;
-        const bool landed = mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1,
-                                      a.err, a.wait_limit_ns);
-        if (landed && tile0 + r >= kend) {
-          const uint32_t vrow = v_s + vst * C::kKVBytes + r * 128;
+        const bool landed =
+            mbar_wait(smem_addr(&v_full[vst]), (j / C::kVStages) & 1, a.err, a.wait_limit_ns);
+        if (landed && tile0 + r >= kend && h < C::kHalves) {
+          const uint32_t vrow = v_s + vst * C::kKVBytes + h * (C::kKeys * 128) + r * 128;
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                               vrow + h * (C::kKeys * 128) + c * 16),
-                           "r"(0u), "r"(0u), "r"(0u), "r"(0u)
-                           : "memory");
+          for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(vrow + c * 16),
+                         "r"(0u), "r"(0u), "r"(0u), "r"(0u)
+                         : "memory");
         }
         fence_proxy_async();
-        if (!landed) {
-          stopped = true;
-          break;
-        }
+        if (!landed) stopped = true;  // the last tile: the epilogue's meeting ends both
       }
+      if (stopped) break;
       tmem_wait_st();
       tmem_fence_before_sync();
       mbar_arrive(smem_addr(&p_full[t]));
@@ -704,50 +739,58 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
 
     // Epilogue: O_t / l -> out (fp16, rows of real query tokens only); the shared-prefix pass
     // writes the rows' partials of partition blockIdx.z instead: m (log2 units), l and O / l.
+    // The two halves' sums are traded through the Q tile's shared memory, which no MMA reads
+    // once `drain` has completed.
     bool ok = !stopped && my_tiles > 0;
     if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err, a.wait_limit_ns);
-    if (CASCADE && !__any_sync(0xffffffffu, !ok)) {
+    float* l_half = reinterpret_cast<float*>(smem) + (t * 2 + h) * C::kRows;
+    if (ok) l_half[r] = l_run;
+    if (!bar_sync_or(pair_bar, 64, !ok)) {
+      const float l_all = l_run + reinterpret_cast<const float*>(smem)[(t * 2 + (h ^ 1)) *
+                                                                      C::kRows + r];
       tmem_fence_after_sync();
-      const float inv = a.v_scale / l_run;  // v_scale: 1, or the FP8 pool's V scale
-      const int64_t pidx = (static_cast<int64_t>(row0 + tok) * a.num_q_heads + g * a.group + hg) *
-                               a.max_parts + blockIdx.z;
-      if (rv) {
-        a.part_m[pidx] = m_run;
-        a.part_l[pidx] = l_run;
-      }
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t tt[32];
-        tmem_ld32(obuf + c0, tt);
-        tmem_wait_ld();
-        tmem_regs_ready(tt);
-        if (rv) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            *reinterpret_cast<float4*>(a.part_o + pidx * D + c0 + c) =
-                make_float4(__uint_as_float(tt[c]) * inv, __uint_as_float(tt[c + 1]) * inv,
-                            __uint_as_float(tt[c + 2]) * inv, __uint_as_float(tt[c + 3]) * inv);
+      const float inv = a.v_scale / l_all;  // v_scale: 1, or the FP8 pool's V scale
+      if constexpr (CASCADE) {
+        const int64_t pidx =
+            (static_cast<int64_t>(row0 + tok) * a.num_q_heads + g * a.group + hg) * a.max_parts +
+            blockIdx.z;
+        if (rv && h == 0) {
+          a.part_m[pidx] = m_run;
+          a.part_l[pidx] = l_all;
         }
-      }
-    } else if (!CASCADE && !__any_sync(0xffffffffu, !ok)) {
-      tmem_fence_after_sync();
-      const float inv = a.v_scale / l_run;  // v_scale: 1, or the FP8 pool's V scale
-      __half* dst = a.out + (static_cast<int64_t>(row0 + tok) * a.num_q_heads + g * a.group + hg) * D;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t tt[32];
-        tmem_ld32(obuf + c0, tt);
-        tmem_wait_ld();
-        tmem_regs_ready(tt);
-        if (rv) {
+        for (int c0 = 0; c0 < kHalfD; c0 += 16) {
+          uint32_t tt[16];
+          tmem_ld16(obuf + c0, tt);
+          tmem_wait_ld();
+          tmem_regs_ready(tt);
+          if (rv) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 v;
-            v.x = pack2<BF>(__uint_as_float(tt[c]) * inv, __uint_as_float(tt[c + 1]) * inv);
-            v.y = pack2<BF>(__uint_as_float(tt[c + 2]) * inv, __uint_as_float(tt[c + 3]) * inv);
-            v.z = pack2<BF>(__uint_as_float(tt[c + 4]) * inv, __uint_as_float(tt[c + 5]) * inv);
-            v.w = pack2<BF>(__uint_as_float(tt[c + 6]) * inv, __uint_as_float(tt[c + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + c0 + c) = v;
+            for (int c = 0; c < 16; c += 4)
+              *reinterpret_cast<float4*>(a.part_o + pidx * D + h * kHalfD + c0 + c) =
+                  make_float4(__uint_as_float(tt[c]) * inv, __uint_as_float(tt[c + 1]) * inv,
+                              __uint_as_float(tt[c + 2]) * inv, __uint_as_float(tt[c + 3]) * inv);
+          }
+        }
+      } else {
+        __half* dst = a.out + (static_cast<int64_t>(row0 + tok) * a.num_q_heads + g * a.group +
+                               hg) * D + h * kHalfD;
+#pragma unroll
+        for (int c0 = 0; c0 < kHalfD; c0 += 16) {
+          uint32_t tt[16];
+          tmem_ld16(obuf + c0, tt);
+          tmem_wait_ld();
+          tmem_regs_ready(tt);
+          if (rv) {
+#pragma unroll
+            for (int c = 0; c < 16; c += 8) {
+              uint4 v;
+              v.x = pack2<BF>(__uint_as_float(tt[c]) * inv, __uint_as_float(tt[c + 1]) * inv);
+              v.y = pack2<BF>(__uint_as_float(tt[c + 2]) * inv, __uint_as_float(tt[c + 3]) * inv);
+              v.z = pack2<BF>(__uint_as_float(tt[c + 4]) * inv, __uint_as_float(tt[c + 5]) * inv);
+              v.w = pack2<BF>(__uint_as_float(tt[c + 6]) * inv, __uint_as_float(tt[c + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + c0 + c) = v;
+            }
           }
         }
       }
@@ -786,6 +829,7 @@ struct ParityCfg {
   static constexpr int kThreads = kSoftmax + 4 * 32;
   // Registers: launched at 168 per thread (384 x 168 = 64512); the producer warpgroup gives
   // back down to 72 and the two softmax warpgroups take 216: 256 x 216 + 128 x 72 = 64512.
+  static constexpr int kLaunchRegs = 168;
   static constexpr int kRegsSoftmax = 216;
   static constexpr int kRegsOther = 72;
   // TMEM columns: S/P of even tiles [0,128), of odd tiles [128,256), O_even, O_odd from 256.
@@ -910,7 +954,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
 
   constexpr int kKWarp = C::kSoftmax / 32, kVWarp = kKWarp + 1, kMmaWarp = kKWarp + 2;
   static_assert(C::kRegsSoftmax * C::kSoftmax + C::kRegsOther * (C::kThreads - C::kSoftmax) <=
-                    168 * C::kThreads,
+                    C::kLaunchRegs * C::kThreads,
                 "register split exceeds the launch allocation");
   if (warp >= kKWarp) {
   // ================================================ producer / MMA warpgroup (warps 8-11)
@@ -1213,7 +1257,8 @@ cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const
   cudaFuncAttributes attr{};
   if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
   if (attr.numRegs * C::kThreads < C::kRegsSoftmax * C::kSoftmax +
-                                       C::kRegsOther * (C::kThreads - C::kSoftmax))
+                                       C::kRegsOther * (C::kThreads - C::kSoftmax) ||
+      attr.numRegs * C::kThreads > 65536)
     return cudaErrorInvalidConfiguration;
   // Query tokens per CTA: whole tokens per Q tile (128 / group rounds down), times the tiles.
   const int rows_q = q_tiles * (C::kRows / a.group);
