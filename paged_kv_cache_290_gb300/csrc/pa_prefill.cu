@@ -1077,7 +1077,6 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
       // the exponent's FMA below); otherwise they are scaled here.  Masked keys become -inf.
       const int key0 = j * C::kKeys;
       const bool masked = !CASCADE && key0 + C::kKeys - 1 > min_pos;
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (prescale || masked) {
 #pragma unroll
         for (int c = 0; c < C::kKeys; ++c) {
@@ -1085,14 +1084,14 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
           if (prescale) v *= a.scale_log2;
           if (masked && key0 + c > pos) v = -INFINITY;
           sv[c >> 5][c & 31] = __float_as_uint(v);
-          m4[c & 3] = fmaxf(m4[c & 3], v);
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < C::kKeys; ++c)
-          m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c >> 5][c & 31]));
       }
-      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mul;
+      float m2[2] = {-INFINITY, -INFINITY};  // two chains of three-input maxima
+#pragma unroll
+      for (int c = 0; c < C::kKeys; c += 2)
+        m2[(c >> 1) & 1] = fmax3(m2[(c >> 1) & 1], __uint_as_float(sv[c >> 5][c & 31]),
+                                 __uint_as_float(sv[c >> 5][(c & 31) + 1]));
+      const float mx = fmaxf(m2[0], m2[1]) * mul;
       float alpha = 1.f;
       if (mx > m_run + C::kRescaleLog2 || (m_run == -INFINITY && mx > -INFINITY)) {
         alpha = ex2_approx(m_run - mx);  // 0 when m_run is still -inf
@@ -1114,20 +1113,31 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
       // P_j (fp16) -> TMEM columns 0..63 of the buffer, two keys per column; l keeps the
       // unrounded p.  A row with every key so far masked keeps m = -inf and gets p = 0.
       const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      // exponents and sums two keys at a time (packed fp32 pairs: the same roundings as fmaf
+      // and + per key)
+      const uint64_t mul2 = f32x2(mul, mul), negm2 = f32x2(neg_m, neg_m);
+      uint64_t ps2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
-      for (int q4 = 0; q4 < C::kKeys / 32; ++q4) {
-        uint32_t pk[16];
+      for (int q8 = 0; q8 < C::kKeys / 16; ++q8) {  // 16 keys -> 8 columns of P at a time
+        uint32_t pk[8];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c]), mul, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[q4][2 * c + 1]), mul, neg_m));
-          ps[c & 3] += p0 + p1;
+        for (int c = 0; c < 8; ++c) {
+          const int k = q8 * 16 + 2 * c;
+          float x0, x1;
+          f32x2_split(ffma2(f32x2(__uint_as_float(sv[k >> 5][k & 31]),
+                                  __uint_as_float(sv[k >> 5][(k & 31) + 1])),
+                            mul2, negm2),
+                      x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          ps2[c & 1] = fadd2(ps2[c & 1], f32x2(p0, p1));
           pk[c] = pack2<BF>(p0, p1);
         }
-        tmem_st16(sbuf + q4 * 16, pk);
+        tmem_st8(sbuf + q8 * 8, pk);
       }
-      l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      float s0, s1, s2, s3;
+      f32x2_split(ps2[0], s0, s1);
+      f32x2_split(ps2[1], s2, s3);
+      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
 
       const int tile0 = j * C::kKeys;
       if (!CASCADE && j == ntiles - 1 && tile0 + C::kKeys > kend) {
