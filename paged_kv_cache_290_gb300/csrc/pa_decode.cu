@@ -29,7 +29,8 @@
 // bfloat16 cache (with bf16 q and out): the fp16 data path with bf16 MMAs, P rounded to bf16
 // for the P V product, and bf16 outputs.
 // Both kernels are programmatic dependents of what precedes them on the stream: they may be
-// scheduled early but read nothing from global memory before griddepcontrol.wait.
+// scheduled early and read their inputs (descriptor, block table, q) at once, but nothing that
+// the kernel before them writes (the pools, the partials) before griddepcontrol.wait.
 #include <algorithm>
 
 #include "pa_common.cuh"
@@ -104,30 +105,35 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
   const int part = pidx + a.cascade_parts, g = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool lead = blockIdx.x == 0;  // reports the sequence's descriptor errors
-  grid_dependency_wait();  // everything the previous kernels wrote is visible from here on
+  // The kernel before this one on the stream (the scatter-write) writes only the pools: the
+  // descriptor, the block table and q are read before waiting for it, and only the K/V copies
+  // wait (griddepcontrol.wait below), so the first wave's set-up overlaps that kernel.
   grid_launch_dependents();
+  // A CTA that leaves early still waits first, so that this grid never completes before the
+  // one it depends on (the stream's order stays transitive for the launches after it).
+  auto leave = [] { grid_dependency_wait(); };
 
   const int row0 = a.query_start_loc[s];
   const int q_len = a.query_start_loc[s + 1] - row0;
   // decode rows, and verify rows (a few per sequence) when the call routes them here
-  if (q_len < 1 || q_len > a.verify_rows) return;
+  if (q_len < 1 || q_len > a.verify_rows) return leave();
   if (row0 < 0 || row0 + q_len > a.num_tokens) {
     if (lead && tid == 0) atomicOr(a.err, kErrDescriptor);
-    return;
+    return leave();
   }
   const int L = a.seq_lens[s];
   const int nparts = (L + kPartitionTokens - 1) / kPartitionTokens;
   if (L < q_len || (L + BS - 1) / BS > a.max_blocks) {
     if (lead && tid == 0) atomicOr(a.err, kErrDescriptor);
-    return;
+    return leave();
   }
   if (nparts > static_cast<int>(gridDim.x) / ncg + a.cascade_parts ||
       (q_len * a.group + 8 * NT - 1) / (8 * NT) > ncg) {
     if (lead && tid == 0) atomicOr(a.err, kErrHint);
-    return;
+    return leave();
   }
   const int ncols = q_len * a.group, col0 = cg * 8 * NT;
-  if (col0 >= ncols) return;
+  if (col0 >= ncols) return leave();
   const int ctx = L - q_len;  // row i sees keys 0 .. ctx + i
   if (a.cascade_parts > 0 && pidx == 0 && cg == 0 && g == 0) {
     // With a shared prefix, the row must have keys past it, and its table must hold sequence
@@ -138,7 +144,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
       differs |= a.block_tables[static_cast<int64_t>(s) * a.bt_stride + j] != a.block_tables[j];
     if (__syncthreads_or(differs) && tid == 0) atomicOr(a.err, kErrDescriptor);
   }
-  if (part >= nparts) return;
+  if (part >= nparts) return leave();
 
   const int tok_begin = part * kPartitionTokens;
   const int tok_end = min(L, tok_begin + kPartitionTokens);
@@ -163,7 +169,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0) atomicOr(a.err, kErrBlockRange);
-    return;
+    return leave();
   }
 
   const int my_n = warp < nunits ? (nunits - warp + C::kWarps - 1) / C::kWarps : 0;
@@ -188,11 +194,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
       }
     }
   };
-  if (lane == 0) {
-    const int n0 = my_n < C::kStages ? my_n : C::kStages;
-    for (int i = 0; i < n0; ++i) issue(i);
-  }
-
   // Q^T as the B operand (k = head_dim, n = this CTA's columns), kept in registers.
   const int gq = lane >> 2, cq = lane & 3;
   uint32_t qf[NT][C::kDK][2];
@@ -209,6 +210,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
       qf[nt][j][0] = hv ? ldg_u32(qrow + j * 16 + (F8 ? 4 * cq : 2 * cq)) : 0u;
       qf[nt][j][1] = hv ? ldg_u32(qrow + j * 16 + (F8 ? 4 * cq + 2 : 8 + 2 * cq)) : 0u;
     }
+  }
+
+  grid_dependency_wait();  // the pools now hold everything the previous kernels wrote
+  if (lane == 0) {
+    const int n0 = my_n < C::kStages ? my_n : C::kStages;
+    for (int i = 0; i < n0; ++i) issue(i);
   }
 
   // Last key position each of this lane's accumulator columns (2cq, 2cq + 1 of each 8) may see:
@@ -475,23 +482,24 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
 // holds l = 0, O = 0 and weighs nothing.
 template <int D, bool BF>
 __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a) {
-  grid_dependency_wait();  // the partials come from the decode kernel just before
   grid_launch_dependents();
+  auto leave = [] { grid_dependency_wait(); };  // as in the decode kernel
   const int s = blockIdx.y, qi = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.x * 4 + warp;
-  if (hq >= a.num_q_heads) return;
+  if (hq >= a.num_q_heads) return leave();
   const int row0 = a.query_start_loc[s], row1 = a.query_start_loc[s + 1];
   const int L = a.seq_lens[s];
   const int q_len = row1 - row0;
   if (q_len < 1 || q_len > a.verify_rows || qi >= q_len || row0 < 0 || row1 > a.num_tokens ||
       L < q_len)
-    return;
+    return leave();
   const int nparts = (L + kPartitionTokens - 1) / kPartitionTokens;
   if (nparts <= 1 || nparts > a.max_parts || (L + a.block_size - 1) / a.block_size > a.max_blocks)
-    return;
+    return leave();
   const int row = row0 + qi;
   const int64_t base = (static_cast<int64_t>(row) * a.num_q_heads + hq) * a.max_parts;
+  grid_dependency_wait();  // the partials come from the kernels before (descriptor: an input)
 
   constexpr int V = D / 32;   // output elements per lane
   constexpr int kBatch = 16;  // partitions whose O rows are in flight at once
