@@ -27,7 +27,8 @@
  *   - Host-checkable errors are returned synchronously and nothing is launched.  Device-data
  *     errors (a slot or block id outside the pool, query_len > seq_len, a sequence longer than
  *     the hint) make the affected work item skip its memory accesses, set a bit in a device
- *     error word and leave its output rows unwritten; pa_get_device_error reports them.
+ *     error word (the device's, or the stream's own: pa_set_stream_error_word) and leave its
+ *     output rows unwritten; pa_get_device_error reports them.
  *   - Every wait inside a kernel gives up after two seconds (pa_set_wait_limit) and reports
  *     PA_ERR_TIMEOUT.
  *   - Thread-safety: functions may be called from several host threads; pa_last_error is
@@ -230,12 +231,26 @@ int pa_attention_static_scratch(const pa_tensor* q, const pa_tensor* k_cache,
 const char* pa_last_error(void);
 
 /*
- * pa_get_device_error -- synchronise `stream`, then read and clear the device error word of
- * the current device.  Returns PA_OK, PA_ERR_TIMEOUT, PA_ERR_OUT_OF_RANGE or PA_ERR_DESCRIPTOR
- * (most severe first); *bits (may be NULL) receives the raw word: 1 timeout, 2 slot out of
- * range, 4 block id out of range, 8 descriptor, 16 hint exceeded.
+ * pa_get_device_error -- synchronise `stream`, then read and clear the error word that calls on
+ * `stream` report into: the word registered for it with pa_set_stream_error_word, else the
+ * current device's own word (shared by every unregistered stream of the device).  Returns PA_OK,
+ * PA_ERR_TIMEOUT, PA_ERR_OUT_OF_RANGE or PA_ERR_DESCRIPTOR (most severe first); *bits (may be
+ * NULL) receives the raw word: 1 timeout, 2 slot out of range, 4 block id out of range,
+ * 8 descriptor, 16 hint exceeded.
  */
 int pa_get_device_error(void* stream, uint32_t* bits);
+
+/*
+ * pa_set_stream_error_word -- let later calls on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream) report their device errors into `device_word` instead of the device's shared
+ * word, so that a caller serving several streams reads each stream's errors apart.  The word is
+ * a caller-owned, 4-byte aligned device uint32 that the caller zeroes first; the library only
+ * ORs bits into it and pa_get_device_error(stream, ...) clears it.  NULL turns the stream back
+ * to the device's word.  The word must stay allocated while calls registered to it can run.  At
+ * most 64 streams hold a word of their own at a time (PA_ERR_INVALID_ARG beyond, and for a
+ * misaligned word).  Any host thread may register; the registration is process-wide.
+ */
+int pa_set_stream_error_word(void* stream, uint32_t* device_word);
 
 /*
  * pa_copy_blocks -- copy whole physical blocks of the pool: K and V of every kv head of block

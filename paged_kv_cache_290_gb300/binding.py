@@ -39,7 +39,7 @@ EXPORTED = ("pa_reshape_and_cache", "pa_attention_workspace_size", "pa_attention
             "pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_append",
             "pa_bm_truncate", "pa_bm_fork", "pa_bm_free", "pa_bm_stats", "pa_bm_sequence",
             "pa_bm_step_descriptor", "pa_step_slot_mapping", "pa_set_wait_limit",
-            "pa_selftest_wait_timeout")
+            "pa_selftest_wait_timeout", "pa_set_stream_error_word")
 
 # Byte tensors are E4M3 codes (the only one-byte type of the ABI).
 _DTYPES = {torch.float16: PA_F16, torch.int32: PA_I32, torch.int64: PA_I64,
@@ -96,6 +96,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                                     ctypes.POINTER(PABatchHint), ctypes.c_void_p]
         lib.pa_set_wait_limit.restype = ctypes.c_int
         lib.pa_set_wait_limit.argtypes = [ctypes.c_uint64]
+        lib.pa_set_stream_error_word.restype = ctypes.c_int
+        lib.pa_set_stream_error_word.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
         lib.pa_selftest_wait_timeout.restype = ctypes.c_int
         lib.pa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, ctypes.c_void_p]
         lib.pa_set_timing_events.restype = ctypes.c_int
@@ -251,6 +253,16 @@ def set_wait_limit(limit_ns: int) -> None:
     """``pa_set_wait_limit``: how long any wait inside later attention kernels of this thread
     may last before it gives up and reports PA_ERR_TIMEOUT (default 2 s)."""
     _check(load_library().pa_set_wait_limit(int(limit_ns)))
+
+
+def set_stream_error_word(stream, word: Optional[torch.Tensor]) -> None:
+    """``pa_set_stream_error_word``: later calls on ``stream`` report device errors into ``word``
+    (a zeroed one-element int32 device tensor the caller keeps alive), read back by
+    ``get_device_error(stream)``; ``None`` returns the stream to the device's shared word."""
+    if word is not None and (word.dtype != torch.int32 or word.numel() < 1 or not word.is_cuda):
+        raise ValueError("the error word must be a one-element int32 device tensor")
+    _check(load_library().pa_set_stream_error_word(
+        _stream_handle(stream), word.data_ptr() if word is not None else None))
 
 
 def get_device_error(stream=None):

@@ -57,6 +57,30 @@ cudaError_t device_error_word(unsigned** out) {
   return cudaSuccess;
 }
 
+// Error words of streams whose caller registered one (pa_set_stream_error_word): the kernels of
+// a call on such a stream report into that word instead of the device's.  A few dozen entries,
+// looked up under a mutex once per call.
+constexpr int kMaxStreamWords = 64;
+struct StreamWord {
+  void* stream = nullptr;
+  unsigned* word = nullptr;
+};
+std::mutex g_stream_mu;
+StreamWord g_stream_words[kMaxStreamWords];
+
+// The word a call on `stream` reports into: the stream's own, else the current device's.
+cudaError_t error_word_for(void* stream, unsigned** out) {
+  {
+    std::lock_guard<std::mutex> lk(g_stream_mu);
+    for (const StreamWord& w : g_stream_words)
+      if (w.word && w.stream == stream) {
+        *out = w.word;
+        return cudaSuccess;
+      }
+  }
+  return device_error_word(out);
+}
+
 // A side stream (highest priority) and two events per device and host thread: a call with both
 // prefill chunks and decode rows runs the prefill kernel there, beside the decode and merge
 // kernels on the caller's stream (fork and join through the events), so the HBM-bound decode
@@ -242,7 +266,7 @@ WorkspaceLayout workspace_layout(int64_t t, int64_t hq, int64_t d, int32_t max_s
 
 namespace pa {
 int set_last_error(int status, const std::string& message) { return fail(status, message); }
-cudaError_t error_word(unsigned** out) { return device_error_word(out); }
+cudaError_t error_word(void* stream, unsigned** out) { return error_word_for(stream, out); }
 }  // namespace pa
 
 extern "C" {
@@ -307,7 +331,7 @@ static int reshape_impl(const pa_tensor* k, const pa_tensor* v, const pa_tensor*
   a.head_dim = static_cast<int>(d);
   a.block_size = static_cast<int>(k_cache->shape[2]);
   a.num_blocks = k_cache->shape[0];
-  cudaError_t e = device_error_word(&a.err);
+  cudaError_t e = error_word_for(stream, &a.err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
   e = pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
@@ -342,7 +366,7 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_
   a.num_pairs = pairs->shape[0];
   a.chunks_per_block = k_cache->shape[1] * k_cache->shape[2] * k_cache->shape[3] / (fp8 ? 16 : 8);
   a.num_blocks = k_cache->shape[0];
-  cudaError_t e = device_error_word(&a.err);
+  cudaError_t e = error_word_for(stream, &a.err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
   e = pa::launch_copy_blocks(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
@@ -468,7 +492,7 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
   a.bf16 = in_dt == PA_BF16 ? 1 : 0;
   a.cascade_parts = sp / PA_PARTITION_TOKENS;
   a.wait_limit_ns = g_wait_limit_ns;
-  cudaError_t e = device_error_word(&a.err);
+  cudaError_t e = error_word_for(stream, &a.err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
   if (a.cascade_parts > 0 && (e = device_sm_count(&a.num_sms)) != cudaSuccess)
     return cuda_fail(e, "device attribute");
@@ -579,12 +603,38 @@ int pa_set_wait_limit(uint64_t limit_ns) {
   return PA_OK;
 }
 
+int pa_set_stream_error_word(void* stream, uint32_t* device_word) {
+  g_last_error.clear();
+  if (device_word && (reinterpret_cast<uintptr_t>(device_word) & 3u))
+    return fail(PA_ERR_INVALID_ARG, "the error word must be 4-byte aligned");
+  std::lock_guard<std::mutex> lk(g_stream_mu);
+  StreamWord* slot = nullptr;
+  for (StreamWord& w : g_stream_words)
+    if (w.word && w.stream == stream) slot = &w;
+  if (!device_word) {  // back to the device's word
+    if (slot) *slot = StreamWord{};
+    return PA_OK;
+  }
+  if (!slot)
+    for (StreamWord& w : g_stream_words)
+      if (!w.word) {
+        slot = &w;
+        break;
+      }
+  if (!slot)
+    return fail(PA_ERR_INVALID_ARG, "already " + std::to_string(kMaxStreamWords) +
+                                        " streams hold an error word of their own");
+  slot->stream = stream;
+  slot->word = reinterpret_cast<unsigned*>(device_word);
+  return PA_OK;
+}
+
 int pa_get_device_error(void* stream, uint32_t* bits) {
   g_last_error.clear();
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
   unsigned* p = nullptr;
-  e = device_error_word(&p);
+  e = error_word_for(stream, &p);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
   unsigned w = 0;
   e = cudaMemcpy(&w, p, sizeof(w), cudaMemcpyDeviceToHost);

@@ -73,8 +73,9 @@ struct AttnArgs {
 // Sets the message pa_last_error() returns on this host thread; returns `status`.
 int set_last_error(int status, const std::string& message);
 
-// Device address of the current device's error word (looked up once per device).
-cudaError_t error_word(unsigned** out);
+// Device address of the error word a call on `stream` reports into: the word the caller
+// registered for that stream, else the current device's (looked up once per device).
+cudaError_t error_word(void* stream, unsigned** out);
 
 // Whole-block copies (copy-on-write of shared blocks).
 struct CopyArgs {

@@ -32,7 +32,7 @@ extern "C" int pa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
                                                       std::to_string(PA_WAIT_LIMIT_MIN_NS) +
                                                       ", 100000000] ns");
   unsigned* err = nullptr;
-  cudaError_t e = pa::error_word(&err);
+  cudaError_t e = pa::error_word(stream, &err);
   if (e != cudaSuccess)
     return pa::set_last_error(PA_ERR_CUDA, std::string("error word: ") + cudaGetErrorString(e));
   wait_without_arrival_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, limit_ns);

@@ -278,3 +278,22 @@ def test_reshape_fp8_checks_scales_and_dtype(lib):
                                         T(B.PA_F8E4M3, [nb, hkv, bs, d]), T(B.PA_I64, [0]))]
     ok = ctypes.byref(B.PAKVScales(0.5, 0.25))
     assert lib.pa_reshape_and_cache_fp8(*empty, ok, None) == B.PA_OK
+
+
+def test_stream_error_word_registry(lib):
+    # fake stream handles and word addresses: registration touches no device memory
+    words = [0x100000 + 16 * i for i in range(65)]
+    try:
+        for i in range(64):
+            assert lib.pa_set_stream_error_word(0x5000 + i, words[i]) == B.PA_OK
+        assert lib.pa_set_stream_error_word(0x5000 + 64, words[64]) == B.PA_ERR_INVALID_ARG
+        assert "64 streams" in msg(lib)
+        # re-registering a stream replaces its word; releasing one frees a place
+        assert lib.pa_set_stream_error_word(0x5000 + 3, words[64]) == B.PA_OK
+        assert lib.pa_set_stream_error_word(0x5000 + 7, None) == B.PA_OK
+        assert lib.pa_set_stream_error_word(0x5000 + 64, words[7]) == B.PA_OK
+        assert lib.pa_set_stream_error_word(0x6000, 0x100002) == B.PA_ERR_INVALID_ARG  # misaligned
+        assert "aligned" in msg(lib)
+    finally:
+        for i in range(65):
+            lib.pa_set_stream_error_word(0x5000 + i, None)
