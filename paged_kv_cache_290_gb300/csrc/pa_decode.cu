@@ -29,8 +29,8 @@
 // bfloat16 cache (with bf16 q and out): the fp16 data path with bf16 MMAs, P rounded to bf16
 // for the P V product, and bf16 outputs.
 // Both kernels are programmatic dependents of what precedes them on the stream: they may be
-// scheduled early and read their inputs (descriptor, block table, q) at once, but nothing that
-// the kernel before them writes (the pools, the partials) before griddepcontrol.wait.
+// scheduled early and read their descriptor and block table at once, but nothing that the
+// kernel before them writes (the pools, the partials) before griddepcontrol.wait.
 #include <algorithm>
 
 #include "pa_common.cuh"
@@ -106,8 +106,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool lead = blockIdx.x == 0;  // reports the sequence's descriptor errors
   // The kernel before this one on the stream (the scatter-write) writes only the pools: the
-  // descriptor, the block table and q are read before waiting for it, and only the K/V copies
-  // wait (griddepcontrol.wait below), so the first wave's set-up overlaps that kernel.
+  // descriptor and the block table are read before waiting for it, and only the K/V copies wait
+  // (griddepcontrol.wait below), so the first wave's set-up overlaps that kernel.  q is read
+  // after the first copies are issued, while they are in flight.
   grid_launch_dependents();
   // A CTA that leaves early still waits first, so that this grid never completes before the
   // one it depends on (the stream's order stays transitive for the launches after it).
@@ -194,6 +195,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
       }
     }
   };
+  grid_dependency_wait();  // the pools now hold everything the previous kernels wrote
+  if (lane == 0) {
+    const int n0 = my_n < C::kStages ? my_n : C::kStages;
+    for (int i = 0; i < n0; ++i) issue(i);
+  }
+
   // Q^T as the B operand (k = head_dim, n = this CTA's columns), kept in registers.
   const int gq = lane >> 2, cq = lane & 3;
   uint32_t qf[NT][C::kDK][2];
@@ -210,12 +217,6 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
       qf[nt][j][0] = hv ? ldg_u32(qrow + j * 16 + (F8 ? 4 * cq : 2 * cq)) : 0u;
       qf[nt][j][1] = hv ? ldg_u32(qrow + j * 16 + (F8 ? 4 * cq + 2 : 8 + 2 * cq)) : 0u;
     }
-  }
-
-  grid_dependency_wait();  // the pools now hold everything the previous kernels wrote
-  if (lane == 0) {
-    const int n0 = my_n < C::kStages ? my_n : C::kStages;
-    for (int i = 0; i < n0; ++i) issue(i);
   }
 
   // Last key position each of this lane's accumulator columns (2cq, 2cq + 1 of each 8) may see:
