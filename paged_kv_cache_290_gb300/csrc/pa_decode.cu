@@ -8,8 +8,9 @@
 // Data path per CTA (4 warps, each with a private ring of shared-memory stages):
 //   * the partition's block ids are read from the block table once (block -> TMA row),
 //   * each 16-token unit of K and of V (one or two 128-byte swizzled boxes per token row) is
-//     fetched by a 2-D TMA tensor load that completes on the stage's mbarrier; warp w takes
-//     units w, w+4, w+8, ... so one partition keeps 4 x stages loads in flight per CTA,
+//     fetched by a 2-D TMA tensor load that completes on the stage's mbarrier (its lines enter
+//     L2 as the first to evict: they are read once); warp w takes units w, w+4, w+8, ... so one
+//     partition keeps 4 x stages loads in flight per CTA,
 //   * S^T = K Q^T on tensor cores (m16n8k16: 16 tokens x 8 heads x 16 dims), scores scaled by
 //     scale*log2(e), masked past seq_len with a select (never arithmetic), online softmax
 //     (running max / sum per head, exp2), P^T moved into the B-operand layout by movmatrix,
@@ -177,6 +178,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
   const uint32_t ring = smem_addr(smem + warp * (C::kStages * C::kStageBytes));
   const uint32_t bar0 = smem_addr(&bars[warp][0]);
 
+  // Every K/V line is read by this CTA alone, once: it goes into L2 as the first to evict, so
+  // the stream does not push out what is read again (the partials the merge reads, the K/V
+  // tiles a prefill grid beside this one shares among its CTAs, the block tables).
+  const uint64_t pol = l2_policy_evict_first();
+  auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y, uint32_t bar) {
+    tma_load_2d_hint(dst, m, x, y, bar, pol);
+  };
   auto issue = [&](int i) {  // lane 0: fetch unit i of this warp into stage i % kStages
     const int u = warp + i * C::kWarps;
     const int st = i % C::kStages;
@@ -185,13 +193,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
     const int y = unit_row[u];
     mbar_arrive_expect_tx(bar, C::kStageBytes);
     if constexpr (F8) {  // one box of 16 rows x D bytes each
-      tma_load_2d(kdst, &kmap, 0, y, bar);
-      tma_load_2d(kdst + C::kKBytes, &vmap, 0, y, bar);
+      load(kdst, &kmap, 0, y, bar);
+      load(kdst + C::kKBytes, &vmap, 0, y, bar);
     } else {
 #pragma unroll
       for (int h = 0; h < C::kHalves; ++h) {
-        tma_load_2d(kdst + h * C::kBoxBytes, &kmap, h * 64, y, bar);
-        tma_load_2d(kdst + C::kKBytes + h * C::kBoxBytes, &vmap, h * 64, y, bar);
+        load(kdst + h * C::kBoxBytes, &kmap, h * 64, y, bar);
+        load(kdst + C::kKBytes + h * C::kBoxBytes, &vmap, h * 64, y, bar);
       }
     }
   };

@@ -120,11 +120,14 @@ __device__ __forceinline__ int find_prefill_seq_longest_first(const AttnArgs& a,
 // A producer warp: streams the K (or V) tiles 0 .. ntiles-1 of sequence s, kv head g, keys
 // [key_base, kend), into a ring of `stages` stages of kKVBytes each.  Each 16-token unit is found
 // through the block table and fetched as 128-byte-swizzled TMA boxes (one per 64 columns).
+// read_once: no other CTA reads these K/V (one CTA per sequence and kv head), so their lines
+// enter L2 as the first to evict; the two-tile kernel's CTAs share every tile and keep the default.
 // Before returning it waits (bounded) for its last copies, so none lands after the CTA retires.
 template <int D, int BS, int kKeys>
 __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap* map, int s, int g,
                                            int kend, int ntiles, int stages, uint64_t* full,
-                                           uint64_t* empty, uint32_t ring, int key_base = 0) {
+                                           uint64_t* empty, uint32_t ring, int key_base,
+                                           bool read_once) {
   constexpr int kUnits = kKeys / 16, kHalves = D / 64, kKVBytes = kHalves * kKeys * 128;
   const int lane = threadIdx.x & 31;
   // Block id of unit `lane` of tile j (0 past the keys).  The ids of tile j + 1 are loaded while
@@ -136,6 +139,7 @@ __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap*
                ? a.block_tables[static_cast<int64_t>(s) * a.bt_stride + (key0 + 16 * lane) / BS]
                : 0;
   };
+  const uint64_t pol = l2_policy_evict_first();  // for K/V no other CTA reads
   int issued = 0;
   int id_next = ntiles > 0 ? unit_block(0) : 0;
   for (int j = 0; j < ntiles; ++j) {
@@ -156,8 +160,12 @@ __device__ __forceinline__ void produce_kv(const AttnArgs& a, const CUtensorMap*
       if (lane == 0) {
         const int y = (blk * a.num_kv_heads + g) * BS + ((key0 + 16 * u) % BS);
 #pragma unroll
-        for (int h = 0; h < kHalves; ++h)
-          tma_load_2d(dst + h * (kKeys * 128) + u * 2048, map, h * 64, y, bar);
+        for (int h = 0; h < kHalves; ++h) {
+          if (read_once)
+            tma_load_2d_hint(dst + h * (kKeys * 128) + u * 2048, map, h * 64, y, bar, pol);
+          else
+            tma_load_2d(dst + h * (kKeys * 128) + u * 2048, map, h * 64, y, bar);
+        }
       }
     }
     issued = j + 1;
@@ -204,7 +212,8 @@ __device__ __forceinline__ void widen_rows_f8(uint32_t dst, int rows, int p0, in
   }
 }
 
-// The same producer over an FP8 (E4M3) pool, with no extra shared memory: a tile's codes
+// The same producer over an FP8 (E4M3) pool (read_once as above), with no extra shared memory: a
+// tile's codes
 // (16-row TMA boxes of D bytes, 128-byte swizzled for D = 128, plain 64-byte rows for D = 64)
 // land in the upper half of the tile's own fp16 stage, completing on the stage's `land`
 // barrier, and the warp widens them in place (exact: every E4M3 value is an fp16 value) into
@@ -249,7 +258,7 @@ template <int D, int BS, int kKeys>
 __device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorMap* map, int s,
                                               int g, int kend, int ntiles, int stages,
                                               uint64_t* full, uint64_t* empty, uint32_t ring,
-                                              uint64_t* land, int key_base) {
+                                              uint64_t* land, int key_base, bool read_once) {
   constexpr int kUnits = kKeys / 16, kKVBytes = (D / 64) * kKeys * 128, kUnit8 = 16 * D;
   constexpr int kCodes = kKVBytes / 2;  // where a stage's codes land
   const int lane = threadIdx.x & 31;
@@ -260,6 +269,7 @@ __device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorM
                ? a.block_tables[static_cast<int64_t>(s) * a.bt_stride + (key0 + 16 * lane) / BS]
                : 0;
   };
+  const uint64_t pol = l2_policy_evict_first();  // for K/V no other CTA reads
   // tile j's codes -> the upper half of its stage, completing on land[stage]
   auto fetch = [&](int j, int id) {
     const int st = j % stages, key0 = key_base + j * kKeys, units = units_of(j);
@@ -268,9 +278,13 @@ __device__ __forceinline__ void produce_kv_f8(const AttnArgs& a, const CUtensorM
     if (lane == 0) mbar_arrive_expect_tx(bar, units * kUnit8);
     for (int u = 0; u < units; ++u) {
       const int blk = __shfl_sync(0xffffffffu, id, u);
-      if (lane == 0)
-        tma_load_2d(dst + u * kUnit8, map, 0,
-                    (blk * a.num_kv_heads + g) * BS + ((key0 + 16 * u) % BS), bar);
+      if (lane == 0) {
+        const int y = (blk * a.num_kv_heads + g) * BS + ((key0 + 16 * u) % BS);
+        if (read_once)
+          tma_load_2d_hint(dst + u * kUnit8, map, 0, y, bar, pol);
+        else
+          tma_load_2d(dst + u * kUnit8, map, 0, y, bar);
+      }
     }
   };
   // tile j (landed) widened in place; false when a wait gave up
@@ -490,11 +504,11 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       produce_kv_f8<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
                                      is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
                                      is_v ? v_empty : k_empty, is_v ? v_s : k_s,
-                                     land[is_v ? 1 : 0], key_base);
+                                     land[is_v ? 1 : 0], key_base, false);
     else
       produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
                                   is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
-                                  is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base);
+                                  is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base, false);
   } else if (warp == kMmaWarp && lane == 0) {
     // ============================================================== MMA issuer (one thread)
     constexpr uint32_t kIdS = umma_idesc_f16(C::kRows, C::kKeys, 0, 0, BF);
@@ -966,11 +980,13 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
       produce_kv_f8<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
                                      is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
                                      is_v ? v_empty : k_empty, is_v ? v_s : k_s,
-                                     land[is_v ? 1 : 0], key_base);
+                                     land[is_v ? 1 : 0], key_base,
+                                     !CASCADE);
     else
       produce_kv<D, BS, C::kKeys>(a, is_v ? &vmap : &kmap, s, g, kend, ntiles,
                                   is_v ? C::kVStages : C::kKStages, is_v ? v_full : k_full,
-                                  is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base);
+                                  is_v ? v_empty : k_empty, is_v ? v_s : k_s, key_base,
+                                  !CASCADE);
   } else if (warp == kMmaWarp && lane == 0) {
     // ============================================================== MMA issuer (one thread)
     // Issuing a tcgen05.mma waits until the pipe takes it and the pipe queues almost nothing,
