@@ -212,10 +212,9 @@ __device__ __forceinline__ void widen_rows_f8(uint32_t dst, int rows, int p0, in
   }
 }
 
-// The same producer over an FP8 (E4M3) pool (read_once as above), with no extra shared memory: a
-// tile's codes
-// (16-row TMA boxes of D bytes, 128-byte swizzled for D = 128, plain 64-byte rows for D = 64)
-// land in the upper half of the tile's own fp16 stage, completing on the stage's `land`
+// The same producer over an FP8 (E4M3) pool (read_once as above), with no extra shared memory:
+// a tile's codes (16-row TMA boxes of D bytes, 128-byte swizzled for D = 128, plain 64-byte rows
+// for D = 64) land in the upper half of the tile's own fp16 stage, completing on the stage's `land`
 // barrier, and the warp widens them in place (exact: every E4M3 value is an fp16 value) into
 // the 128-byte-swizzled [64-column chunk][key][128 B] layout of an fp16 tile, one key row per
 // lane.  In place is safe: for D = 128 row k's fp16 bytes cover exactly row k's own codes,
