@@ -115,15 +115,25 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
   // one it depends on (the stream's order stays transitive for the launches after it).
   auto leave = [] { grid_dependency_wait(); };
 
+  // One round of loads: the row range, the length, and the block ids of this partition's units
+  // (thread u: unit u), read before the length is known: every column inside the table is a
+  // valid address, and ids past the sequence's keys are never used.
   const int row0 = a.query_start_loc[s];
-  const int q_len = a.query_start_loc[s + 1] - row0;
+  const int row_end = a.query_start_loc[s + 1];
+  const int L = a.seq_lens[s];
+  int32_t unit_blk = 0;
+  {
+    const int col = (part * kPartitionTokens + tid * 16) / BS;
+    if (tid < C::kUnitsPerPart && col < a.max_blocks)
+      unit_blk = a.block_tables[static_cast<int64_t>(s) * a.bt_stride + col];
+  }
+  const int q_len = row_end - row0;
   // decode rows, and verify rows (a few per sequence) when the call routes them here
   if (q_len < 1 || q_len > a.verify_rows) return leave();
   if (row0 < 0 || row0 + q_len > a.num_tokens) {
     if (lead && tid == 0) atomicOr(a.err, kErrDescriptor);
     return leave();
   }
-  const int L = a.seq_lens[s];
   const int nparts = (L + kPartitionTokens - 1) / kPartitionTokens;
   if (L < q_len || (L + BS - 1) / BS > a.max_blocks) {
     if (lead && tid == 0) atomicOr(a.err, kErrDescriptor);
@@ -152,17 +162,17 @@ __global__ void __launch_bounds__(DecodeCfg<D, BS, NT, KV == kKvE4M3>::kThreads,
   const int tok_end = min(L, tok_begin + kPartitionTokens);
   const int nunits = (tok_end - tok_begin + 15) >> 4;
 
-  // Block table -> TMA row of every unit of the partition; ids outside the pool stop the CTA.
+  // Block id -> TMA row of every unit of the partition; ids outside the pool stop the CTA.
+  static_assert(C::kUnitsPerPart <= C::kThreads, "one thread per unit");
   int bad = 0;
-  for (int u = tid; u < nunits; u += C::kThreads) {
-    const int tok = tok_begin + u * 16;
-    const int32_t blk = a.block_tables[static_cast<int64_t>(s) * a.bt_stride + tok / BS];
+  if (tid < nunits) {
+    const int tok = tok_begin + tid * 16;
     int y = 0;
-    if (blk >= 0 && blk < a.num_blocks)
-      y = (blk * a.num_kv_heads + g) * BS + (tok % BS);
+    if (unit_blk >= 0 && unit_blk < a.num_blocks)
+      y = (unit_blk * a.num_kv_heads + g) * BS + (tok % BS);
     else
       bad = 1;
-    unit_row[u] = y;
+    unit_row[tid] = y;
   }
   if (lane == 0) {
 #pragma unroll
