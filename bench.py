@@ -140,17 +140,31 @@ def all_prefill(b) -> bool:
     return not verify_path(b) and b.max_query_len > 1 and b.num_prefill_seqs == b.num_seqs
 
 
+def prefill_slice_ctas(b, num_sms: int = 152) -> int:
+    """CTAs per launch of the two-tile prefill kernel beside decode rows, as pa_attention chooses
+    them (0: one full grid): two thirds of the SMs when the decode rows' estimated SM time is at
+    least 0.8 of the prefill rows' ((decode rows / prefill rows) / G x 70, halved over FP8)."""
+    group = b.num_q_heads // b.num_kv_heads
+    decode_rows = b.num_seqs - b.num_prefill_seqs
+    prefill_rows = max(b.num_tokens - decode_rows, 1)
+    r = decode_rows / prefill_rows / group * 70.0 * (0.5 if b.kv_dtype == "e4m3" else 1.0)
+    return num_sms * 2 // 3 if r >= 0.8 else 0
+
+
 def prefill_launches(b, decode: bool, num_sms: int = 152) -> int:
     """Launches of the chunked-prefill kernel in one call: one, except for the two-tile kernel
-    beside decode rows, which goes as launches of one wave (num_sms CTAs) each over its items
+    beside decode rows, which may go as launches of prefill_slice_ctas CTAs each over its items
     (pairs of 128-row Q tiles x kv heads x prefill sequences)."""
     if b.max_query_len <= 1 or verify_path(b):
         return 0
     group = b.num_q_heads // b.num_kv_heads
     if b.max_query_len <= 128 // group or not decode:
         return 1
+    per = prefill_slice_ctas(b, num_sms)
+    if per == 0:
+        return 1
     items = -(-b.max_query_len // (2 * (128 // group))) * b.num_kv_heads * b.num_prefill_seqs
-    return -(-items // num_sms)
+    return -(-items // per)
 
 
 def launches_per_step(b, sp: int = 0, num_sms: int = 152) -> int:

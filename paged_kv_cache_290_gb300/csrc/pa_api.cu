@@ -110,11 +110,26 @@ cudaError_t side_stream(SideStream** out) {
   return cudaSuccess;
 }
 
-// CTAs per launch of the two-tile prefill kernel when it runs beside the decode kernel: one
-// wave.  (Measured on the 4 x 512 + 128-decode step: slices of one wave 459 us, one full grid
-// 475 us; smaller slices leave the prefill kernel a long serial chain of short launches,
-// 602 us at half the SMs, 889 us at 40.)
-int prefill_ctas_beside_decode(int num_sms) { return num_sms; }
+// CTAs per launch of the two-tile prefill kernel beside the decode kernel (0: one full grid).
+// The prefill launches hold whole SMs; the decode kernel streams on the rest.  When the decode
+// rows carry at least about as much SM time as the prefill rows, the prefill goes as launches of
+// two thirds of the SMs (the decode kernel keeps a third from the start); otherwise as one full
+// grid.  The estimate: decode over prefill SM time ~ (decode rows / prefill rows) / G x 70 for
+// contexts of similar length (one decode row moves Hkv d 4 bytes per key at ~75 GB/s per SM; one
+// prefill row does 4 Hq d flops per key at ~5.3 TFLOP/s per SM), halved over an FP8 pool.
+// Measured on the 4 x 512-row + 128-decode step (estimate 1.1; FP8 0.55), steps in us:
+//   CTAs per launch    152    136    120    104    96     88     80     64     full grid
+//   fp16 (bs 16)       447.6  454.2  441.6  424.5  425.3  431.0  562.9  493.9  458.9
+//   FP8 pool           379.7                482.1         471.3  610.0  528.2  371.6
+// Four or more launches in a row (80 CTAs and fewer here) chain the slowest CTA of each.  With
+// 8 decode rows (estimate 0.07) one full grid takes 232.0 us against 275.0 in launches of 152.
+int prefill_ctas_beside_decode(int num_sms, int64_t decode_rows, int64_t prefill_rows,
+                               int group, bool fp8) {
+  const double r = static_cast<double>(decode_rows) /
+                   static_cast<double>(std::max<int64_t>(prefill_rows, 1)) / group * 70.0 *
+                   (fp8 ? 0.5 : 1.0);
+  return r >= 0.8 ? num_sms * 2 / 3 : 0;
+}
 
 // SM count of the current device (looked up once per device).
 cudaError_t device_sm_count(int* out) {
@@ -532,7 +547,9 @@ static int attention_impl(const pa_tensor* q, const pa_tensor* k_cache, const pa
   } join;
   if (!all_prefill && !verify && hint->max_query_len > 1) {
     if ((e = device_sm_count(&a.num_sms)) != cudaSuccess) return cuda_fail(e, "device attribute");
-    a.prefill_ctas = prefill_ctas_beside_decode(a.num_sms);
+    const int64_t decode_rows = n - a.prefill_seqs;
+    a.prefill_ctas = prefill_ctas_beside_decode(a.num_sms, decode_rows, t - decode_rows, a.group,
+                                                fp8);
     SideStream* side = nullptr;
     if ((e = side_stream(&side)) != cudaSuccess) return cuda_fail(e, "side stream");
     if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess ||

@@ -69,11 +69,21 @@ def test_mixed_step_counts_prefill_launch():
     b = small_mixed()
     assert bench.launches_per_step(b) == 4
     # the full mixed step: 4 chunks x 8 pairs of 32-token Q tiles x 8 kv heads = 256 items of
-    # the two-tile kernel, which beside decode rows go as launches of one wave (152 + 104)
+    # the two-tile kernel; its 128 decode rows weigh about as much as the 2048 prefill rows
+    # (estimate 128 / 2048 / 4 x 70 = 1.1), so the items go as launches of two thirds of the
+    # SMs (101 + 101 + 54)
     m = W.mixed_step(16, keep_contiguous=False, keep_pre=False)
-    assert bench.prefill_launches(m, decode=True) == 2
-    assert bench.launches_per_step(m) == 5
-    assert bench.launches_per_step(m, num_sms=256) == 4
+    assert bench.prefill_slice_ctas(m) == 101
+    assert bench.prefill_launches(m, decode=True) == 3
+    assert bench.launches_per_step(m) == 6
+    assert bench.launches_per_step(m, num_sms=256) == 5
+    # over an FP8 pool the decode rows weigh half as much (0.55): one full grid
+    f8 = W.to_fp8(m)
+    assert bench.prefill_slice_ctas(f8) == 0
+    assert bench.prefill_launches(f8, decode=True) == 1
+    # eight decode rows beside the chunks: one full grid
+    m8 = W.mixed_step(16, num_decode=8, keep_contiguous=False, keep_pre=False)
+    assert bench.prefill_launches(m8, decode=True) == 1
     # alone (no decode rows) it is one full grid
     assert bench.prefill_launches(W.mixed_step(16, num_decode=0, keep_contiguous=False,
                                                keep_pre=False), decode=False) == 1
