@@ -523,7 +523,15 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a)
   constexpr int V = D / 32;   // output elements per lane
   constexpr int kBatch = 16;  // partitions whose O rows are in flight at once
   constexpr int kHeld = 2;    // m and l of partitions lane, lane + 32 held in registers
+  // A shared-prefix CTA that covered several prefix partitions wrote its partial to the first
+  // one's slot; the others hold nothing and weigh nothing.
+  auto unused = [&](int p) { return p < a.cascade_parts && p % a.cascade_span != 0; };
   auto load_o = [&](int p, float (&x)[V]) {
+    if (unused(p)) {
+#pragma unroll
+      for (int e = 0; e < V; ++e) x[e] = 0.f;
+      return;
+    }
     const float* op = a.part_o + (base + p) * D + lane * V;
     if constexpr (V == 4) {
       const float4 t = *reinterpret_cast<const float4*>(op);
@@ -537,15 +545,16 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a)
 #pragma unroll
   for (int k = 0; k < kHeld; ++k) {
     const int p = lane + 32 * k;
-    mh[k] = p < nparts ? a.part_m[base + p] : -INFINITY;
-    lh[k] = p < nparts ? a.part_l[base + p] : 0.f;
+    mh[k] = p < nparts && !unused(p) ? a.part_m[base + p] : -INFINITY;
+    lh[k] = p < nparts && !unused(p) ? a.part_l[base + p] : 0.f;
   }
   float x[kBatch][V];
 #pragma unroll
   for (int j = 0; j < kBatch; ++j)
     if (j < nparts) load_o(j, x[j]);
   float M = -INFINITY;
-  for (int p = lane + 32 * kHeld; p < nparts; p += 32) M = fmaxf(M, a.part_m[base + p]);
+  for (int p = lane + 32 * kHeld; p < nparts; p += 32)
+    if (!unused(p)) M = fmaxf(M, a.part_m[base + p]);
 #pragma unroll
   for (int k = 0; k < kHeld; ++k) M = fmaxf(M, mh[k]);
 #pragma unroll
@@ -577,7 +586,7 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const AttnArgs a)
           for (int k = 1; k < kHeld; ++k) src = (p >> 5) == k ? wh[k] : src;
           wj = __shfl_sync(0xffffffffu, src, p & 31);
         } else {  // past 32 * kHeld partitions: read m and l again (the same address in every lane)
-          wj = exp2f(a.part_m[base + p] - M) * a.part_l[base + p];
+          wj = unused(p) ? 0.f : exp2f(a.part_m[base + p] - M) * a.part_l[base + p];
         }
         wsum += wj;
 #pragma unroll

@@ -58,6 +58,8 @@ struct AttnArgs {
   int kv_fp8;        // 1: the pools hold E4M3 codes
   int bf16;          // 1: q, out and the pools are bfloat16 (else fp16)
   int cascade_parts; // leading 512-key partitions every sequence shares (attended once for all)
+  int cascade_span;  // prefix partitions one shared-prefix CTA covers (their partial goes to the
+                     //   first one's slot; the merge skips the others)
   int num_sms;       // SMs of the device (launch-shape choices)
   int verify_rows;   // the decode kernel and its merge serve sequences with 1 .. verify_rows
                      //   query rows (1: decode rows only)

@@ -402,14 +402,11 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     qt = blockIdx.x;
     row0 = 0;
     q_len = static_cast<int>(a.num_tokens);
-    key_base = blockIdx.z * kPartitionTokens;
+    key_base = blockIdx.z * a.cascade_span * kPartitionTokens;
     ctx = 0;  // unused: no causal mask inside the shared prefix
-    kend = key_base + kPartitionTokens;
-    ntiles = kPartitionTokens / C::kKeys;
-    if (qt * C::kQTiles * tile_q >= q_len) {
-      grid_dependency_wait();
-      return;
-    }
+    kend = key_base + a.cascade_span * kPartitionTokens;
+    ntiles = a.cascade_span * kPartitionTokens / C::kKeys;
+    if (qt * C::kQTiles * tile_q >= q_len) return;
 #pragma unroll
     for (int t = 0; t < C::kQTiles; ++t)
       tiles[t] = qt * C::kQTiles * tile_q + t * tile_q < q_len ? ntiles : 0;
@@ -455,7 +452,6 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0) atomicOr(a.err, kErrBlockRange);
-    if constexpr (CASCADE) grid_dependency_wait();
     return;
   }
 
@@ -766,7 +762,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       if constexpr (CASCADE) {
         const int64_t pidx =
             (static_cast<int64_t>(row0 + tok) * a.num_q_heads + g * a.group + hg) * a.max_parts +
-            blockIdx.z;
+            blockIdx.z * a.cascade_span;
         if (rv && h == 0) {
           a.part_m[pidx] = m_run;
           a.part_l[pidx] = l_all;
@@ -817,10 +813,6 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(C::kTmemCols)
                  : "memory");
-  // The shared-prefix pass may start while the decode kernel before it is still running (it
-  // reads nothing that kernel writes); it must not finish first, since the merge after it waits
-  // only on this grid and reads the decode kernel's partials too.
-  if constexpr (CASCADE) grid_dependency_wait();
 }
 
 template <int D, bool F8 = false>
@@ -886,13 +878,10 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     row0 = 0;
     q_len = static_cast<int>(a.num_tokens);
     ctx = 0;  // unused: no causal mask inside the shared prefix
-    key_base = blockIdx.z * kPartitionTokens;
-    kend = key_base + kPartitionTokens;
-    ntiles = kPartitionTokens / C::kKeys;
-    if (qt * tile_q >= q_len) {
-      grid_dependency_wait();
-      return;
-    }
+    key_base = blockIdx.z * a.cascade_span * kPartitionTokens;
+    kend = key_base + a.cascade_span * kPartitionTokens;
+    ntiles = a.cascade_span * kPartitionTokens / C::kKeys;
+    if (qt * tile_q >= q_len) return;
   } else {
     // Later q tiles of a chunk see more keys, and longer sequences more tiles: dispatch them
     // first so the grid's tail is short.
@@ -930,7 +919,6 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0) atomicOr(a.err, kErrBlockRange);
-    if constexpr (CASCADE) grid_dependency_wait();
     return;
   }
 
@@ -1202,7 +1190,7 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
       // of O / l.
       tmem_fence_after_sync();
       const int64_t pidx = (static_cast<int64_t>(qbase + qi) * a.num_q_heads + g * a.group + hg) *
-                               a.max_parts + blockIdx.z;
+                               a.max_parts + blockIdx.z * a.cascade_span;
       if (rv && par == 0) {
         a.part_m[pidx] = mm;
         a.part_l[pidx] = l_all;
@@ -1265,7 +1253,6 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(C::kTmemCols)
                  : "memory");
-  if constexpr (CASCADE) grid_dependency_wait();  // see the pair kernel
 }
 
 // Both kernels share the launch shape rules: 384 threads, one CTA per SM (TMEM and shared
@@ -1303,25 +1290,11 @@ cudaError_t launch_one(K kern, const AttnArgs& a, const CUtensorMap& kmap, const
     }
     return cudaSuccess;
   }
-  if (!cascade) {
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
-    return cudaGetLastError();
-  }
-  // The shared-prefix pass: every query row of the batch, every kv head, every prefix
-  // partition; a programmatic dependent of the decode kernel, so its CTAs take SMs as the
-  // decode grid drains.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((a.num_tokens + rows_q - 1) / rows_q),
-                     a.num_kv_heads, a.cascade_parts);
-  cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
+  if (cascade)  // every query row of the batch, every kv head, every group of prefix partitions
+    grid = dim3(static_cast<unsigned>((a.num_tokens + rows_q - 1) / rows_q), a.num_kv_heads,
+                a.cascade_parts / a.cascade_span);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, a);
+  return cudaGetLastError();
 }
 
 // Chunks that fit one Q tile (speculative verify, short chunks) go to the parity kernel, which
@@ -1345,7 +1318,7 @@ cudaError_t launch_cascade_t(const AttnArgs& a, const CUtensorMap& kmap, const C
                              cudaStream_t stream) {
   const int64_t rows_pair = PairCfg<D>::kQTiles * (PairCfg<D>::kRows / a.group);
   const int64_t pair_ctas = (a.num_tokens + rows_pair - 1) / rows_pair * a.num_kv_heads *
-                            a.cascade_parts;
+                            (a.cascade_parts / a.cascade_span);
   if (pair_ctas < a.num_sms)
     return launch_one<ParityCfg<D, F8>>(prefill_parity_kernel<D, BS, true, BF, F8>, a, kmap,
                                         vmap, 1, stream, true);

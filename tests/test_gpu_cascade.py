@@ -70,8 +70,9 @@ def oracle_of(b):
 
 # (rows, prefix, d, bs, q heads, kv heads): Q tiles of 128 // G tokens, so each case spans
 # several CTAs with a ragged last one; G = 12 leaves 8 padding rows in every tile.  Small grids
-# run one Q tile per CTA; the last case's grid (640 rows, 2 Q tiles of 16 per CTA, 8 kv heads:
-# 160 CTAs) fills the GPU and runs on the two-Q-tile kernel.
+# run one Q tile per CTA; the last cases' grids (640 rows, 2 Q tiles of 16 per CTA, 8 kv heads:
+# 160 CTAs) fill the GPU and run on the two-Q-tile kernel.  An even number of prefix partitions
+# goes two per CTA (the merge skips the second's slot); an odd one, one per CTA.
 CASES = {
     "g7_d128_bs16_p512": (40, 512, 128, 16, 28, 4),
     "g4_d128_bs32_p1024": (70, 1024, 128, 32, 32, 8),
@@ -80,6 +81,7 @@ CASES = {
     "g16_d128_bs16_p512": (12, 512, 128, 16, 32, 2),
     "g12_d128_bs32_p2048": (25, 2048, 128, 32, 24, 2),
     "pair_g8_d128_bs16_p512": (640, 512, 128, 16, 64, 8),
+    "pair_g8_d128_bs16_p1024": (640, 1024, 128, 16, 64, 8),
 }
 
 
@@ -101,7 +103,7 @@ def test_shared_prefix_pass_matches_oracle(name):
     assert_close(plain, ref)
 
 
-@pytest.mark.parametrize("name", ["g7_d128_bs16_p512", "g8_d64_bs16_p512"])
+@pytest.mark.parametrize("name", ["g7_d128_bs16_p512", "g8_d64_bs16_p512", "g4_d128_bs32_p1024"])
 def test_shared_prefix_pass_over_fp8(name):
     """Over an FP8 pool the pass widens the prefix's codes into fp16 in shared memory."""
     n, prefix, d, bs, hq, hkv = CASES[name]
