@@ -353,9 +353,10 @@ struct PairCfg {
 };
 
 // CASCADE: the shared-prefix pass.  Rows are every query row of the batch (all decode rows,
-// row i of q), keys are the 512-key partition blockIdx.z of the prefix that every sequence
-// shares (read through sequence 0's table), no causal mask; the epilogue writes the rows'
-// partition partials (m, l, O / l) for the log-sum-exp merge instead of the output.
+// row i of q), keys are the cascade_span 512-key partitions blockIdx.z * cascade_span .. of the
+// prefix that every sequence shares (read through sequence 0's table), no causal mask; the
+// epilogue writes the rows' partials (m, l, O / l) for the log-sum-exp merge into the slot of
+// the first of those partitions instead of the output.
 template <int D, int BS, bool CASCADE, bool BF, bool F8>
 __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -747,7 +748,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     }
 
     // Epilogue: O_t / l -> out (fp16, rows of real query tokens only); the shared-prefix pass
-    // writes the rows' partials of partition blockIdx.z instead: m (log2 units), l and O / l.
+    // writes the rows' partials of its prefix partitions instead: m (log2 units), l and O / l.
     // The two halves' sums are traded through the Q tile's shared memory, which no MMA reads
     // once `drain` has completed.
     bool ok = !stopped && my_tiles > 0;
@@ -844,7 +845,7 @@ struct ParityCfg {
 };
 
 // CASCADE: the shared-prefix pass, as in the pair kernel (rows: every query row of the batch;
-// keys: prefix partition blockIdx.z through sequence 0's table; partials out).
+// keys: prefix partitions blockIdx.z * cascade_span .. through sequence 0's table; partials out).
 template <int D, int BS, bool CASCADE, bool BF, bool F8>
 __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     prefill_parity_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -1186,8 +1187,8 @@ __global__ void __launch_bounds__(ParityCfg<D>::kThreads, 1)
     bool ok = !*reinterpret_cast<volatile int*>(&softmax_stop);
     if (ok) ok = mbar_wait(smem_addr(&drain), 0, a.err, a.wait_limit_ns);
     if (CASCADE && !__any_sync(0xffffffffu, !ok)) {
-      // The rows' partials of partition blockIdx.z: m (log2 units), l, and this thread's half
-      // of O / l.
+      // The rows' partials of the CTA's prefix partitions: m (log2 units), l, and this thread's
+      // half of O / l.
       tmem_fence_after_sync();
       const int64_t pidx = (static_cast<int64_t>(qbase + qi) * a.num_q_heads + g * a.group + hg) *
                                a.max_parts + blockIdx.z * a.cascade_span;
