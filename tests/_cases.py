@@ -5,6 +5,8 @@ second, yet they span several key blocks, several 512-token partitions, ragged p
 (query lengths that are not multiples of any tile), block tails, GQA groups of 1, 2, 4, 7 and 8
 and both block sizes.
 """
+import torch
+
 from paged_kv_cache_290_gb300.workloads import SeqSpec, build_batch
 
 
@@ -36,6 +38,16 @@ def small_prefix(seed=9300, n=6, prefix=64, d=128, bs=16):
     return build_batch("small_prefix", [SeqSpec(L, 1) for L in lens], num_q_heads=28,
                        num_kv_heads=4, head_dim=d, block_size=bs, seed_base=seed,
                        shared_prefix_len=prefix)
+
+
+def small_shared(seed=9600, n=24, prefix=1024, d=128, bs=16, hq=28, hkv=4):
+    """n decode rows behind a shared prefix of `prefix` keys (two 512-key partitions, attended
+    once by the shared-prefix pass), private continuations of 1 to 700 keys."""
+    g = torch.Generator().manual_seed(seed)
+    priv = torch.randint(1, 701, (n,), generator=g).tolist()
+    return build_batch(f"small_shared_{n}x{prefix}", [SeqSpec(prefix + p, 1) for p in priv],
+                       num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                       seed_base=seed, shared_prefix_len=prefix)
 
 
 def small_spec(d=128, bs=16, hq=32, hkv=4, seed=9400):

@@ -153,14 +153,16 @@ def test_block_manager_drives_a_serving_loop():
     srv.step({6: 73 - 64, 1: 1})
 
 
-@pytest.mark.parametrize("make", ["mixed", "decode"])
+@pytest.mark.parametrize("make", ["mixed", "decode", "shared"])
 def test_step_replays_in_a_cuda_graph(make):
     """A serving step (scatter-write, then attention) captured once in a CUDA graph and
-    replayed: the mixed step forks the prefill launch onto the library's side stream and joins
-    it back with events, which a capture records as a fork and a join.  The replay must give
-    the oracle's result, like an eager call."""
-    from _cases import small_decode, small_mixed
-    b = small_mixed(seed=9250) if make == "mixed" else small_decode(seed=9251)
+    replayed: the mixed step forks the prefill launch, the shared-prefix step its pass, onto the
+    library's side stream and joins it back with events, which a capture records as a fork and a
+    join.  The replay must give the oracle's result, like an eager call."""
+    from _cases import small_decode, small_mixed, small_shared
+    b = (small_mixed(seed=9250) if make == "mixed" else
+         small_shared(seed=9252) if make == "shared" else small_decode(seed=9251))
+    sp = b.meta.get("shared_prefix_len", 0) if make == "shared" else 0
     dev = "cuda"
     kc, vc = b.k_cache_pre.to(dev), b.v_cache_pre.to(dev)
     k_new, v_new, slots = b.k_new.to(dev), b.v_new.to(dev), b.slot_mapping.to(dev)
@@ -173,7 +175,7 @@ def test_step_replays_in_a_cuda_graph(make):
     def step():
         pa.reshape_and_cache(k_new, v_new, kc, vc, slots)
         pa.attention(q, kc, vc, bt, sl, qsl, b.scale, out, b.max_query_len, b.max_seq_len,
-                     workspace=ws, num_prefill_seqs=b.num_prefill_seqs)
+                     workspace=ws, num_prefill_seqs=b.num_prefill_seqs, shared_prefix_tokens=sp)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
