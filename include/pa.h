@@ -155,8 +155,11 @@ size_t pa_attention_workspace_size(int64_t num_tokens, int64_t num_q_heads, int6
  * Rows with q_len = 1 and more than 512 keys are computed in 512-key partitions merged with
  * the log-sum-exp rule; so are verify rows (every sequence with at most a few rows: q_len x G
  * <= 8, or <= 32 over an FP8 cache), each with its own causal limit.  Longer chunks run on the
- * tensor-core prefill kernels, beside the decode work when the call has both (a side stream of
- * the library's, forked from and joined back into `stream` with events).
+ * tensor-core prefill kernels, beside the decode work when the call has both; the
+ * shared-prefix pass (hint->shared_prefix_tokens) runs beside the decode kernel too.  Both use
+ * a side stream of the library's (one per device and host thread, created by the first such
+ * call), forked from and joined back into `stream` with events, so a capture of the call into a
+ * CUDA graph records the fork and the join.
  * Supported: d in {64, 128}, bs in {16, 32}, Hq / Hkv in 1..16.
  */
 int pa_attention(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
