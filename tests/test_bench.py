@@ -245,3 +245,22 @@ def test_clock_sampler_counts_samples_in_the_soak_window():
     assert r["samples"] == 4 and r["samples_under_load"] == 2
     assert r["sm_mhz"] == 1990.0 and r["sm_mhz_under_load_median"] == 1990.0
     assert r["reasons"] == ["sw_power_cap"]
+
+
+def test_dominant_kernel_is_the_longest_at_its_roof():
+    """The step's roofline names the kernel whose own work takes longest at its roof, not the one
+    with the longest (possibly overlapping) event interval."""
+    peaks = {"hbm_gbs": 6786.9, "tflops": 1876.8, "hbm_src": "m", "tflops_src": "m"}
+    nbytes = {"decode_kernel_bytes": 2_153_076_204, "prefill_kernel": "prefill_pair_kernel",
+              "prefill_kernel_bytes": 120_973_572, "prefill_kernel_flops": 170_448_125_952}
+    # the prefill's interval (beside the decode kernel) is the longer one
+    k = bench.kernel_rooflines(nbytes, {"decode": 0.4073, "prefill": 0.4183}, peaks)
+    assert k["decode"]["bound"] == "hbm" and k["prefill"]["bound"] == "tensor"
+    assert bench.dominant_kernel(k) == "decode"
+    # alone, the prefill kernel is the step's only kernel
+    k = bench.kernel_rooflines(nbytes, {"prefill": 0.2101}, peaks)
+    assert bench.dominant_kernel(k) == "prefill"
+    # a small decode beside heavy prefill work: the prefill bounds the step
+    nbytes_small = dict(nbytes, decode_kernel_bytes=50_000_000)
+    k = bench.kernel_rooflines(nbytes_small, {"decode": 0.16, "prefill": 0.22}, peaks)
+    assert bench.dominant_kernel(k) == "prefill"
