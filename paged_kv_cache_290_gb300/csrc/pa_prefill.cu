@@ -17,14 +17,14 @@
 // prefill_pair_kernel: work item = one CTA = (two Q tiles, kv head g, prefill sequence).  A Q
 // tile is 128 rows, each a (query token, head of the GQA group) pair, so one K/V tile serves
 // every head of the group, and every K/V tile the CTA loads serves both Q tiles (256 rows).
-// Warp roles:
-//   * producers (warps 8 and 9): stream 128-key K and V tiles (8 units of 16 tokens gathered
+// 640 threads; warp roles:
+//   * producers (warps 16 and 17): stream 128-key K and V tiles (8 units of 16 tokens gathered
 //     through the block table, 128-byte-swizzled TMA boxes) into a 2-stage K ring and a 3-stage
 //     V ring; a K stage is released once both S = Q K^T products that read it are done, a V
 //     stage as soon as both P V products are (before the next S is issued).  The next tile's
 //     block ids are read while a producer waits for its stage, and the MMA issuer waits for
 //     K_{j+1} only right before S(j+1),
-//   * MMA issuer (lane 0 of warp 10): per Q tile t, S_t = Q_t K_j^T into TMEM buffer t (M 128,
+//   * MMA issuer (lane 0 of warp 18): per Q tile t, S_t = Q_t K_j^T into TMEM buffer t (M 128,
 //     N 128, K d, both operands K-major from shared memory) and O_t += P_t V_j with P_t read
 //     from TMEM (it overwrites the first 64 columns of S_t's buffer, two fp16 per column) and
 //     V_j MN-major from shared memory.  Issue order S_A(0), S_B(0), then per key tile j:
@@ -33,11 +33,14 @@
 //     order, S_t(j+1) never overwrites P_t(j) before P_t V_j has read it.  Issuing an MMA
 //     waits until the pipe takes it, so this thread runs alone and never joins a warp
 //     collective (that would idle the pipe),
-//   * softmax: warpgroup t (warps 4t .. 4t+3) owns Q tile t, one thread per row (TMEM lane), all
-//     128 columns of a key tile: online softmax in base 2 with scale * log2(e) folded into the
-//     exponent.  The running max is only raised (and O_t rescaled in TMEM) when it grows by more
-//     than 8 in log2 units, which keeps P <= 256 in fp16.  S_t(j)'s completion implies
-//     P_t V_{j-1} is done (it was issued after it), so no softmax step waits on a P V.
+//   * softmax (warps 0 .. 15): two warpgroups per Q tile t (warps 8t .. 8t+7), one per half of
+//     each key tile's columns and of O's columns, a thread per (row, half); the two halves of a
+//     row trade their maxima once per key tile through a named barrier.  Online softmax in base
+//     2 with scale * log2(e) folded into the exponent, on packed fp32 pairs.  The running max is
+//     only raised (and O_t rescaled in TMEM) when it grows by more than 8 in log2 units, which
+//     keeps P <= 256 in fp16.  S_t(j)'s completion implies P_t V_{j-1} is done (it was issued
+//     after it), so no softmax step waits on a P V,
+//   * warp 19 widens half of each tile's E4M3 codes over an FP8 pool (d 128), else idles.
 // V rows past the last visible key of the chunk are zeroed in shared memory before the first
 // P V product of the last key tile (0 * NaN would poison the sum).  Every wait is bounded.
 // A bfloat16 batch (q, pools and out bf16) runs the same kernels with bf16 operands in both
@@ -578,7 +581,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     // ============================================================== FP8 widening helper
     widen_helper_f8<D, C::kKeys>(a, kend, ntiles, key_base, C::kKStages, C::kVStages, k_s, v_s,
                                  k_full, v_full, land);
-  }  // lanes 1-31 of warp 10 have no role (warp 11 neither, unless it helps widen FP8 tiles)
+  }  // lanes 1-31 of warp 18 have no role (warp 19 neither, unless it helps widen FP8 tiles)
   } else {
     // ============================================================== softmax warps 0-15
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
